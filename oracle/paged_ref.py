@@ -65,12 +65,13 @@ def cache_write(cache_bits: np.ndarray, rows_bits: np.ndarray, slot_mapping) -> 
 # Gather through block_table
 # --------------------------------------------------------------------------
 def gather_sequence(cache: np.ndarray, table_row, length: int, block_size: int) -> np.ndarray:
-    """Contiguous [length, ...] copy of one sequence's rows: row pos comes from
-    cache[table_row[pos // bs], pos % bs]."""
+    """Contiguous [length, ...] float64 copy of one sequence's rows: row pos comes
+    from cache[table_row[pos // bs], pos % bs]. A uint16 cache holds bf16 bit
+    patterns and is widened exactly after the gather."""
     out = np.empty((length,) + cache.shape[2:], dtype=cache.dtype)
     for pos in range(length):
         out[pos] = cache[int(table_row[pos // block_size]), pos % block_size]
-    return out
+    return bf16_bits_to_f64(out) if out.dtype == np.uint16 else out.astype(np.float64)
 
 
 # --------------------------------------------------------------------------
@@ -90,7 +91,9 @@ def softmax_combine(z: np.ndarray, V: np.ndarray, visible: np.ndarray):
     e = np.exp(z - m)
     l = e.sum()
     p = e / l
-    return p @ V, m + np.log(l), p
+    # o = sum over the visible keys only; masked rows (e.g. expired positions whose
+    # table entry is the null block) never enter the sum, whatever they hold.
+    return p[visible] @ V[visible], m + np.log(l), p
 
 
 def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, visible: np.ndarray, scale: float):
@@ -106,7 +109,8 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, block_size: int, sc
     """Decode attention for each (b, h): the query sees positions
     [max(0, len_b - W), len_b) of its sequence (all of [0, len_b) when W = 0).
 
-    q [B, H, d] float64; caches [nb, bs, H_kv, d] float64; returns o [B, H, d] and
+    q [B, H, d] float64; caches [nb, bs, H_kv, d] float64 or bf16 bits (uint16);
+    returns o [B, H, d] and
     lse [B, H] (rows not in ``batch_indices`` stay NaN).
     """
     B, H, _ = q.shape

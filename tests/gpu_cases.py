@@ -1,0 +1,100 @@
+"""Shared set-up of GPU parity cases: draw inputs, build tables with the library's
+host generator (checked against the oracle's), write through the CUDA path and
+through the oracle, and compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import synth
+from oracle import block_pool_ref as bp
+from oracle import paged_ref as ref
+from paged_kv_cache_77_gb300 import api
+
+MAX_ABS_TOL = 1e-2  # attention outputs from bf16 inputs vs the fp64 oracle
+MEAN_ABS_TOL = 1e-3
+LSE_TOL = 2e-3
+
+
+def tables(wl: synth.Workload, d: synth.Draw):
+    """Library block table + slot mapping, asserted equal to the oracle's."""
+    if wl.layout == "arange":
+        table = api.build_block_table_arange(wl.batch, d.max_blocks_per_seq)
+        ref_table = bp.block_table_arange(wl.batch, d.max_blocks_per_seq)
+    else:
+        table = api.BlockPool(d.num_blocks, d.pool_order).build_block_table(
+            d.seq_lens, wl.block_size, wl.window, d.max_blocks_per_seq)
+        ref_table = bp.prepare_block_tables(bp.BlockPool(d.num_blocks, d.pool_order), d.seq_lens,
+                                            wl.block_size, wl.window, d.max_blocks_per_seq)
+    assert np.array_equal(table, ref_table)
+    slots = api.build_slot_mapping(table, d.start_pos, d.num_new, wl.block_size)
+    assert np.array_equal(slots, bp.slot_mapping(ref_table, d.start_pos, d.num_new, wl.block_size))
+    return table, slots
+
+
+class DecodeCase:
+    """One decode instance on the GPU plus the oracle's view of the same bytes."""
+
+    def __init__(self, wl: synth.Workload, d: synth.Draw | None = None, poison: bool = True):
+        self.wl = wl
+        self.d = d if d is not None else synth.draw(wl)
+        self.v = synth.values(wl, self.d, "cuda", poison_null=poison)
+        self.table_np, self.slots_np = tables(wl, self.d)
+        self.table = torch.from_numpy(self.table_np).cuda()
+        self.slots = torch.from_numpy(self.slots_np).cuda()
+        self.seq_lens = torch.from_numpy(self.d.seq_lens).cuda()
+        names = ("cache_nope", "cache_rope") if wl.kind == "mla_decode" else ("k_cache", "v_cache")
+        # Host copies taken before the CUDA write: the oracle writes its own.
+        self.pre = {n: synth.bf16_bits(self.v[n]) for n in names}
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def gpu_write(self):
+        if self.wl.kind == "mla_decode":
+            api.kv_cache_write(self.v["cache_nope"], self.v["cache_rope"], self.v["nope_new"],
+                               self.v["rope_new"], self.slots, dev_status=self.status)
+        else:
+            api.kv_cache_write(self.v["k_cache"], self.v["v_cache"], self.v["k_new"],
+                               self.v["v_new"], self.slots, dev_status=self.status)
+
+    def oracle_write(self):
+        if self.wl.kind == "mla_decode":
+            pairs = (("cache_nope", "nope_new"), ("cache_rope", "rope_new"))
+        else:
+            pairs = (("k_cache", "k_new"), ("v_cache", "v_new"))
+        self.post = {c: ref.cache_write(self.pre[c], synth.bf16_bits(self.v[r]), self.slots_np)
+                     for c, r in pairs}
+
+    def check_write_bit_exact(self):
+        for name, expect in self.post.items():
+            got = synth.bf16_bits(self.v[name])
+            assert np.array_equal(got, expect), f"{name} differs from the oracle's write"
+        assert int(self.status.item()) == 0
+
+
+def compare(out: torch.Tensor, lse: torch.Tensor | None, o_ref: np.ndarray, lse_ref: np.ndarray,
+            rows, what: str):
+    """Max / mean abs error on the selected leading-index rows."""
+    got = out.float().cpu().numpy()[rows]
+    exp = o_ref[rows]
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - exp)
+    assert err.max() <= MAX_ABS_TOL, f"{what}: max abs err {err.max():.3e}"
+    assert err.mean() <= MEAN_ABS_TOL, f"{what}: mean abs err {err.mean():.3e}"
+    if lse is not None:
+        lg = lse.cpu().numpy()[rows]
+        le = lse_ref[rows]
+        fin = np.isfinite(le)
+        assert np.array_equal(np.isfinite(lg), fin)
+        assert np.abs(lg[fin] - le[fin]).max(initial=0) <= LSE_TOL, f"{what}: lse"
+    return float(err.max()), float(err.mean())
+
+
+def sample_rows(seq_lens: np.ndarray, k: int, seed: int) -> list[int]:
+    """The longest and shortest sequences plus k random others."""
+    B = len(seq_lens)
+    if B <= k + 2:
+        return list(range(B))
+    rng = np.random.default_rng(seed)
+    pick = {int(np.argmax(seq_lens)), int(np.argmin(seq_lens))}
+    pick |= set(int(x) for x in rng.choice(B, size=k, replace=False))
+    return sorted(pick)

@@ -262,3 +262,18 @@ def test_mla_rope_term_contributes():
     rope[0, :, 0, 0] = [0.0, 0.0, 0.0, 50.0]
     o, _ = ref.mla_decode(np.zeros((1, 1, 2)), np.ones((1, 1, 1)), nope, rope, table, [4], bs, 1.0)
     assert o[0, 0, 0] == pytest.approx(40.0, abs=1e-12)
+
+
+def test_masked_rows_never_contribute_even_if_nan():
+    # The null block holds no real data; rows outside the visible set must not
+    # reach the output even when they are NaN.
+    rng = np.random.default_rng(12)
+    K, V = _rand(rng, 6, 4), _rand(rng, 6, 3)
+    K[:2] = np.nan
+    V[:2] = np.nan
+    vis = np.array([False, False, True, True, True, True])
+    o, lse, _ = ref.attend(_rand(rng, 4), K, V, vis, 0.5)
+    assert np.isfinite(o).all() and np.isfinite(lse)
+    o2, lse2, _ = ref.attend(np.zeros(4), K[2:], V[2:], vis[2:], 0.5)
+    o3, _, _ = ref.attend(np.zeros(4), K, V, vis, 0.5)
+    assert np.allclose(o3, o2) and np.allclose(o3, V[2:].mean(axis=0))
