@@ -1,0 +1,396 @@
+"""Benchmark of the paged KV cache hot path on one GB300 (or N replicas).
+
+One step = the whole decode hot path over one batch: the slot_mapping write of the
+new K/V rows (kv_cache_write) followed by paged decode attention (split-KV
+attention + LSE merge). Inputs are synthetic (synth/), resident in HBM; the KV
+cache of the default workload (4.3 GB) is far larger than the 129 MB L2, so no L2
+flush is needed between steps.
+
+Prints one JSON line (rank 0). Usage:
+  python bench.py [--gpus N --steps K --warmup W] [--workload gqa_long|swa|mha_tiny]
+  python bench.py --impl reference ...   # the fp64 CPU oracle as the reference arm
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+if "--impl" in sys.argv and "reference" in sys.argv or "--cpu-baseline-child" in sys.argv:
+    # The oracle timing runs single-threaded; pin BLAS before numpy loads.
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "paged-KV decode attention: achieved HBM GB/s (% of peak), seq-steps/s"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------- byte accounting
+def decode_bytes(wl: synth.Workload, d: synth.Draw, out_bytes: int = 2) -> dict:
+    """Algorithmic bytes of one decode step (visible keys only, no block overread)."""
+    lens = d.seq_lens.astype(np.int64)
+    vis = np.minimum(lens, wl.window) if wl.window > 0 else lens
+    row = wl.num_kv_heads * wl.head_dim * 2  # bytes of one token's K (or V) row
+    kv = int(vis.sum()) * row * 2
+    nblk = -(-lens // wl.block_size)
+    live = nblk - (np.maximum(lens - wl.window, 0) // wl.block_size if wl.window > 0 else 0)
+    qo = wl.batch * wl.num_heads * wl.head_dim * (2 + out_bytes)
+    meta = int(live.sum()) * 4 + wl.batch * 4
+    attn = kv + qo + meta
+    new_rows = int(d.num_new.sum())
+    write = new_rows * row * 2 * 2 + new_rows * 4  # read + write K and V rows, slots
+    return {"attention": attn, "write": write, "step": attn + write, "kv": kv}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        # Samples under load: the upper half of the observed clocks (the sampler
+        # also sees the ramp before and after the timed region).
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle timing
+def oracle_sample_step(wl, d, vals, seqs):
+    """One oracle pass (write + decode) over the sequences `seqs` of a sub-instance."""
+    from oracle import paged_ref as ref
+
+    post_k = ref.cache_write(vals["k_cache"], vals["k_new"], vals["slots"])
+    post_v = ref.cache_write(vals["v_cache"], vals["v_new"], vals["slots"])
+    ref.paged_decode(vals["q"], post_k, post_v, vals["table"], d.seq_lens, wl.block_size, wl.scale,
+                     wl.window, batch_indices=seqs)
+
+
+def oracle_sub_instance(wl: synth.Workload, d: synth.Draw, nseq: int):
+    """The first nseq sequences of the workload as a self-contained CPU instance."""
+    from oracle import block_pool_ref as bp
+
+    sub = wl.scaled(batch=nseq)
+    lens = d.seq_lens[:nseq]
+    sd = synth.draw_explicit(sub, lens) if wl.layout == "pool" else synth.Draw(
+        lens, d.num_new[:nseq], d.start_pos[:nseq], None, nseq * d.max_blocks_per_seq,
+        d.max_blocks_per_seq)
+    v = synth.values(sub, sd, "cpu")
+    if wl.layout == "pool":
+        table = bp.prepare_block_tables(bp.BlockPool(sd.num_blocks, sd.pool_order), lens,
+                                        wl.block_size, wl.window, sd.max_blocks_per_seq)
+    else:
+        table = bp.block_table_arange(nseq, d.max_blocks_per_seq)
+    slots = bp.slot_mapping(table, sd.start_pos, sd.num_new, wl.block_size)
+    vals = {"k_cache": synth.bf16_bits(v["k_cache"]), "v_cache": synth.bf16_bits(v["v_cache"]),
+            "k_new": synth.bf16_bits(v["k_new"]), "v_new": synth.bf16_bits(v["v_new"]),
+            "q": v["q"].double().numpy(), "table": table, "slots": slots}
+    return sub, sd, vals
+
+
+def time_oracle(wl, d, budget_s: float, max_seq: int):
+    """Time oracle steps over a growing sub-batch until ~budget_s of work is sampled."""
+    nseq = 1
+    sub, sd, vals = oracle_sub_instance(wl, d, max_seq)
+    bytes_per_seq = [decode_bytes(sub.scaled(batch=1), synth.Draw(
+        sd.seq_lens[i:i + 1], sd.num_new[i:i + 1], sd.start_pos[i:i + 1], None, 1, 1))["step"]
+        for i in range(max_seq)]
+    t = time.perf_counter()
+    oracle_sample_step(sub, sd, vals, [0])
+    one = time.perf_counter() - t
+    nseq = int(max(1, min(max_seq, budget_s / max(one, 1e-3))))
+    seqs = list(range(nseq))
+    t = time.perf_counter()
+    oracle_sample_step(sub, sd, vals, seqs)
+    el = time.perf_counter() - t
+    nbytes = sum(bytes_per_seq[:nseq])
+    return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seq_steps_per_s": nseq / el,
+            "sample": f"{nseq} of {wl.batch} sequences (write + decode, fp64, 1 thread), "
+                      f"{el:.1f} s"}
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[args.workload]
+    d = synth.draw(wl)
+    per_step_budget = max(0.05, 150.0 / max(1, args.steps + args.warmup))
+    sub, sd, vals = oracle_sub_instance(wl, d, min(8, wl.batch))
+    t = time.perf_counter()
+    oracle_sample_step(sub, sd, vals, [0])
+    one = time.perf_counter() - t
+    nseq = int(max(1, min(sub.batch, per_step_budget / max(one, 1e-3))))
+    seqs = list(range(nseq))
+    step_bytes = decode_bytes(sub.scaled(batch=nseq), synth.Draw(
+        sd.seq_lens[:nseq], sd.num_new[:nseq], sd.start_pos[:nseq], None, 1, 1))["step"]
+    for _ in range(args.warmup):
+        oracle_sample_step(sub, sd, vals, seqs)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_step(sub, sd, vals, seqs)
+    el = time.perf_counter() - t
+    value = step_bytes * args.steps / el / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "sample_sequences": nseq, "batch": wl.batch},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{nseq} of {wl.batch} sequences per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_child(args):
+    wl = synth.WORKLOADS[args.workload]
+    d = synth.draw(wl)
+    print(json.dumps(time_oracle(wl, d, budget_s=15.0, max_seq=min(8, wl.batch))), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+def traffic_from_profiles(kernel_key: str):
+    """DRAM bytes per launch recorded from an ncu capture, if the kernel source is unchanged."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path))[kernel_key]
+        h = hashlib.sha256()
+        for f in rec["sources"]:
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        if h.hexdigest() != rec["sha256"]:
+            return None
+        return rec["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_cache_77_gb300 import api
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    api.set_decode_kernel({"auto": api.KERNEL_AUTO, "cuda_core": api.KERNEL_CUDA_CORE,
+                           "tensor_core": api.KERNEL_TENSOR_CORE}[args.decode_kernel])
+    wl = synth.WORKLOADS[args.workload]
+    d = synth.draw(wl)
+    v = synth.values(wl, d, dev)
+    if wl.layout == "pool":
+        pool = api.BlockPool(d.num_blocks, d.pool_order)
+        table_np = pool.build_block_table(d.seq_lens, wl.block_size, wl.window, d.max_blocks_per_seq)
+    else:
+        table_np = api.build_block_table_arange(wl.batch, d.max_blocks_per_seq)
+    slots_np = api.build_slot_mapping(table_np, d.start_pos, d.num_new, wl.block_size)
+    table = torch.from_numpy(table_np).to(dev)
+    slots = torch.from_numpy(slots_np).to(dev)
+    seq_lens = torch.from_numpy(d.seq_lens).to(dev)
+    out = torch.empty((wl.batch, wl.num_heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(api.decode_workspace_size(wl.batch, wl.num_heads, wl.num_kv_heads,
+                                               wl.head_dim), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        api.kv_cache_write(v["k_cache"], v["v_cache"], v["k_new"], v["v_new"], slots)
+        api.paged_attention_decode(v["q"], v["k_cache"], v["v_cache"], table, seq_lens, wl.scale,
+                                   wl.window, out=out, workspace=ws)
+
+    nbytes = decode_bytes(wl, d, out_bytes=2)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- device-resident timing: K steps, events around each decode call too
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        api.kv_cache_write(v["k_cache"], v["v_cache"], v["k_new"], v["v_new"], slots)
+        ev_dec[i][0].record(stream)
+        api.paged_attention_decode(v["q"], v["k_cache"], v["v_cache"], table, seq_lens, wl.scale,
+                                   wl.window, out=out, workspace=ws)
+        ev_dec[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_dec)
+
+    # ---- end to end through the public API with host buffers
+    pin = {k: v[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")}
+    lens_pin = torch.from_numpy(d.seq_lens).pin_memory()
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(v["q"]), torch.empty_like(v["k_new"]), torch.empty_like(v["v_new"])
+    slots_dev = torch.empty_like(slots)
+    h2d = sum(t.numel() * t.element_size() for t in pin.values()) + lens_pin.numel() * 4 + \
+        slots_np.nbytes
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        sm = api.build_slot_mapping(table_np, d.start_pos, d.num_new, wl.block_size)
+        sm_pin = torch.from_numpy(sm)
+        dq.copy_(pin["q"], non_blocking=True)
+        dk.copy_(pin["k_new"], non_blocking=True)
+        dv.copy_(pin["v_new"], non_blocking=True)
+        seq_lens.copy_(lens_pin, non_blocking=True)
+        slots_dev.copy_(sm_pin, non_blocking=False)
+        api.kv_cache_write(v["k_cache"], v["v_cache"], dk, dv, slots_dev)
+        api.paged_attention_decode(dq, v["k_cache"], v["v_cache"], table, seq_lens, wl.scale,
+                                   wl.window, out=out, workspace=ws)
+        out_host.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    e2e_steps = max(10, args.steps // 4)
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+
+    hbm, _, peak_kind = peaks()
+    value = nbytes["step"] * world / (ms_step * 1e-3) / 1e9
+    achieved = nbytes["attention"] / (dec_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "seq_steps_per_s": wl.batch * world / (ms_step * 1e-3),
+        "pct_of_peak": value / world / hbm,
+        "config": {"workload": f"{wl.name}: B={wl.batch} H={wl.num_heads} H_kv={wl.num_kv_heads} "
+                               f"d={wl.head_dim} bs={wl.block_size} window={wl.window}",
+                   "seq_lens": f"U[{wl.len_lo},{wl.len_hi}] (sum {int(d.seq_lens.sum())})",
+                   "step": "kv_cache_write + paged_attention_decode (attention + LSE merge)",
+                   "step_bytes": nbytes["step"],
+                   "l2": "inputs larger than L2 (KV cache %.2f GB vs 129 MB L2)" % (nbytes["kv"] / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic_from_profiles(f"decode:{wl.name}"),
+                     "kernel": "paged_attention_decode (split-KV attention + merge), "
+                               f"{dec_ms * 1e3:.1f} us per call",
+                     "decode_kernel": ["auto", "cuda_core", "tensor_core"][api.get_decode_kernel()],
+                     "peak_kind": peak_kind},
+        "e2e": {"value": nbytes["step"] * world / e2e_s / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child",
+                            "--workload", wl.name], capture_output=True, text=True,
+                           env={**os.environ, "OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1",
+                                "MKL_NUM_THREADS": "1", "CUDA_VISIBLE_DEVICES": ""})
+        try:
+            line["cpu_baseline"] = json.loads(r.stdout.strip().splitlines()[-1])
+        except Exception:
+            line["cpu_baseline"] = {"value": None, "error": r.stderr[-300:]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gqa_long", choices=["gqa_long", "swa", "mha_tiny"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-kernel", default="auto", choices=["auto", "cuda_core", "tensor_core"])
+    ap.add_argument("--cpu-baseline-child", action="store_true")
+    args = ap.parse_args()
+    if args.cpu_baseline_child:
+        cpu_baseline_child(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

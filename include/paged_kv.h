@@ -1,0 +1,177 @@
+/*
+ * paged_kv.h -- C ABI of the GB300 paged KV cache library (libpaged_kv.so).
+ *
+ * The problem these calls solve is the one stated by the pages:
+ *   - the physical KV cache is laid out [num_blocks, block_size, H_kv, d]
+ *     ("KVCache 优化技能" skill note, 模式二 and §3.1);
+ *   - new K/V rows are written through slot_mapping, one slot per new token,
+ *     slot = block_table[b, pos / block_size] * block_size + pos % block_size
+ *     (same note §3.1 / §3.3; "KV Cache 管理设计文档" §4.2.2 prepare_slot_mapping);
+ *   - attention reads each sequence's keys through block_table with per-sequence
+ *     lengths (actual_seq_lengths_kv), for GQA, sliding windows whose expired
+ *     table entries hold a null block, causal prefill, and the absorbed MLA form.
+ *
+ * Conventions shared by every call:
+ *   - Return value: PKV_OK (0) or a negative PKV_ERR_* code. On error nothing was
+ *     launched and pkv_last_error() (thread-local) holds a one-line reason.
+ *   - Device calls take device pointers owned by the caller and run
+ *     asynchronously on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *     The library never allocates, frees or synchronises device memory; scratch
+ *     space is a caller-provided `workspace` of at least the size the matching
+ *     *_workspace_size() call returns, 256-byte aligned.
+ *   - Element types: q, caches and new rows are bf16 (raw 16-bit storage);
+ *     block tables, slot mappings and lengths are int32. `out_dtype` selects a
+ *     bf16 (PKV_BF16, round-to-nearest-even) or fp32 (PKV_F32) output.
+ *   - `scale` has no default: callers pass it (the pages warn that a softmax
+ *     scale silently falling back to 1.0 ruins accuracy, standalone guide FA
+ *     v1/v2 parameter table).
+ *   - `dev_status` (nullable) is a device int the kernels set to a nonzero
+ *     PKV_DEV_* bit mask when they meet a bad table entry, slot or length; the
+ *     offending access is skipped (never performed). The caller zeroes it.
+ *   - Tensor-memory-accelerator (TMA) reads need 16-byte aligned base pointers
+ *     and row strides; every pointer below must be 16-byte aligned.
+ */
+#ifndef PAGED_KV_H
+#define PAGED_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARG (-1)   /* null pointer, bad size, misaligned pointer   */
+#define PKV_ERR_UNSUPPORTED (-2)   /* a shape this build does not implement        */
+#define PKV_ERR_WORKSPACE (-3)     /* workspace missing or too small               */
+#define PKV_ERR_LAUNCH (-4)        /* CUDA launch or driver call failed             */
+#define PKV_ERR_OUT_OF_BLOCKS (-5) /* pool cannot satisfy an all-or-nothing request */
+#define PKV_ERR_DOUBLE_FREE (-6)   /* freeing a free block or the null block        */
+
+/* bits of *dev_status */
+#define PKV_DEV_BAD_SLOT 1         /* slot_mapping entry >= num_blocks * block_size  */
+#define PKV_DEV_BAD_BLOCK 2        /* block_table entry outside [0, num_blocks)      */
+#define PKV_DEV_BAD_LENGTH 4       /* length > max_blocks_per_seq * block_size, < 0  */
+#define PKV_DEV_TIMEOUT 8          /* a bounded wait inside a kernel gave up         */
+
+#define PKV_BF16 0
+#define PKV_F32 1
+
+/* One-line reason for the last non-OK return on this thread ("" if none). */
+const char* pkv_last_error(void);
+/* Library ABI version (major * 100 + minor). */
+int pkv_version(void);
+
+/* ==========================================================================
+ * Host-side block management (no device pointers)
+ * ========================================================================== */
+
+/* Opaque BlockPool: FIFO free queue plus a set that catches double frees
+ * ("KV Cache 管理设计文档" §2.4). The queue starts as `initial_order` (a
+ * permutation of 0..num_blocks-1; NULL = 0,1,2,...); the first id popped becomes
+ * the null block, which is never handed out. Seeded shuffles are expressed by
+ * passing a shuffled order. The pool is owned by the caller: destroy it with
+ * pkv_pool_destroy. Not thread-safe. */
+typedef struct pkv_pool pkv_pool;
+int pkv_pool_create(int64_t num_blocks, const int32_t* initial_order, pkv_pool** out);
+void pkv_pool_destroy(pkv_pool* pool);
+int32_t pkv_pool_null_block(const pkv_pool* pool);
+int64_t pkv_pool_num_free(const pkv_pool* pool);
+/* Pop n ids from the head of the queue into ids_out[n]; all-or-nothing
+ * (PKV_ERR_OUT_OF_BLOCKS leaves the pool unchanged). */
+int pkv_pool_alloc(pkv_pool* pool, int64_t n, int32_t* ids_out);
+/* Append ids[n] to the tail; PKV_ERR_DOUBLE_FREE (pool unchanged) if any id is
+ * free already, is the null block, repeats, or is out of range. */
+int pkv_pool_free(pkv_pool* pool, const int32_t* ids, int64_t n);
+
+/* Skipped tokens of a manager after n computed tokens: 0 for full attention
+ * (window <= 0), max(0, n - window + 1) for a sliding window
+ * ("KV Cache 管理设计文档" §2.3 get_num_skipped_tokens). */
+int64_t pkv_num_skipped_tokens(int64_t num_computed_tokens, int64_t window);
+
+/* Batch block table [B, max_blocks_per_seq] (row-major, host memory) for sequences
+ * of total length seq_lens[b] (including the newest token). Row b holds
+ * ceil(len/bs) logical entries; with window > 0 the leading
+ * floor(skipped(len - 1) / bs) entries, wholly outside the window, are the null
+ * block and take nothing from the pool (§2.3.2); the others are popped from the
+ * pool in FIFO order, sequence by sequence. Unused entries hold the null block.
+ * All-or-nothing: PKV_ERR_OUT_OF_BLOCKS leaves the pool unchanged. */
+int pkv_build_block_table(pkv_pool* pool, const int32_t* seq_lens, int32_t B, int32_t block_size,
+                          int32_t window, int32_t max_blocks_per_seq, int32_t* table_out);
+/* Static table arange(B * blocks_per_seq).reshape(B, -1) ("KVCache 优化技能" §3.2). */
+int pkv_build_block_table_arange(int32_t B, int32_t blocks_per_seq, int32_t* table_out);
+/* slot_mapping for num_new[b] tokens at positions start_pos[b].. of each sequence,
+ * concatenated in sequence order (host memory). slot = table[b][pos / bs] * bs +
+ * pos % bs ("KVCache 优化技能" §3.1; "KV Cache 管理设计文档" §4.2.2). Returns the
+ * number of slots written (>= 0) or an error code. */
+int64_t pkv_build_slot_mapping(const int32_t* block_table, int32_t max_blocks_per_seq,
+                               const int32_t* start_pos, const int32_t* num_new, int32_t B,
+                               int32_t block_size, int32_t* slots_out, int64_t slots_capacity);
+
+/* Pool sizing ("KV Cache 管理设计文档" §4.2.1 calculate_block_num); each "+1" is
+ * the null block. */
+int64_t pkv_block_num_fixed(int64_t max_concurrency, int64_t sliding_window, int64_t next_n,
+                            int64_t block_size);
+int64_t pkv_block_num_full_offline(int64_t max_len, int64_t block_size, int64_t max_concurrency);
+int64_t pkv_block_num_full_online(int64_t available_bytes, int64_t per_token_bytes,
+                                  int64_t block_size);
+
+/* ==========================================================================
+ * Device calls
+ * ========================================================================== */
+
+/* Cache write through slot_mapping (standalone guide 模式二: the cache viewed as
+ * [num_blocks * block_size, H_kv, d] takes row t at index slot_mapping[t]).
+ *   k_cache [num_blocks, block_size, num_kv_heads, head_dim_k]  written
+ *   v_cache [num_blocks, block_size, num_kv_heads, head_dim_v]  written; NULL
+ *           (with v = NULL) writes the k side only
+ *   k [num_tokens, num_kv_heads, head_dim_k], v [num_tokens, num_kv_heads, head_dim_v]
+ *   slot_mapping [num_tokens] int32 (device)
+ * The MLA latent write passes cache_nope as k (H_kv 1, 512) and cache_rope as v
+ * (H_kv 1, 64). A bit-exact copy; slot < 0 skips the row; slot >= num_blocks *
+ * block_size skips it and sets PKV_DEV_BAD_SLOT. Duplicate slots in one call are
+ * undefined (one of the rows wins). Row sizes must be multiples of 16 bytes. */
+int pkv_kv_cache_write(void* k_cache, void* v_cache, const void* k, const void* v,
+                       const int32_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                       int32_t block_size, int32_t num_kv_heads, int32_t head_dim_k,
+                       int32_t head_dim_v, int* dev_status, void* stream);
+
+/* Decode attention, one query token per sequence (sparse_mode 0 / band 4).
+ * For each b, h: o = softmax(scale * q[b,h] . K^T) V over positions
+ * [max(0, len_b - window), len_b) (window <= 0: [0, len_b)) of sequence b, read
+ * through block_table; query head h uses kv head h / (H / H_kv) ("KV Cache 笔记",
+ * MHA -> MQA -> GQA, repeat_kv). seq_lens counts every visible position including
+ * the token just written (the FA reads up to the new token: skill note §3.6).
+ *   out  [B, H, head_dim] (bf16 or fp32), lse [B, H] fp32 natural log (nullable);
+ *        len_b = 0 gives o = 0, lse = -inf
+ *   q    [B, H, head_dim] bf16
+ *   k_cache, v_cache [num_blocks, block_size, H_kv, head_dim] bf16
+ *   block_table [B, max_blocks_per_seq] int32; seq_lens [B] int32 (device)
+ * Supported: head_dim 128, block_size 128, H % H_kv == 0, H / H_kv <= 16.
+ * Entries of block_table outside the visible range are never read. */
+size_t pkv_decode_workspace_size(int32_t B, int32_t H, int32_t H_kv, int32_t head_dim);
+
+/* Kernel used by pkv_paged_attention_decode, process-wide (not thread-safe to change
+ * while calls are in flight). PKV_KERNEL_AUTO picks the tcgen05 tensor-core kernel
+ * for head groups of 4 or more query heads per kv head and the CUDA-core kernel
+ * otherwise; the other values force one of them. Both produce the same partial
+ * results up to fp32 rounding. */
+#define PKV_KERNEL_AUTO 0
+#define PKV_KERNEL_CUDA_CORE 1
+#define PKV_KERNEL_TENSOR_CORE 2
+int pkv_set_decode_kernel(int32_t kernel);
+int32_t pkv_get_decode_kernel(void);
+int pkv_paged_attention_decode(void* out, int32_t out_dtype, float* lse, const void* q,
+                               const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, int32_t max_blocks_per_seq,
+                               const int32_t* seq_lens, int32_t B, int32_t H, int32_t H_kv,
+                               int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                               float scale, int32_t window, void* workspace,
+                               size_t workspace_bytes, int* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGED_KV_H */

@@ -1,0 +1,143 @@
+// C ABI entry points for the device calls: argument validation, workspace
+// carving and kernel dispatch onto the caller's stream. Nothing here allocates,
+// frees or synchronises device memory.
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "abi_common.h"
+#include "launch.h"
+
+namespace pkv {
+
+// SM count of the current device (queried once per device).
+static int current_num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static int cached[64] = {0};
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+// Decode kernel choice (process-wide): 0 = automatic, 1 = CUDA cores, 2 = tensor cores.
+static int g_decode_kernel = 0;
+
+static int launch_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return PKV_OK;
+  set_error("%s: %s", what, cudaGetErrorString(e));
+  return PKV_ERR_LAUNCH;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+int pkv_kv_cache_write(void* k_cache, void* v_cache, const void* k, const void* v,
+                       const int32_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
+                       int32_t block_size, int32_t num_kv_heads, int32_t head_dim_k,
+                       int32_t head_dim_v, int* dev_status, void* stream) {
+  PKV_REQUIRE(num_tokens >= 0 && num_blocks > 0 && block_size > 0 && num_kv_heads > 0 &&
+                  head_dim_k > 0,
+              PKV_ERR_INVALID_ARG, "pkv_kv_cache_write: non-positive size");
+  PKV_REQUIRE(k_cache && (num_tokens == 0 || (k && slot_mapping)), PKV_ERR_INVALID_ARG,
+              "pkv_kv_cache_write: null pointer");
+  PKV_REQUIRE((v_cache == nullptr) == (v == nullptr), PKV_ERR_INVALID_ARG,
+              "pkv_kv_cache_write: v_cache and v must both be set or both be NULL");
+  const int64_t row_k = (int64_t)num_kv_heads * head_dim_k * 2;
+  const int64_t row_v = v_cache ? (int64_t)num_kv_heads * head_dim_v * 2 : 0;
+  PKV_REQUIRE(row_k % 16 == 0 && row_v % 16 == 0, PKV_ERR_UNSUPPORTED,
+              "pkv_kv_cache_write: row sizes must be multiples of 16 bytes");
+  PKV_REQUIRE(aligned16(k_cache) && aligned16(k) && aligned16(v_cache) && aligned16(v),
+              PKV_ERR_INVALID_ARG, "pkv_kv_cache_write: pointers must be 16-byte aligned");
+  const int64_t num_slots = num_blocks * block_size;
+  clear_error();
+  return launch_status(launch_kv_write(k_cache, v_cache, k, v, slot_mapping, num_tokens, num_slots,
+                                       row_k, row_v, dev_status, (cudaStream_t)stream,
+                                       current_num_sms()),
+                       "pkv_kv_cache_write");
+}
+
+int pkv_set_decode_kernel(int32_t kernel) {
+  PKV_REQUIRE(kernel >= PKV_KERNEL_AUTO && kernel <= PKV_KERNEL_TENSOR_CORE, PKV_ERR_INVALID_ARG,
+              "pkv_set_decode_kernel: unknown kernel %d", kernel);
+  g_decode_kernel = kernel;
+  return PKV_OK;
+}
+
+int32_t pkv_get_decode_kernel(void) { return g_decode_kernel; }
+
+size_t pkv_decode_workspace_size(int32_t B, int32_t H, int32_t H_kv, int32_t head_dim) {
+  if (B < 0 || H <= 0 || H_kv <= 0 || H % H_kv || head_dim <= 0) return 0;
+  return decode_workspace_bytes(B, H, H_kv, head_dim, current_num_sms());
+}
+
+int pkv_paged_attention_decode(void* out, int32_t out_dtype, float* lse, const void* q,
+                               const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, int32_t max_blocks_per_seq,
+                               const int32_t* seq_lens, int32_t B, int32_t H, int32_t H_kv,
+                               int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                               float scale, int32_t window, void* workspace,
+                               size_t workspace_bytes, int* dev_status, void* stream) {
+  PKV_REQUIRE(B >= 0 && H > 0 && H_kv > 0 && max_blocks_per_seq > 0 && num_blocks > 0,
+              PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode: bad sizes");
+  PKV_REQUIRE(H % H_kv == 0, PKV_ERR_INVALID_ARG,
+              "pkv_paged_attention_decode: H (%d) not a multiple of H_kv (%d)", H, H_kv);
+  const int n_rep = H / H_kv;
+  PKV_REQUIRE(head_dim == 128 && block_size == 128, PKV_ERR_UNSUPPORTED,
+              "pkv_paged_attention_decode: only head_dim 128 and block_size 128 are implemented");
+  PKV_REQUIRE(n_rep == 1 || n_rep == 2 || n_rep == 4 || n_rep == 8 || n_rep == 16,
+              PKV_ERR_UNSUPPORTED, "pkv_paged_attention_decode: H / H_kv = %d unsupported", n_rep);
+  PKV_REQUIRE(out_dtype == PKV_BF16 || out_dtype == PKV_F32, PKV_ERR_INVALID_ARG,
+              "pkv_paged_attention_decode: bad out_dtype");
+  PKV_REQUIRE(std::isfinite(scale) && scale > 0.f, PKV_ERR_INVALID_ARG,
+              "pkv_paged_attention_decode: scale must be a positive finite number");
+  PKV_REQUIRE(window >= 0, PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode: negative window");
+  PKV_REQUIRE(num_blocks * block_size <= INT32_MAX, PKV_ERR_UNSUPPORTED,
+              "pkv_paged_attention_decode: num_blocks * block_size must fit in int32");
+  if (B == 0) return PKV_OK;
+  PKV_REQUIRE(out && q && k_cache && v_cache && block_table && seq_lens, PKV_ERR_INVALID_ARG,
+              "pkv_paged_attention_decode: null pointer");
+  PKV_REQUIRE(aligned16(out) && aligned16(q) && aligned16(k_cache) && aligned16(v_cache),
+              PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode: pointers must be 16-byte aligned");
+  const int G = current_num_sms();
+  PKV_REQUIRE(G > 0, PKV_ERR_LAUNCH, "pkv_paged_attention_decode: no CUDA device");
+  const size_t need = decode_workspace_bytes(B, H, H_kv, head_dim, G);
+  PKV_REQUIRE(workspace && workspace_bytes >= need && (((uintptr_t)workspace) & 255) == 0,
+              PKV_ERR_WORKSPACE, "pkv_paged_attention_decode: workspace needs %zu bytes, 256-aligned",
+              need);
+  DecodeArgs a{};
+  a.q = (const uint16_t*)q;
+  a.k_cache = (const uint8_t*)k_cache;
+  a.v_cache = (const uint8_t*)v_cache;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.lse = lse;
+  a.dev_status = dev_status;
+  a.num_blocks = num_blocks;
+  a.B = B;
+  a.H = H;
+  a.Hkv = H_kv;
+  a.n_rep = n_rep;
+  a.max_blocks = max_blocks_per_seq;
+  a.window = window;
+  a.out_f32 = out_dtype == PKV_F32;
+  a.num_ctas = G;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  decode_workspace_carve(a, workspace);
+  clear_error();
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool tensor_cores = g_decode_kernel == PKV_KERNEL_TENSOR_CORE ||
+                            (g_decode_kernel == PKV_KERNEL_AUTO && n_rep >= 4);
+  int rc = launch_status(tensor_cores ? launch_decode_tc(a, s) : launch_decode_simt(a, s),
+                         "pkv_paged_attention_decode (attention)");
+  if (rc != PKV_OK) return rc;
+  return launch_status(launch_decode_merge(a, s), "pkv_paged_attention_decode (merge)");
+}
+
+}  // extern "C"

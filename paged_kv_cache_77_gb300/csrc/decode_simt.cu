@@ -1,0 +1,353 @@
+// Split-KV flash-decoding on CUDA cores, and the LSE merge of split pieces.
+//
+// Each (b, h) output is softmax(scale * q . K^T) V over the visible positions of
+// sequence b ("KV Cache 笔记", decode incremental form; GQA head h reads kv head
+// h / n_rep, "MHA -> MQA -> GQA"). The keys are read block by block through
+// block_table (skill note §3.1) and never gathered into a contiguous copy.
+//
+// Kernel shape: one CTA per SM walks its balanced share of (b, kv head, block)
+// tiles (device_common.cuh). A tile is 128 tokens of one kv head: 32 KB of K and
+// 32 KB of V, staged into shared memory by cp.async in a 3-deep ring with the
+// 16-byte chunks XOR-swizzled by row so that both the row-wise (QK) and the
+// column-wise (PV) reads are bank-conflict free. Scores are fp32 in log2 units
+// (q pre-multiplied by scale * log2 e); the running max and sum follow the online
+// softmax with the row max subtracted before exp ("三个工程细节"). The block max
+// uses warp-shuffle reductions plus one shared-memory exchange across warps.
+//
+// Roofline: HBM. Algorithmic bytes per tile = 2 * 128 * 128 * 2 (K and V of one
+// kv head); per call add q and out. This kernel is the CUDA-core path (used for
+// MHA, and as the comparison point for the tensor-core GQA kernel).
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace pkv {
+
+namespace simt {
+constexpr int D = 128;
+constexpr int BS = 128;
+constexpr int THREADS = 128;
+constexpr int STAGES = 3;
+constexpr int ROW_BYTES = D * 2;                 // 256 bytes per token row
+constexpr int TILE_BYTES = BS * ROW_BYTES;       // 32 KB for K (or V)
+constexpr int STAGE_BYTES = 2 * TILE_BYTES;      // K + V
+
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return (uint32_t)(row * ROW_BYTES + ((chunk ^ (row & 7)) << 4));
+}
+}  // namespace simt
+
+template <int NREP>
+struct SimtSmem {
+  alignas(128) uint8_t stage[simt::STAGES][simt::STAGE_BYTES];
+  float q[NREP][simt::D];
+  float p[simt::BS][NREP];
+  float red[4][NREP];
+  float lred[4][NREP];
+  long long total;
+};
+
+template <int NREP>
+__global__ void __launch_bounds__(simt::THREADS, 1) decode_simt_kernel(DecodeArgs a) {
+  using namespace simt;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  auto& S = *reinterpret_cast<SimtSmem<NREP>*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int bs = BS;
+  const int cap = a.max_blocks * BS;
+
+  if (warp == 0) {
+    int64_t tot = total_live_blocks(a.seq_lens, a.B, bs, a.window, cap, a.dev_status);
+    if (lane == 0) S.total = tot * a.Hkv;
+  }
+  __syncthreads();
+  const int64_t T = S.total, G = gridDim.x;
+  const int64_t t0 = cta_tile_start(blockIdx.x, T, G), t1 = cta_tile_start(blockIdx.x + 1, T, G);
+  if (t0 >= t1) return;
+
+  TileCursor cur, pre;
+  cursor_seek(cur, a.seq_lens, a.B, a.Hkv, bs, a.window, cap, t0, t1);
+  pre = cur;
+  bool pre_valid = true;
+
+  const int64_t kv_row_elems = (int64_t)a.Hkv * D;  // elements between consecutive tokens
+
+  // Issue the cp.async copies of the tile under `pre` into ring slot `slot`.
+  auto issue = [&](int slot) {
+    if (pre_valid) {
+      int blk = __ldg(a.block_table + (int64_t)pre.b * a.max_blocks + pre.jlo + pre.j);
+      bool ok = blk >= 0 && (int64_t)blk < a.num_blocks;
+      if (!ok && tid == 0) flag_status(a.dev_status, PKV_DEV_BAD_BLOCK);
+      const int64_t elem0 = ((int64_t)(ok ? blk : 0) * bs * a.Hkv + pre.g) * D;
+      const uint8_t* kb = a.k_cache + elem0 * 2;
+      const uint8_t* vb = a.v_cache + elem0 * 2;
+      const uint32_t sk = smem_u32(S.stage[slot]);
+      const uint32_t sv = sk + TILE_BYTES;
+#pragma unroll 4
+      for (int k = 0; k < (BS * 16) / THREADS; ++k) {
+        const int idx = tid + k * THREADS;
+        const int row = idx >> 4, chunk = idx & 15;
+        const int64_t goff = (int64_t)row * kv_row_elems * 2 + chunk * 16;
+        cp_async_16(sk + swz(row, chunk), kb + goff, ok ? 16u : 0u);
+        cp_async_16(sv + swz(row, chunk), vb + goff, ok ? 16u : 0u);
+      }
+      pre_valid = cursor_next(pre, a.seq_lens, a.B, a.Hkv, bs, a.window, cap);
+    }
+    cp_async_commit();
+  };
+
+#pragma unroll
+  for (int s = 0; s < STAGES - 1; ++s) issue(s);
+
+  float m_run[NREP], l_part[NREP], o_acc[NREP];
+  int64_t piece_first = t0;
+  int it = 0;
+  for (;;) {
+    const bool piece_start = (cur.t == t0) || (cur.j == 0);
+    if (piece_start) {
+      piece_first = cur.t;
+      // q of the NREP heads of this group, pre-scaled to log2 units.
+      const uint16_t* qg = a.q + ((int64_t)cur.b * a.H + (int64_t)cur.g * NREP) * D;
+      for (int e = tid; e < NREP * D; e += THREADS)
+        S.q[e / D][e % D] = __uint_as_float((uint32_t)qg[e] << 16) * a.scale_log2;
+#pragma unroll
+      for (int h = 0; h < NREP; ++h) {
+        m_run[h] = -INFINITY;
+        l_part[h] = 0.f;
+        o_acc[h] = 0.f;
+      }
+    }
+    issue((it + STAGES - 1) % STAGES);
+    cp_async_wait<STAGES - 1>();
+    __syncthreads();
+
+    const uint8_t* kt = S.stage[it % STAGES];
+    const uint8_t* vt = kt + TILE_BYTES;
+    const int blk = __ldg(a.block_table + (int64_t)cur.b * a.max_blocks + cur.jlo + cur.j);
+    const bool blk_ok = blk >= 0 && (int64_t)blk < a.num_blocks;
+    const int lo = (a.window > 0 && cur.len > a.window) ? cur.len - a.window : 0;
+
+    // ---- scores: thread = token ----
+    const int pos = (cur.jlo + cur.j) * bs + tid;
+    const bool valid = blk_ok && pos < cur.len && pos >= lo;
+    float s[NREP];
+#pragma unroll
+    for (int h = 0; h < NREP; ++h) s[h] = 0.f;
+#pragma unroll 2
+    for (int c = 0; c < 16; ++c) {
+      const uint4 w = *reinterpret_cast<const uint4*>(kt + swz(tid, c));
+      const float kf[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
+                           bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+#pragma unroll
+      for (int h = 0; h < NREP; ++h) {
+        const float4 qa = *reinterpret_cast<const float4*>(&S.q[h][c * 8]);
+        const float4 qb = *reinterpret_cast<const float4*>(&S.q[h][c * 8 + 4]);
+        s[h] += qa.x * kf[0] + qa.y * kf[1] + qa.z * kf[2] + qa.w * kf[3] + qb.x * kf[4] +
+                qb.y * kf[5] + qb.z * kf[6] + qb.w * kf[7];
+      }
+    }
+    float mx[NREP];
+#pragma unroll
+    for (int h = 0; h < NREP; ++h) {
+      s[h] = valid ? s[h] : -INFINITY;
+      float m = s[h];
+#pragma unroll
+      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      mx[h] = m;
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int h = 0; h < NREP; ++h) S.red[warp][h] = mx[h];
+    }
+    __syncthreads();
+    float alpha[NREP];
+#pragma unroll
+    for (int h = 0; h < NREP; ++h) {
+      const float mb = fmaxf(fmaxf(S.red[0][h], S.red[1][h]), fmaxf(S.red[2][h], S.red[3][h]));
+      const float mn = fmaxf(m_run[h], mb);
+      alpha[h] = (mn == -INFINITY) ? 1.f : exp2f(m_run[h] - mn);
+      const float p = (s[h] == -INFINITY) ? 0.f : exp2f(s[h] - mn);
+      S.p[tid][h] = p;
+      l_part[h] = l_part[h] * alpha[h] + p;
+      m_run[h] = mn;
+    }
+    __syncthreads();
+
+    // ---- values: thread = output element d ----
+    float acc[NREP];
+#pragma unroll
+    for (int h = 0; h < NREP; ++h) acc[h] = 0.f;
+    const int dchunk = tid >> 3, dsub = (tid & 7) * 2;
+#pragma unroll 4
+    for (int tok = 0; tok < BS; ++tok) {
+      const uint16_t vb = *reinterpret_cast<const uint16_t*>(vt + swz(tok, dchunk) + dsub);
+      const float vf = __uint_as_float((uint32_t)vb << 16);
+#pragma unroll
+      for (int h = 0; h < NREP; ++h) acc[h] += S.p[tok][h] * vf;
+    }
+#pragma unroll
+    for (int h = 0; h < NREP; ++h) o_acc[h] = o_acc[h] * alpha[h] + acc[h];
+
+    const bool piece_end = (cur.t + 1 == t1) || (cur.j + 1 == cur.n);
+    if (piece_end) {
+      // Sum the per-token partial normalisers across the CTA.
+#pragma unroll
+      for (int h = 0; h < NREP; ++h) {
+        float l = l_part[h];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) S.lred[warp][h] = l;
+      }
+      __syncthreads();
+      const bool whole = (piece_first == cur.seg_base) && (cur.j + 1 == cur.n);
+      const int64_t slot = (piece_first == cur.seg_base)
+                               ? (int64_t)cur.b * a.Hkv + cur.g
+                               : (int64_t)a.B * a.Hkv + blockIdx.x;
+#pragma unroll
+      for (int h = 0; h < NREP; ++h) {
+        const float l = S.lred[0][h] + S.lred[1][h] + S.lred[2][h] + S.lred[3][h];
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float ov = o_acc[h] * inv;
+        const float lse2 = l > 0.f ? m_run[h] + log2f(l) : -INFINITY;
+        if (whole) {
+          const int64_t row = (int64_t)cur.b * a.H + (int64_t)cur.g * NREP + h;
+          if (a.out_f32)
+            reinterpret_cast<float*>(a.out)[row * D + tid] = ov;
+          else
+            reinterpret_cast<__nv_bfloat16*>(a.out)[row * D + tid] = __float2bfloat16_rn(ov);
+          if (a.lse && tid == 0) a.lse[row] = lse2 * kLn2;
+        } else {
+          a.ws_o[(slot * NREP + h) * D + tid] = ov;
+          if (tid == 0) a.ws_lse[slot * NREP + h] = lse2;
+        }
+      }
+    }
+    __syncthreads();  // everyone is done with this ring slot and with S.p / S.q
+    ++it;
+    if (!cursor_next(cur, a.seq_lens, a.B, a.Hkv, bs, a.window, cap)) break;
+  }
+  cp_async_wait<0>();
+}
+
+// --------------------------------------------------------------------------
+// LSE merge of split pieces: lse = log sum_i exp(lse_i), o = sum_i exp(lse_i - lse) o_i.
+// One CTA per (b, kv head); thread = output element d. Segments finished inside
+// one attention CTA are skipped; empty sequences get o = 0, lse = -inf.
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeArgs a) {
+  constexpr int D = 128;
+  const int seg = blockIdx.x;  // b * Hkv + g
+  const int b = seg / a.Hkv, g = seg % a.Hkv;
+  const int tid = threadIdx.x;
+  __shared__ long long sh[2];
+  const int bs = 128;
+  const int cap = a.max_blocks * bs;
+  if (tid < 32) {
+    int64_t tot = 0, before = 0;
+    for (int bb = tid; bb < a.B; bb += 32) {
+      int n = live_blocks(clamp_len(__ldg(a.seq_lens + bb), cap), bs, a.window).n;
+      tot += n;
+      if (bb < b) before += n;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+    }
+    if (tid == 0) {
+      sh[0] = tot * a.Hkv;
+      sh[1] = before * a.Hkv;
+    }
+  }
+  __syncthreads();
+  const int64_t T = sh[0], G = a.num_ctas;
+  const int n = live_blocks(clamp_len(__ldg(a.seq_lens + b), cap), bs, a.window).n;
+  const int64_t base = sh[1] + (int64_t)g * n;
+  const int n_rep = a.n_rep;
+  if (n == 0) {
+    for (int h = 0; h < n_rep; ++h) {
+      const int64_t row = (int64_t)b * a.H + (int64_t)g * n_rep + h;
+      if (a.out_f32)
+        reinterpret_cast<float*>(a.out)[row * D + tid] = 0.f;
+      else
+        reinterpret_cast<__nv_bfloat16*>(a.out)[row * D + tid] = __float2bfloat16_rn(0.f);
+      if (a.lse && tid == 0) a.lse[row] = -INFINITY;
+    }
+    return;
+  }
+  const int64_t i0 = cta_of_tile(base, T, G), i1 = cta_of_tile(base + n - 1, T, G);
+  if (i0 == i1) return;  // finished by the attention kernel
+  for (int h = 0; h < n_rep; ++h) {
+    // Pass 1: max of the piece LSEs (log2 units).
+    float mx = a.ws_lse[(int64_t)seg * n_rep + h];
+    for (int64_t i = i0 + 1; i <= i1; ++i) {
+      if (cta_tile_start(i + 1, T, G) == cta_tile_start(i, T, G)) continue;  // empty CTA
+      mx = fmaxf(mx, a.ws_lse[((int64_t)a.B * a.Hkv + i) * n_rep + h]);
+    }
+    float wsum = 0.f, acc = 0.f;
+    {
+      const float l2 = a.ws_lse[(int64_t)seg * n_rep + h];
+      const float w = (l2 == -INFINITY) ? 0.f : exp2f(l2 - mx);
+      wsum += w;
+      acc += w * a.ws_o[((int64_t)seg * n_rep + h) * D + tid];
+    }
+    for (int64_t i = i0 + 1; i <= i1; ++i) {
+      if (cta_tile_start(i + 1, T, G) == cta_tile_start(i, T, G)) continue;
+      const int64_t slot = (int64_t)a.B * a.Hkv + i;
+      const float l2 = a.ws_lse[slot * n_rep + h];
+      const float w = (l2 == -INFINITY) ? 0.f : exp2f(l2 - mx);
+      wsum += w;
+      acc += w * a.ws_o[(slot * n_rep + h) * D + tid];
+    }
+    const float ov = wsum > 0.f ? acc / wsum : 0.f;
+    const int64_t row = (int64_t)b * a.H + (int64_t)g * n_rep + h;
+    if (a.out_f32)
+      reinterpret_cast<float*>(a.out)[row * D + tid] = ov;
+    else
+      reinterpret_cast<__nv_bfloat16*>(a.out)[row * D + tid] = __float2bfloat16_rn(ov);
+    if (a.lse && tid == 0) a.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * kLn2 : -INFINITY;
+  }
+}
+
+size_t decode_workspace_bytes(int B, int H, int Hkv, int D, int G) {
+  const int64_t slots = (int64_t)B * Hkv + G;
+  const int64_t n_rep = H / Hkv;
+  const size_t o_bytes = (size_t)(slots * n_rep * D * 4 + 255) / 256 * 256;
+  const size_t l_bytes = (size_t)(slots * n_rep * 4 + 255) / 256 * 256;
+  return o_bytes + l_bytes;
+}
+
+void decode_workspace_carve(DecodeArgs& a, void* ws) {
+  const int64_t slots = (int64_t)a.B * a.Hkv + a.num_ctas;
+  const size_t o_bytes = (size_t)(slots * a.n_rep * 128 * 4 + 255) / 256 * 256;
+  a.ws_o = reinterpret_cast<float*>(ws);
+  a.ws_lse = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + o_bytes);
+}
+
+template <int NREP>
+static cudaError_t launch_simt_n(const DecodeArgs& a, cudaStream_t stream) {
+  const size_t smem = sizeof(SimtSmem<NREP>);
+  cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel<NREP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_simt_kernel<NREP><<<a.num_ctas, simt::THREADS, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream) {
+  switch (a.n_rep) {
+    case 1: return launch_simt_n<1>(a, stream);
+    case 2: return launch_simt_n<2>(a, stream);
+    case 4: return launch_simt_n<4>(a, stream);
+    case 8: return launch_simt_n<8>(a, stream);
+    case 16: return launch_simt_n<16>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.B * a.Hkv == 0) return cudaSuccess;
+  decode_merge_kernel<<<a.B * a.Hkv, 128, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,41 @@
+// Internal launcher interface between the C ABI layer (abi.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+cudaError_t launch_kv_write(void* k_cache, void* v_cache, const void* k, const void* v,
+                            const int32_t* slots, int64_t num_tokens, int64_t num_slots,
+                            int64_t row_k_bytes, int64_t row_v_bytes, int* dev_status,
+                            cudaStream_t stream, int num_sms);
+
+// Arguments of the split-KV decode kernels and their LSE merge.
+struct DecodeArgs {
+  const uint16_t* q;          // [B, H, D] bf16
+  const uint8_t* k_cache;     // [nb, bs, Hkv, D] bf16
+  const uint8_t* v_cache;
+  const int32_t* block_table; // [B, max_blocks]
+  const int32_t* seq_lens;    // [B]
+  void* out;                  // [B, H, D] bf16 or f32
+  float* lse;                 // [B, H] or null
+  float* ws_o;                // [(B*Hkv + G) * n_rep * D] partial outputs
+  float* ws_lse;              // [(B*Hkv + G) * n_rep] partial log2-sum-exp
+  int* dev_status;
+  int64_t num_blocks;
+  int B, H, Hkv, n_rep, max_blocks, window, out_f32;
+  int num_ctas;               // G: CTAs of the attention kernel (one per SM)
+  float scale_log2;           // scale * log2(e)
+};
+
+size_t decode_workspace_bytes(int B, int H, int Hkv, int D, int G);
+void decode_workspace_carve(DecodeArgs& a, void* ws);
+
+// CUDA-core split-KV decode (any group size 1..16) followed by the LSE merge.
+cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream);
+// tcgen05 split-KV decode for head groups (n_rep 1..16), same partials as above.
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace pkv

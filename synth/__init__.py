@@ -1,7 +1,8 @@
 """Seeded synthetic inputs shared by the oracle tests, the GPU parity tests and the bench.
 
 Holds no addressing or attention arithmetic (see ``workloads``)."""
-from .workloads import (BF16_NAN_BITS, WORKLOADS, Draw, Workload, bf16_bits, draw,
+from .workloads import (BF16_NAN_BITS, WORKLOADS, Draw, Workload, bf16_bits, draw, draw_explicit,
                         values)
 
-__all__ = ["BF16_NAN_BITS", "WORKLOADS", "Draw", "Workload", "bf16_bits", "draw", "values"]
+__all__ = ["BF16_NAN_BITS", "WORKLOADS", "Draw", "Workload", "bf16_bits", "draw", "draw_explicit",
+           "values"]

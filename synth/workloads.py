@@ -188,3 +188,18 @@ def values(wl: Workload, d: Draw, device="cpu", poison_null: bool = False) -> di
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """Raw bf16 bit pattern of a tensor as a host uint16 array."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def draw_explicit(wl: Workload, seq_lens, num_new=None, extra_blocks: int = 0) -> Draw:
+    """A Draw with given total lengths (and new-row counts, default 1 per
+    non-empty sequence); the pool order is shuffled with ``wl.seed``."""
+    rng = np.random.default_rng(wl.seed)
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    if num_new is None:
+        num_new = (seq_lens > 0).astype(np.int32)
+    num_new = np.asarray(num_new, dtype=np.int32)
+    start_pos = (seq_lens - num_new).astype(np.int32)
+    nblk = _ceil_div(seq_lens.astype(np.int64), wl.block_size)
+    num_blocks = int(nblk.sum()) + 1 + extra_blocks
+    order = np.concatenate([[0], 1 + rng.permutation(num_blocks - 1)]).astype(np.int32)
+    return Draw(seq_lens, num_new, start_pos, order, num_blocks, max(int(nblk.max()), 1))

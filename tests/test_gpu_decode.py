@@ -11,6 +11,14 @@ from tests.gpu_cases import DecodeCase, compare, sample_rows
 pytestmark = pytest.mark.gpu
 
 BASE = synth.WORKLOADS["gqa_long"]
+KERNELS = {"cuda_core": api.KERNEL_CUDA_CORE, "tensor_core": api.KERNEL_TENSOR_CORE}
+
+
+@pytest.fixture(params=list(KERNELS))
+def kernel(request):
+    api.set_decode_kernel(KERNELS[request.param])
+    yield request.param
+    api.set_decode_kernel(api.KERNEL_AUTO)
 
 
 def _run_decode(case: DecodeCase, rows, out_dtype=torch.float32):
@@ -33,16 +41,16 @@ def _run_decode(case: DecodeCase, rows, out_dtype=torch.float32):
 
 @pytest.mark.parametrize("H,Hkv", [(4, 4), (8, 4), (16, 4), (16, 2), (32, 2)])
 @pytest.mark.parametrize("window", [0, 200])
-def test_decode_small_edge_cases(H, Hkv, window):
+def test_decode_small_edge_cases(H, Hkv, window, kernel):
     lens = [1, 127, 128, 129, 700, 0, 2000, 255]
     wl = BASE.scaled(batch=len(lens), num_heads=H, num_kv_heads=Hkv, window=window, seed=7)
     case = DecodeCase(wl, synth.draw_explicit(wl, lens))
     out, lse, o_ref, lse_ref = _run_decode(case, list(range(len(lens))))
-    compare(out, lse, o_ref, lse_ref, list(range(len(lens))), f"H{H}/Hkv{Hkv}/W{window}")
+    compare(out, lse, o_ref, lse_ref, list(range(len(lens))), f"{kernel} H{H}/Hkv{Hkv}/W{window}")
     assert out[5].abs().max().item() == 0.0 and torch.isinf(lse[5]).all()  # empty sequence
 
 
-def test_decode_bf16_output_and_many_splits():
+def test_decode_bf16_output_and_many_splits(kernel):
     lens = [5000, 3, 4096, 12000]
     wl = BASE.scaled(batch=4, num_heads=64, num_kv_heads=8, seed=8)
     case = DecodeCase(wl, synth.draw_explicit(wl, lens))
@@ -52,13 +60,13 @@ def test_decode_bf16_output_and_many_splits():
 
 
 @pytest.mark.parametrize("name", ["mha_tiny", "gqa_long", "swa"])
-def test_decode_workloads_full_size(name):
+def test_decode_workloads_full_size(name, kernel):
     wl = synth.WORKLOADS[name]
     case = DecodeCase(wl)
     rows = sample_rows(case.d.seq_lens, 4, wl.seed)
     out, lse, o_ref, lse_ref = _run_decode(case, rows)
-    mx, mean = compare(out, lse, o_ref, lse_ref, rows, name)
-    print(f"{name}: rows {rows} max abs {mx:.2e} mean abs {mean:.2e}")
+    mx, mean = compare(out, lse, o_ref, lse_ref, rows, f"{kernel} {name}")
+    print(f"{kernel} {name}: rows {rows} max abs {mx:.2e} mean abs {mean:.2e}")
 
 
 def test_worked_slot_marker_row():
@@ -66,7 +74,7 @@ def test_worked_slot_marker_row():
     cache = torch.zeros((32, 128, 1, 8), dtype=torch.bfloat16, device="cuda")
     row = torch.arange(1, 9, dtype=torch.float32, device="cuda").to(torch.bfloat16).view(1, 1, 8)
     table = api.build_block_table_arange(2, 16)
-    slots = torch.from_numpy(api.build_slot_mapping(table, [300, 0], [1, 0], 128)).cuda()
+    slots = torch.from_numpy(api.build_slot_mapping(table, [0, 300], [0, 1], 128)).cuda()
     assert slots.tolist() == [2348]
     api.kv_cache_write(cache, None, row, None, slots)
     torch.cuda.synchronize()
@@ -74,7 +82,7 @@ def test_worked_slot_marker_row():
     assert cache.float().abs().sum().item() == row.float().sum().item()
 
 
-def test_paged_equals_contiguous_bitwise():
+def test_paged_equals_contiguous_bitwise(kernel):
     # Same logical KV under the arange table and under a shuffled table: the
     # tile plan depends only on the lengths, so the outputs are bit-identical.
     lens = np.array([900, 130, 4000], dtype=np.int32)
@@ -107,7 +115,7 @@ def test_paged_equals_contiguous_bitwise():
     assert torch.equal(o1, o2)
 
 
-def test_constant_values_give_constant_output():
+def test_constant_values_give_constant_output(kernel):
     lens = [1, 333, 5000]
     wl = BASE.scaled(batch=3, num_heads=16, num_kv_heads=2, seed=10)
     case = DecodeCase(wl, synth.draw_explicit(wl, lens), poison=False)
@@ -118,7 +126,7 @@ def test_constant_values_give_constant_output():
     assert (out - 1.0).abs().max().item() < 1e-5
 
 
-def test_bad_block_and_bad_slot_are_reported_not_read():
+def test_bad_block_and_bad_slot_are_reported_not_read(kernel):
     lens = [300]
     wl = BASE.scaled(batch=1, num_heads=8, num_kv_heads=8, seed=11)
     case = DecodeCase(wl, synth.draw_explicit(wl, lens), poison=False)
@@ -135,3 +143,18 @@ def test_bad_block_and_bad_slot_are_reported_not_read():
                        dev_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) & 1
+
+
+def test_cuda_core_and_tensor_core_kernels_agree():
+    lens = [77, 4000, 129, 9000, 1]
+    wl = BASE.scaled(batch=5, seed=12)
+    case = DecodeCase(wl, synth.draw_explicit(wl, lens), poison=True)
+    outs = []
+    for k in (api.KERNEL_CUDA_CORE, api.KERNEL_TENSOR_CORE):
+        api.set_decode_kernel(k)
+        outs.append(api.paged_attention_decode(case.v["q"], case.v["k_cache"], case.v["v_cache"],
+                                               case.table, case.seq_lens, wl.scale))
+    api.set_decode_kernel(api.KERNEL_AUTO)
+    torch.cuda.synchronize()
+    # Different accumulation orders (and bf16 P in the tensor-core path): close, not equal.
+    assert (outs[0] - outs[1]).abs().max().item() < 5e-3
