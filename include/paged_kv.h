@@ -171,6 +171,31 @@ int pkv_paged_attention_decode(void* out, int32_t out_dtype, float* lse, const v
                                float scale, int32_t window, void* workspace,
                                size_t workspace_bytes, int* dev_status, void* stream);
 
+/* Decode without any caller-provided scratch. The paper has no counterpart for
+ * this call; it exists for callers that cannot allocate device memory (a plugin
+ * inside a runtime that owns the allocator, a serving loop whose HBM is already
+ * fully partitioned, code that must not risk the device synchronisation a
+ * cudaMalloc can cause). Same arguments and result as pkv_paged_attention_decode
+ * minus the workspace: the split-KV partials live in a file-scope device array of
+ * PKV_DECODE_STATIC_SCRATCH_BYTES that every GPU loading the library keeps until
+ * the process exits.
+ *   - Rejects (PKV_ERR_WORKSPACE) any problem whose workspace would exceed that
+ *     size (pkv_decode_workspace_size(B, H, H_kv, head_dim) tells).
+ *   - Allocates nothing and calls no allocating routine.
+ *   - The first call on a device, with that device current, looks up the array's
+ *     device address (cudaGetSymbolAddress) and caches it; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents. No part
+ *     of it needs to start at zero. Calls that overlap on the GPU (other streams,
+ *     other host threads) race on it: serialise them. */
+#define PKV_DECODE_STATIC_SCRATCH_BYTES (8 * 1024 * 1024)
+int pkv_paged_attention_decode_static(void* out, int32_t out_dtype, float* lse, const void* q,
+                                      const void* k_cache, const void* v_cache,
+                                      const int32_t* block_table, int32_t max_blocks_per_seq,
+                                      const int32_t* seq_lens, int32_t B, int32_t H, int32_t H_kv,
+                                      int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                      float scale, int32_t window, int* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -178,3 +178,30 @@ def paged_attention_decode(q, k_cache, v_cache, block_table, seq_lens, scale: fl
         _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream)),
         "pkv_paged_attention_decode")
     return out
+
+
+STATIC_SCRATCH_BYTES = 8 * 1024 * 1024  # PKV_DECODE_STATIC_SCRATCH_BYTES
+
+
+def paged_attention_decode_static(q, k_cache, v_cache, block_table, seq_lens, scale: float,
+                                  window: int = 0, out=None, lse=None, out_dtype=torch.float32,
+                                  dev_status=None, stream=None):
+    """Decode attention without a workspace, for callers that cannot allocate device
+    memory: the library keeps the split-KV partials in its own fixed device array
+    (STATIC_SCRATCH_BYTES, shared by every call; overlapping calls race). Same result
+    as paged_attention_decode. The caller still passes (or lets this wrapper create)
+    the output tensor."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _dev_bf16(t, n)
+    _dev_i32(block_table, "block_table")
+    _dev_i32(seq_lens, "seq_lens")
+    B, H, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty((B, H, d), dtype=out_dtype, device=q.device)
+    code = PKV_F32 if out.dtype == torch.float32 else PKV_BF16
+    check(load().pkv_paged_attention_decode_static(
+        _ptr(out), code, _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), B, H, hkv, d, bs, nb, float(scale), int(window),
+        _ptr(dev_status), _stream(stream)), "pkv_paged_attention_decode_static")
+    return out
