@@ -235,7 +235,11 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     api.set_decode_kernel({"auto": api.KERNEL_AUTO, "cuda_core": api.KERNEL_CUDA_CORE,
                            "tensor_core": api.KERNEL_TENSOR_CORE}[args.decode_kernel])
+    if args.workload == "scatter":
+        return run_scatter(args, dev)
     wl = synth.WORKLOADS[args.workload]
+    if args.batch:
+        wl = wl.scaled(batch=args.batch)
     d = synth.draw(wl)
     v = synth.values(wl, d, dev)
     if wl.layout == "pool":
@@ -373,13 +377,64 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_scatter(args, dev):
+    """kv_cache_write alone at bandwidth scale: 262,144 rows of K and V (H_kv 8, d 128)
+    scattered to a random permutation of the slots of a 2048-block cache."""
+    import torch
+
+    from paged_kv_cache_77_gb300 import api
+
+    rows, hkv, d, bs = args.batch or 262144, 8, 128, 128
+    nb = rows // bs
+    g = torch.Generator(device=dev)
+    g.manual_seed(1005)
+    k = torch.randn((rows, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((rows, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    kc = torch.zeros((nb, bs, hkv, d), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    perm = np.random.default_rng(1005).permutation(nb * bs).astype(np.int32)
+    slots = torch.from_numpy(perm).to(dev)
+    nbytes = rows * hkv * d * 2 * 2 * 2 + rows * 4  # read + write of K and V rows, slots
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        api.kv_cache_write(kc, vc, k, v, slots)
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(args.steps):
+        api.kv_cache_write(kc, vc, k, v, slots)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    hbm, _, peak_kind = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "kv_cache_write scatter: achieved HBM GB/s", "value": gbs, "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"scatter: {rows} rows x (K+V) H_kv {hkv} d {d}, random slots",
+                   "l2": "inputs larger than L2 (%.2f GB moved per step)" % (nbytes / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": gbs / hbm, "traffic": traffic_from_profiles("write:scatter"),
+                     "peak_kind": peak_kind},
+        "gpu_launches": args.steps, "clocks": clocks}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="gqa_long", choices=["gqa_long", "swa", "mha_tiny"])
+    ap.add_argument("--workload", default="gqa_long",
+                    choices=["gqa_long", "swa", "mha_tiny", "scatter"])
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-kernel", default="auto", choices=["auto", "cuda_core", "tensor_core"])
     ap.add_argument("--cpu-baseline-child", action="store_true")
