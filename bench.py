@@ -237,6 +237,8 @@ def run_ours(args):
                            "tensor_core": api.KERNEL_TENSOR_CORE}[args.decode_kernel])
     if args.workload == "scatter":
         return run_scatter(args, dev)
+    if args.workload == "mla":
+        return run_mla(args, dev)
     wl = synth.WORKLOADS[args.workload]
     if args.batch:
         wl = wl.scaled(batch=args.batch)
@@ -377,6 +379,85 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_mla(args, dev):
+    """Absorbed MLA decode step: latent row write (nope + rope) + mla_paged_decode."""
+    import torch
+
+    from paged_kv_cache_77_gb300 import api
+
+    wl = synth.WORKLOADS["mla"]
+    if args.batch:
+        wl = wl.scaled(batch=args.batch)
+    d = synth.draw(wl)
+    v = synth.values(wl, d, dev)
+    pool = api.BlockPool(d.num_blocks, d.pool_order)
+    table_np = pool.build_block_table(d.seq_lens, wl.block_size, 0, d.max_blocks_per_seq)
+    slots = torch.from_numpy(api.build_slot_mapping(table_np, d.start_pos, d.num_new,
+                                                    wl.block_size)).to(dev)
+    table = torch.from_numpy(table_np).to(dev)
+    seq_lens = torch.from_numpy(d.seq_lens).to(dev)
+    out = torch.empty((wl.batch, wl.num_heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(api.mla_decode_workspace_size(wl.batch, wl.num_heads), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+    lens = d.seq_lens.astype(np.int64)
+    row = (wl.head_dim + wl.rope_dim) * 2
+    attn_bytes = int(lens.sum()) * row + wl.batch * wl.num_heads * (wl.head_dim + wl.rope_dim) * 2 \
+        + wl.batch * wl.num_heads * wl.head_dim * 2 + int((-(-lens // 128)).sum()) * 4
+    write_bytes = wl.batch * row * 2 + wl.batch * 4
+    flops = int(lens.sum()) * wl.num_heads * (2 * (wl.head_dim + wl.rope_dim) + 2 * wl.head_dim)
+
+    def write():
+        api.kv_cache_write(v["cache_nope"], v["cache_rope"], v["nope_new"], v["rope_new"], slots)
+
+    def attend():
+        api.mla_paged_decode(v["q_nope"], v["q_rope"], v["cache_nope"], v["cache_rope"], table,
+                             seq_lens, wl.scale, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        write()
+        attend()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        write()
+        evs[i][0].record(stream)
+        attend()
+        evs[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    hbm, tf, peak_kind = peaks()
+    ach = attn_bytes / (dec_ms * 1e-3) / 1e9
+    tfl = flops / (dec_ms * 1e-3) / 1e12
+    print(json.dumps({
+        "metric": "MLA absorbed paged decode: achieved HBM GB/s and TFLOP/s", "value":
+        (attn_bytes + write_bytes) / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "seq_steps_per_s": wl.batch / (ms * 1e-3),
+        "config": {"workload": f"mla: B={wl.batch} H={wl.num_heads} latent {wl.head_dim} + rope "
+                               f"{wl.rope_dim} bs {wl.block_size}",
+                   "seq_lens": f"U[{wl.len_lo},{wl.len_hi}] (sum {int(lens.sum())})",
+                   "l2": "inputs larger than L2 (latent cache %.2f GB)" % (int(lens.sum()) * row / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                     "traffic": traffic_from_profiles("mla:mla"),
+                     "kernel": f"mla_paged_decode (attention + merge), {dec_ms * 1e3:.1f} us per call",
+                     "peak_kind": peak_kind},
+        "tensor": {"achieved_tflops": tfl, "peak_tflops": tf, "frac": tfl / tf,
+                   "note": "algorithmic flops; the kernel executes S twice (two latent halves)"},
+        "gpu_launches": 3 * args.steps, "clocks": clocks}), flush=True)
+
+
 def run_scatter(args, dev):
     """kv_cache_write alone at bandwidth scale: 262,144 rows of K and V (H_kv 8, d 128)
     scattered to a random permutation of the slots of a 2048-block cache."""
@@ -432,7 +513,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa_long",
-                    choices=["gqa_long", "swa", "mha_tiny", "scatter"])
+                    choices=["gqa_long", "swa", "mha_tiny", "scatter", "mla"])
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

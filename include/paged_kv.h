@@ -171,6 +171,26 @@ int pkv_paged_attention_decode(void* out, int32_t out_dtype, float* lse, const v
                                float scale, int32_t window, void* workspace,
                                size_t workspace_bytes, int* dev_status, void* stream);
 
+/* Absorbed MLA decode ("KVCache 优化技能" 模式三; standalone guide 模式三 FA absorb
+ * call: key = value = cache_nope, query_rope / key_rope passed separately, one
+ * latent kv head). For each b and query head h, over positions [0, len_b):
+ *   s_j = scale * (q_nope[b,h] . nope_j + q_rope[b,h] . rope_j),  o = softmax(s) . nope
+ *   out [B, H, kv_lora_rank] (bf16 or fp32), lse [B, H] fp32 natural log (nullable)
+ *   q_nope [B, H, kv_lora_rank] bf16, q_rope [B, H, rope_dim] bf16
+ *   cache_nope [num_blocks, block_size, 1, kv_lora_rank] bf16
+ *   cache_rope [num_blocks, block_size, 1, rope_dim] bf16
+ *   block_table [B, max_blocks_per_seq] int32, seq_lens [B] int32 (device)
+ * New latent rows are written beforehand with pkv_kv_cache_write (k = nope,
+ * v = rope). Supported: kv_lora_rank 512, rope_dim 64, block_size 128, H <= 128.
+ * Workspace: pkv_mla_decode_workspace_size(B, H) bytes. */
+size_t pkv_mla_decode_workspace_size(int32_t B, int32_t H);
+int pkv_mla_paged_decode(void* out, int32_t out_dtype, float* lse, const void* q_nope,
+                         const void* q_rope, const void* cache_nope, const void* cache_rope,
+                         const int32_t* block_table, int32_t max_blocks_per_seq,
+                         const int32_t* seq_lens, int32_t B, int32_t H, int32_t kv_lora_rank,
+                         int32_t rope_dim, int32_t block_size, int64_t num_blocks, float scale,
+                         void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
+
 /* Decode without any caller-provided scratch. The paper has no counterpart for
  * this call; it exists for callers that cannot allocate device memory (a plugin
  * inside a runtime that owns the allocator, a serving loop whose HBM is already

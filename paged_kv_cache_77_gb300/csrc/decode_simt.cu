@@ -230,82 +230,73 @@ __global__ void __launch_bounds__(simt::THREADS, 1) decode_simt_kernel(DecodeArg
 
 // --------------------------------------------------------------------------
 // LSE merge of split pieces: lse = log sum_i exp(lse_i), o = sum_i exp(lse_i - lse) o_i.
-// One CTA per (b, kv head); thread = output element d. Segments finished inside
-// one attention CTA are skipped; empty sequences get o = 0, lse = -inf.
+// One CTA per (b, kv head) with one warp per query head of the group; lane = 4
+// consecutive output elements. Segments finished inside one attention CTA are
+// skipped; empty sequences get o = 0, lse = -inf.
 // --------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(512) decode_merge_kernel(DecodeArgs a) {
   constexpr int D = 128;
   const int seg = blockIdx.x;  // b * Hkv + g
   const int b = seg / a.Hkv, g = seg % a.Hkv;
-  const int tid = threadIdx.x;
-  __shared__ long long sh[2];
+  const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_rep = a.n_rep;
+  if (h >= n_rep) return;
   const int bs = 128;
   const int cap = a.max_blocks * bs;
-  if (tid < 32) {
-    int64_t tot = 0, before = 0;
-    for (int bb = tid; bb < a.B; bb += 32) {
-      int n = live_blocks(clamp_len(__ldg(a.seq_lens + bb), cap), bs, a.window).n;
-      tot += n;
-      if (bb < b) before += n;
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      tot += __shfl_xor_sync(0xffffffffu, tot, o);
-      before += __shfl_xor_sync(0xffffffffu, before, o);
-    }
-    if (tid == 0) {
-      sh[0] = tot * a.Hkv;
-      sh[1] = before * a.Hkv;
-    }
+  int64_t tot = 0, before = 0;
+  for (int bb = lane; bb < a.B; bb += 32) {
+    const int n = live_blocks(clamp_len(__ldg(a.seq_lens + bb), cap), bs, a.window).n;
+    tot += n;
+    if (bb < b) before += n;
   }
-  __syncthreads();
-  const int64_t T = sh[0], G = a.num_ctas;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+  }
+  const int64_t T = tot * a.Hkv, G = a.num_ctas;
   const int n = live_blocks(clamp_len(__ldg(a.seq_lens + b), cap), bs, a.window).n;
-  const int64_t base = sh[1] + (int64_t)g * n;
-  const int n_rep = a.n_rep;
-  if (n == 0) {
-    for (int h = 0; h < n_rep; ++h) {
-      const int64_t row = (int64_t)b * a.H + (int64_t)g * n_rep + h;
-      if (a.out_f32)
-        reinterpret_cast<float*>(a.out)[row * D + tid] = 0.f;
-      else
-        reinterpret_cast<__nv_bfloat16*>(a.out)[row * D + tid] = __float2bfloat16_rn(0.f);
-      if (a.lse && tid == 0) a.lse[row] = -INFINITY;
+  const int64_t base = before * a.Hkv + (int64_t)g * n;
+  const int64_t row = (int64_t)b * a.H + (int64_t)g * n_rep + h;
+  auto put = [&](float4 v) {
+    if (a.out_f32) {
+      reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + row * D)[lane] = v;
+    } else {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+      reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + row * D)[lane] =
+          make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
     }
+  };
+  if (n == 0) {
+    put(make_float4(0.f, 0.f, 0.f, 0.f));
+    if (a.lse && lane == 0) a.lse[row] = -INFINITY;
     return;
   }
   const int64_t i0 = cta_of_tile(base, T, G), i1 = cta_of_tile(base + n - 1, T, G);
   if (i0 == i1) return;  // finished by the attention kernel
-  for (int h = 0; h < n_rep; ++h) {
-    // Pass 1: max of the piece LSEs (log2 units).
-    float mx = a.ws_lse[(int64_t)seg * n_rep + h];
-    for (int64_t i = i0 + 1; i <= i1; ++i) {
-      if (cta_tile_start(i + 1, T, G) == cta_tile_start(i, T, G)) continue;  // empty CTA
-      mx = fmaxf(mx, a.ws_lse[((int64_t)a.B * a.Hkv + i) * n_rep + h]);
-    }
-    float wsum = 0.f, acc = 0.f;
-    {
-      const float l2 = a.ws_lse[(int64_t)seg * n_rep + h];
-      const float w = (l2 == -INFINITY) ? 0.f : exp2f(l2 - mx);
-      wsum += w;
-      acc += w * a.ws_o[((int64_t)seg * n_rep + h) * D + tid];
-    }
-    for (int64_t i = i0 + 1; i <= i1; ++i) {
-      if (cta_tile_start(i + 1, T, G) == cta_tile_start(i, T, G)) continue;
-      const int64_t slot = (int64_t)a.B * a.Hkv + i;
-      const float l2 = a.ws_lse[slot * n_rep + h];
-      const float w = (l2 == -INFINITY) ? 0.f : exp2f(l2 - mx);
-      wsum += w;
-      acc += w * a.ws_o[(slot * n_rep + h) * D + tid];
-    }
-    const float ov = wsum > 0.f ? acc / wsum : 0.f;
-    const int64_t row = (int64_t)b * a.H + (int64_t)g * n_rep + h;
-    if (a.out_f32)
-      reinterpret_cast<float*>(a.out)[row * D + tid] = ov;
-    else
-      reinterpret_cast<__nv_bfloat16*>(a.out)[row * D + tid] = __float2bfloat16_rn(ov);
-    if (a.lse && tid == 0) a.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * kLn2 : -INFINITY;
+  auto slot_of = [&](int64_t i) { return (i == i0) ? (int64_t)seg : (int64_t)a.B * a.Hkv + i; };
+  float mx = -INFINITY;
+  for (int64_t i = i0; i <= i1; ++i) {
+    if (i > i0 && cta_tile_start(i + 1, T, G) == cta_tile_start(i, T, G)) continue;  // empty CTA
+    mx = fmaxf(mx, a.ws_lse[slot_of(i) * n_rep + h]);
   }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  for (int64_t i = i0; i <= i1; ++i) {
+    if (i > i0 && cta_tile_start(i + 1, T, G) == cta_tile_start(i, T, G)) continue;
+    const int64_t slot = slot_of(i);
+    const float l2 = a.ws_lse[slot * n_rep + h];
+    const float w = (l2 == -INFINITY) ? 0.f : exp2f(l2 - mx);
+    const float4 x = reinterpret_cast<const float4*>(a.ws_o + (slot * n_rep + h) * D)[lane];
+    acc.x += w * x.x;
+    acc.y += w * x.y;
+    acc.z += w * x.z;
+    acc.w += w * x.w;
+    wsum += w;
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  put(make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+  if (a.lse && lane == 0) a.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * kLn2 : -INFINITY;
 }
 
 size_t decode_workspace_bytes(int B, int H, int Hkv, int D, int G) {
@@ -346,7 +337,7 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream) {
   if (a.B * a.Hkv == 0) return cudaSuccess;
-  decode_merge_kernel<<<a.B * a.Hkv, 128, 0, stream>>>(a);
+  decode_merge_kernel<<<a.B * a.Hkv, 32 * a.n_rep, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -38,4 +38,12 @@ cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream);
 // tcgen05 split-KV decode for head groups (n_rep 1..16), same partials as above.
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream);
 
+// Absorbed MLA decode (tcgen05) plus its merge. Workspace: mla_workspace_bytes.
+size_t mla_workspace_bytes(int B, int g_half);
+cudaError_t launch_mla_decode(const void* q_nope, const void* q_rope, const void* cache_nope,
+                              const void* cache_rope, const int32_t* block_table, int max_blocks,
+                              const int32_t* seq_lens, void* out, int out_f32, float* lse, int B,
+                              int H, int64_t num_blocks, float scale, void* ws, int* dev_status,
+                              int num_sms, cudaStream_t stream);
+
 }  // namespace pkv
