@@ -239,6 +239,8 @@ def run_ours(args):
         return run_scatter(args, dev)
     if args.workload == "mla":
         return run_mla(args, dev)
+    if args.workload == "mixed_prefill":
+        return run_prefill(args, dev)
     wl = synth.WORKLOADS[args.workload]
     if args.batch:
         wl = wl.scaled(batch=args.batch)
@@ -458,6 +460,86 @@ def run_mla(args, dev):
         "gpu_launches": 3 * args.steps, "clocks": clocks}), flush=True)
 
 
+def run_prefill(args, dev):
+    """Mixed chunked-prefill + decode step: write the new K/V rows through slot_mapping,
+    then causal paged prefill over every new row (tensor-core bound)."""
+    import torch
+
+    from paged_kv_cache_77_gb300 import api
+
+    wl = synth.WORKLOADS["mixed_prefill"]
+    if args.batch:
+        wl = wl.scaled(batch=args.batch)
+    d = synth.draw(wl)
+    v = synth.values(wl, d, dev)
+    pool = api.BlockPool(d.num_blocks, d.pool_order)
+    table_np = pool.build_block_table(d.seq_lens, wl.block_size, 0, d.max_blocks_per_seq)
+    slots = torch.from_numpy(api.build_slot_mapping(table_np, d.start_pos, d.num_new,
+                                                    wl.block_size)).to(dev)
+    table = torch.from_numpy(table_np).to(dev)
+    seq_lens = torch.from_numpy(d.seq_lens).to(dev)
+    cu = torch.from_numpy(np.cumsum(d.num_new).astype(np.int32)).to(dev)
+    T = int(d.num_new.sum())
+    out = torch.empty((T, wl.num_heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(api.prefill_workspace_size(), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    q = d.num_new.astype(np.int64)
+    c = (d.seq_lens - d.num_new).astype(np.int64)
+    pairs = int((q * c + q * (q + 1) // 2).sum())  # visible (query row, key) pairs per head
+    flops = pairs * wl.num_heads * 4 * wl.head_dim
+    row = wl.num_kv_heads * wl.head_dim * 2
+    write_bytes = T * row * 2 * 2 + T * 4
+
+    def write():
+        api.kv_cache_write(v["k_cache"], v["v_cache"], v["k_new"], v["v_new"], slots)
+
+    def attend():
+        api.paged_attention_prefill(v["q"], cu, v["k_cache"], v["v_cache"], table, seq_lens,
+                                    wl.scale, causal=True, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        write()
+        attend()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        write()
+        evs[i][0].record(stream)
+        attend()
+        evs[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    pf_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    hbm, tf, peak_kind = peaks()
+    tfl = flops / (pf_ms * 1e-3) / 1e12
+    print(json.dumps({
+        "metric": "causal paged prefill (mixed with decode rows): achieved TFLOP/s",
+        "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "tokens_per_s": T / (ms * 1e-3),
+        "config": {"workload": f"mixed_prefill: {wl.batch} seqs H={wl.num_heads} "
+                               f"H_kv={wl.num_kv_heads} d={wl.head_dim}, {T} new rows, "
+                               f"prior U[{wl.len_lo},{wl.len_hi}], q U[{wl.q_lo},{wl.q_hi}], "
+                               f"{wl.forced_q1} decode rows",
+                   "step": "kv_cache_write of the new rows + paged_attention_prefill",
+                   "write_bytes": write_bytes, "flops": flops},
+        "roofline": {"bound": "tensor", "achieved": tfl, "peak": tf, "unit": "TFLOP/s",
+                     "frac": tfl / tf, "traffic": traffic_from_profiles("prefill:mixed_prefill"),
+                     "kernel": f"paged_attention_prefill (attention + merge), {pf_ms * 1e3:.1f} us",
+                     "peak_kind": peak_kind + " bf16 dense burst"},
+        "gpu_launches": 3 * args.steps, "clocks": clocks}), flush=True)
+
+
 def run_scatter(args, dev):
     """kv_cache_write alone at bandwidth scale: 262,144 rows of K and V (H_kv 8, d 128)
     scattered to a random permutation of the slots of a 2048-block cache."""
@@ -513,7 +595,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa_long",
-                    choices=["gqa_long", "swa", "mha_tiny", "scatter", "mla"])
+                    choices=["gqa_long", "swa", "mha_tiny", "scatter", "mla", "mixed_prefill"])
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

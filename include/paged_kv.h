@@ -171,6 +171,31 @@ int pkv_paged_attention_decode(void* out, int32_t out_dtype, float* lse, const v
                                float scale, int32_t window, void* workspace,
                                size_t workspace_bytes, int* dev_status, void* stream);
 
+/* Prefill attention over TND-packed queries (standalone guide: sparse_mode 3 for
+ * TND paged prefill, q in cumulative form, kv in direct form; "KV Cache 笔记"
+ * "手写40行": the causal mask is bottom-right aligned when a cache precedes the new
+ * rows). Sequence b owns query rows [cu[b-1], cu[b]) (cu[-1] = 0), q_b rows, and
+ * c_b = seq_lens_kv[b] - q_b cached positions before them; its new K/V rows must
+ * already be in the cache (pkv_kv_cache_write). Query row r (0-based in the
+ * sequence) of head h attends, with kv head h / (H / H_kv), to keys
+ * j <= c_b + r when causal = 1, to all seq_lens_kv[b] keys when causal = 0.
+ * q_len = 1 rows are decode rows and mix freely with prefill rows.
+ *   out [num_tokens, H, head_dim] (bf16 or fp32), lse [num_tokens, H] fp32 (nullable)
+ *   q [num_tokens, H, head_dim] bf16; cu_seqlens_q [B] int32 cumulative ends (no
+ *   leading zero), seq_lens_kv [B] int32 direct totals, q_b <= seq_lens_kv[b]
+ *   k_cache, v_cache [num_blocks, block_size, H_kv, head_dim] bf16
+ * Supported: head_dim 128, block_size 128, H / H_kv in {1, 2, 4, 8, 16}.
+ * Workspace: pkv_prefill_workspace_size() bytes (depends only on the device). */
+size_t pkv_prefill_workspace_size(void);
+int pkv_paged_attention_prefill(void* out, int32_t out_dtype, float* lse, const void* q,
+                                const int32_t* cu_seqlens_q, int32_t num_tokens,
+                                const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, int32_t max_blocks_per_seq,
+                                const int32_t* seq_lens_kv, int32_t B, int32_t H, int32_t H_kv,
+                                int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                float scale, int32_t causal, void* workspace,
+                                size_t workspace_bytes, int* dev_status, void* stream);
+
 /* Absorbed MLA decode ("KVCache 优化技能" 模式三; standalone guide 模式三 FA absorb
  * call: key = value = cache_nope, query_rope / key_rope passed separately, one
  * latent kv head). For each b and query head h, over positions [0, len_b):

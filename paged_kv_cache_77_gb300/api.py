@@ -180,6 +180,36 @@ def paged_attention_decode(q, k_cache, v_cache, block_table, seq_lens, scale: fl
     return out
 
 
+def prefill_workspace_size() -> int:
+    return load().pkv_prefill_workspace_size()
+
+
+def paged_attention_prefill(q, cu_seqlens_q, k_cache, v_cache, block_table, seq_lens_kv,
+                            scale: float, causal: bool = True, out=None, lse=None,
+                            out_dtype=torch.float32, workspace=None, dev_status=None, stream=None):
+    """Prefill (TND queries, bottom-right causal) over the paged cache; returns out [T, H, d]."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _dev_bf16(t, n)
+    for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (block_table, "block_table"),
+                 (seq_lens_kv, "seq_lens_kv")):
+        _dev_i32(t, n)
+    T, H, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    B = cu_seqlens_q.numel()
+    if out is None:
+        out = torch.empty((T, H, d), dtype=out_dtype, device=q.device)
+    code = PKV_F32 if out.dtype == torch.float32 else PKV_BF16
+    if workspace is None:
+        workspace = torch.empty(max(prefill_workspace_size(), 256), dtype=torch.uint8,
+                                device=q.device)
+    check(load().pkv_paged_attention_prefill(
+        _ptr(out), code, _ptr(lse), _ptr(q), _ptr(cu_seqlens_q), T, _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens_kv), B, H, hkv, d, bs, nb,
+        float(scale), int(bool(causal)), _ptr(workspace), workspace.numel(), _ptr(dev_status),
+        _stream(stream)), "pkv_paged_attention_prefill")
+    return out
+
+
 def mla_decode_workspace_size(B: int, H: int) -> int:
     return load().pkv_mla_decode_workspace_size(B, H)
 

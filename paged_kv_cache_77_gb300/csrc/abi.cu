@@ -140,6 +140,52 @@ int pkv_paged_attention_decode(void* out, int32_t out_dtype, float* lse, const v
   return launch_status(launch_decode_merge(a, s), "pkv_paged_attention_decode (merge)");
 }
 
+size_t pkv_prefill_workspace_size(void) { return prefill_workspace_bytes(current_num_sms()); }
+
+int pkv_paged_attention_prefill(void* out, int32_t out_dtype, float* lse, const void* q,
+                                const int32_t* cu_seqlens_q, int32_t num_tokens,
+                                const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, int32_t max_blocks_per_seq,
+                                const int32_t* seq_lens_kv, int32_t B, int32_t H, int32_t H_kv,
+                                int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                                float scale, int32_t causal, void* workspace,
+                                size_t workspace_bytes, int* dev_status, void* stream) {
+  PKV_REQUIRE(B >= 0 && num_tokens >= 0 && H > 0 && H_kv > 0 && max_blocks_per_seq > 0 &&
+                  num_blocks > 0,
+              PKV_ERR_INVALID_ARG, "pkv_paged_attention_prefill: bad sizes");
+  PKV_REQUIRE(H % H_kv == 0, PKV_ERR_INVALID_ARG,
+              "pkv_paged_attention_prefill: H (%d) not a multiple of H_kv (%d)", H, H_kv);
+  const int n_rep = H / H_kv;
+  PKV_REQUIRE(head_dim == 128 && block_size == 128, PKV_ERR_UNSUPPORTED,
+              "pkv_paged_attention_prefill: only head_dim 128 and block_size 128 are implemented");
+  PKV_REQUIRE(n_rep == 1 || n_rep == 2 || n_rep == 4 || n_rep == 8 || n_rep == 16,
+              PKV_ERR_UNSUPPORTED, "pkv_paged_attention_prefill: H / H_kv = %d unsupported", n_rep);
+  PKV_REQUIRE(out_dtype == PKV_BF16 || out_dtype == PKV_F32, PKV_ERR_INVALID_ARG,
+              "pkv_paged_attention_prefill: bad out_dtype");
+  PKV_REQUIRE(std::isfinite(scale) && scale > 0.f, PKV_ERR_INVALID_ARG,
+              "pkv_paged_attention_prefill: scale must be a positive finite number");
+  PKV_REQUIRE(causal == 0 || causal == 1, PKV_ERR_INVALID_ARG, "pkv_paged_attention_prefill: causal");
+  PKV_REQUIRE(num_blocks * block_size <= INT32_MAX, PKV_ERR_UNSUPPORTED,
+              "pkv_paged_attention_prefill: num_blocks * block_size must fit in int32");
+  if (B == 0 || num_tokens == 0) return PKV_OK;
+  PKV_REQUIRE(out && q && cu_seqlens_q && k_cache && v_cache && block_table && seq_lens_kv,
+              PKV_ERR_INVALID_ARG, "pkv_paged_attention_prefill: null pointer");
+  PKV_REQUIRE(aligned16(out) && aligned16(q) && aligned16(k_cache) && aligned16(v_cache),
+              PKV_ERR_INVALID_ARG, "pkv_paged_attention_prefill: pointers must be 16-byte aligned");
+  const int G = current_num_sms();
+  PKV_REQUIRE(G > 0, PKV_ERR_LAUNCH, "pkv_paged_attention_prefill: no CUDA device");
+  const size_t need = prefill_workspace_bytes(G);
+  PKV_REQUIRE(workspace && workspace_bytes >= need && (((uintptr_t)workspace) & 255) == 0,
+              PKV_ERR_WORKSPACE, "pkv_paged_attention_prefill: workspace needs %zu bytes, 256-aligned",
+              need);
+  clear_error();
+  return launch_status(launch_prefill(q, cu_seqlens_q, k_cache, v_cache, block_table,
+                                      max_blocks_per_seq, seq_lens_kv, out, out_dtype == PKV_F32, lse,
+                                      num_tokens, B, H, H_kv, num_blocks, scale, causal, workspace,
+                                      dev_status, G, (cudaStream_t)stream),
+                       "pkv_paged_attention_prefill");
+}
+
 size_t pkv_mla_decode_workspace_size(int32_t B, int32_t H) {
   if (B < 0 || H <= 0) return 0;
   return mla_workspace_bytes(B, current_num_sms() / 2);

@@ -46,4 +46,12 @@ cudaError_t launch_mla_decode(const void* q_nope, const void* q_rope, const void
                               int H, int64_t num_blocks, float scale, void* ws, int* dev_status,
                               int num_sms, cudaStream_t stream);
 
+// Causal paged prefill (tcgen05, stream-K) plus its merge.
+size_t prefill_workspace_bytes(int G);
+cudaError_t launch_prefill(const void* q, const int32_t* cu_q, const void* k_cache,
+                           const void* v_cache, const int32_t* block_table, int max_blocks,
+                           const int32_t* seq_lens, void* out, int out_f32, float* lse, int T,
+                           int B, int H, int Hkv, int64_t num_blocks, float scale, int causal,
+                           void* ws, int* dev_status, int num_sms, cudaStream_t stream);
+
 }  // namespace pkv

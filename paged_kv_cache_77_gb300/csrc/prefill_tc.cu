@@ -1,0 +1,685 @@
+// Causal paged prefill (and chunked prefill mixed with decode rows) on tcgen05.
+//
+// Query row r of sequence b, with q_b new rows after c_b = len_b - q_b cached
+// positions, attends to keys j <= c_b + r: bottom-right causal alignment, the
+// sparse_mode 3 semantics of the standalone guide ("手写40行" mask of "KV Cache 笔记":
+// m = (arange(Skv) > arange(Sq)[:, None] + Skv - Sq) * -inf). GQA: query head h
+// reads kv head h / n_rep. Queries are TND-packed; cu_seqlens_q holds cumulative
+// ends, seq_lens_kv direct totals (standalone guide, actual_seq_lengths table).
+//
+// Unit of work: (sequence b, q tile, kv head g). A q tile is 128 / n_rep query
+// tokens; its 128 rows are (token, head of the group) in TND memory order, so one
+// 3-D TMA box {64 d, n_rep heads, 128/n_rep tokens} loads it and the group's K/V
+// tile serves all of them. Per 128-key block of the unit's causal range:
+//
+//   S [128 x 128] = Q [128 x 128 d] . K_blk^T          (tcgen05, fp32 in TMEM)
+//   O [128 x 128] += P [128 x 128 keys] . V_blk         (P bf16 in TMEM, V MN-major)
+//
+// Softmax: eight warps, two per TMEM lane quarter, each owning half of every row's
+// 128 scores; the running max is raised only when a block exceeds it by more than
+// 8 (log2 units), and O in TMEM is rescaled only then (warp-uniform).
+// Loads: warp 0 streams Q and K tiles (K ring 3 deep, a tile freed as soon as its
+// score product completes), warp 6 streams V tiles (2 deep). Warp 1 issues the
+// score products and warp 7 the value products, so neither waits behind the other.
+// Work split: stream-K over all (unit, key block) tiles, one persistent CTA per SM
+// with an equal share; a unit cut by a CTA boundary leaves partial (o, lse) pieces
+// that prefill_merge_kernel combines by LSE. A CTA owns at most two such pieces:
+// one that starts inside a unit ("head") and one that starts a unit it does not
+// finish ("tail").
+//
+// Roofline: tensor cores (dense contraction). Algorithmic flops per visible
+// (query row, key) pair = 4 * 128 (q.k and p.v).
+#include <cuda.h>
+
+#include "device_common.cuh"
+#include "launch.h"
+#include "tc_ptx.cuh"
+
+namespace pkv {
+
+bool make_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
+                    const uint64_t* strides, const uint32_t* box);
+
+namespace pf {
+constexpr int D = 128;
+constexpr int BS = 128;
+constexpr int M = 128;
+constexpr int NK = 3;            // K ring: a K tile is released once its score product is done
+constexpr int NV = 2;            // V ring: a V tile is released after its value product
+constexpr int NTHREADS = 384;    // warp 0 Q/K loads, 1 MMAs, 2 V loads, 4-11 softmax
+constexpr int NSM = 256;         // softmax threads: two warps per TMEM lane quarter
+constexpr int HALF = 16384;      // [128 rows x 128 bytes]
+constexpr int TILE = 2 * HALF;   // K or V tile, or a Q tile
+constexpr int OFF_Q = 0;                          // 2 Q buffers
+constexpr int OFF_K = OFF_Q + 2 * TILE;           // NK K tiles
+constexpr int OFF_V = OFF_K + NK * TILE;          // NV V tiles
+constexpr int OFF_BAR = OFF_V + NV * TILE;        // 229376
+enum {
+  B_KFULL = 0,
+  B_KEMPTY = B_KFULL + NK,
+  B_VFULL = B_KEMPTY + NK,
+  B_VEMPTY = B_VFULL + NV,
+  B_QFULL = B_VEMPTY + NV,
+  B_QEMPTY = B_QFULL + 2,
+  B_SFULL = B_QEMPTY + 2,
+  B_SEMPTY = B_SFULL + 2,
+  B_PFULL = B_SEMPTY + 2,
+  B_PEMPTY = B_PFULL + 2,
+  B_ODONE = B_PEMPTY + 2,
+  B_OFREE = B_ODONE + 2,
+  B_COUNT = B_OFREE + 1
+};
+constexpr int OFF_XCH = OFF_BAR + B_COUNT * 8;      // float [2 halves][128 rows]
+constexpr int OFF_AFL = OFF_XCH + 2 * 128 * 4;      // int [2 halves][4 quarters] abort votes
+constexpr int OFF_MISC = OFF_AFL + 2 * 4 * 4;
+constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
+constexpr uint32_t TMEM_COLS = 512;
+__device__ __forceinline__ uint32_t s_col(int b) { return b * 128; }
+__device__ __forceinline__ uint32_t p_col(int b) { return 256 + b * 64; }
+constexpr uint32_t O_COL = 384;
+}  // namespace pf
+
+struct PrefillArgs {
+  const int32_t* cu_q;        // [B] cumulative query ends
+  const int32_t* seq_lens;    // [B] total kv lengths
+  const int32_t* block_table;
+  void* out;                  // [T, H, D]
+  float* lse;                 // [T, H] or null
+  float* ws_o;                // [G][2][128][128]
+  float* ws_lse;              // [G][2][128]
+  int* dev_status;
+  int64_t num_blocks;
+  int B, H, Hkv, n_rep, qt_tokens, max_blocks, causal, out_f32, T;
+  float scale_log2;
+};
+
+// Geometry of sequence b: query start / length, prior length, number of q tiles.
+struct PfSeq {
+  int q0, qlen, kvlen, c, nqt;
+};
+
+__device__ __forceinline__ PfSeq pf_seq(const PrefillArgs& a, int b) {
+  PfSeq s;
+  s.q0 = b > 0 ? __ldg(a.cu_q + b - 1) : 0;
+  const int q1 = __ldg(a.cu_q + b);
+  s.qlen = max(q1 - s.q0, 0);
+  s.kvlen = clamp_len(__ldg(a.seq_lens + b), a.max_blocks * pf::BS);
+  if (s.qlen > s.kvlen) s.qlen = s.kvlen;  // more queries than keys: only the last kvlen rows are meaningful
+  s.c = s.kvlen - s.qlen;
+  s.nqt = (s.qlen + a.qt_tokens - 1) / a.qt_tokens;
+  return s;
+}
+
+// Key blocks a q tile needs: its causal range is keys [0, c + last token + 1).
+__device__ __forceinline__ int pf_nkv(const PrefillArgs& a, const PfSeq& s, int qt) {
+  const int tok_end = min((qt + 1) * a.qt_tokens, s.qlen);
+  const int keys = a.causal ? s.c + tok_end : s.kvlen;
+  return (keys + pf::BS - 1) / pf::BS;
+}
+
+// Cursor over one CTA's (unit, key block) tiles; units ordered b -> q tile -> g.
+struct PfCursor {
+  int b, qt, g, j, n;
+  PfSeq s;
+  int64_t seg_base, t, t_end;
+};
+
+__device__ inline int64_t pf_seq_work(const PrefillArgs& a, const PfSeq& s) {
+  int64_t w = 0;
+  for (int qt = 0; qt < s.nqt; ++qt) w += pf_nkv(a, s, qt);
+  return w * a.Hkv;
+}
+
+__device__ inline void pf_seek(PfCursor& c, const PrefillArgs& a, int64_t t, int64_t t_end) {
+  c.t = t;
+  c.t_end = t_end;
+  c.b = a.B;
+  if (t >= t_end) return;
+  int64_t base = 0;
+  for (int b = 0; b < a.B; ++b) {
+    const PfSeq s = pf_seq(a, b);
+    const int64_t w = pf_seq_work(a, s);
+    if (t < base + w) {
+      for (int qt = 0; qt < s.nqt; ++qt) {
+        const int n = pf_nkv(a, s, qt);
+        const int64_t wq = (int64_t)n * a.Hkv;
+        if (t < base + wq) {
+          const int64_t off = t - base;
+          c.b = b;
+          c.s = s;
+          c.qt = qt;
+          c.n = n;
+          c.g = (int)(off / n);
+          c.j = (int)(off % n);
+          c.seg_base = base + (int64_t)c.g * n;
+          return;
+        }
+        base += wq;
+      }
+    }
+    base += w;
+  }
+}
+
+__device__ inline bool pf_next(PfCursor& c, const PrefillArgs& a) {
+  ++c.t;
+  if (c.t >= c.t_end) return false;
+  if (++c.j < c.n) return true;
+  c.j = 0;
+  c.seg_base += c.n;
+  if (++c.g < a.Hkv) return true;
+  c.g = 0;
+  for (;;) {
+    if (++c.qt < c.s.nqt) {
+      c.n = pf_nkv(a, c.s, c.qt);
+      if (c.n > 0) return true;
+      continue;
+    }
+    if (++c.b >= a.B) return false;
+    c.s = pf_seq(a, c.b);
+    c.qt = -1;
+  }
+}
+
+__device__ inline int64_t pf_total_work(const PrefillArgs& a) {
+  // One warp: lanes take sequences, then reduce.
+  int64_t w = 0;
+  for (int b = threadIdx.x & 31; b < a.B; b += 32) w += pf_seq_work(a, pf_seq(a, b));
+#pragma unroll
+  for (int o = 16; o; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+  return w;
+}
+
+__global__ void __launch_bounds__(pf::NTHREADS, 1)
+    prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+  using namespace pf;
+  using namespace tc;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(base);
+  auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(base + OFF_MISC);
+  volatile uint32_t* abort_flag = misc + 1;
+  long long* total_s = reinterpret_cast<long long*>(misc + 2);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(bar(B_KFULL + i), 1);
+      mbar_init(bar(B_KEMPTY + i), 1);
+    }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(bar(B_VFULL + i), 1);
+      mbar_init(bar(B_VEMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_QFULL + i), 1);
+      mbar_init(bar(B_QEMPTY + i), 1);
+      mbar_init(bar(B_SFULL + i), 1);
+      mbar_init(bar(B_SEMPTY + i), NSM);
+      mbar_init(bar(B_PFULL + i), NSM);
+      mbar_init(bar(B_PEMPTY + i), 1);
+      mbar_init(bar(B_ODONE + i), 1);
+    }
+    mbar_init(bar(B_OFREE), NSM);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    const int64_t w = pf_total_work(a);
+    if (lane == 0) {
+      *total_s = w;
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(sbase + OFF_MISC, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const int64_t W = *total_s, G = gridDim.x;
+  const int64_t t0 = cta_tile_start(blockIdx.x, W, G), t1 = cta_tile_start(blockIdx.x + 1, W, G);
+  const int ntiles = (int)(t1 - t0);
+  auto fail = [&]() {
+    *abort_flag = 1;
+    flag_status(a.dev_status, PKV_DEV_TIMEOUT);
+  };
+
+  if (ntiles > 0 && warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    PfCursor c;
+    pf_seek(c, a, t0, t1);
+    int piece = 0;
+    const int rows_oob = (int)(a.num_blocks * BS);
+    for (int j = 0; j < ntiles && !*abort_flag; ++j) {
+      if (j == 0 || c.j == 0) {
+        const int qb = piece & 1;
+        if (!mbar_wait(bar(B_QEMPTY + qb), ((piece >> 1) & 1) ^ 1)) { fail(); break; }
+        mbar_expect_tx(bar(B_QFULL + qb), TILE);
+        const int tok = c.s.q0 + c.qt * a.qt_tokens;
+        const uint32_t qs = sbase + OFF_Q + qb * TILE;
+        tma_load_3d(qs, &tm_q, bar(B_QFULL + qb), 0, c.g * a.n_rep, tok);
+        tma_load_3d(qs + HALF, &tm_q, bar(B_QFULL + qb), 64, c.g * a.n_rep, tok);
+        ++piece;
+      }
+      const int st = j % NK;
+      if (!mbar_wait(bar(B_KEMPTY + st), ((j / NK) & 1) ^ 1)) { fail(); break; }
+      const int blk = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.j);
+      const bool ok = blk >= 0 && (int64_t)blk < a.num_blocks;
+      if (!ok) flag_status(a.dev_status, PKV_DEV_BAD_BLOCK);
+      const int row = ok ? blk * BS : rows_oob;
+      const uint32_t ks = sbase + OFF_K + st * TILE;
+      mbar_expect_tx(bar(B_KFULL + st), TILE);
+      tma_load_3d(ks, &tm_k, bar(B_KFULL + st), 0, c.g, row);
+      tma_load_3d(ks + HALF, &tm_k, bar(B_KFULL + st), 64, c.g, row);
+      pf_next(c, a);
+    }
+  } else if (ntiles > 0 && warp == 2 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer (V)
+    PfCursor c;
+    pf_seek(c, a, t0, t1);
+    const int rows_oob = (int)(a.num_blocks * BS);
+    for (int j = 0; j < ntiles && !*abort_flag; ++j) {
+      const int st = j % NV;
+      if (!mbar_wait(bar(B_VEMPTY + st), ((j / NV) & 1) ^ 1)) { fail(); break; }
+      const int blk = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.j);
+      const bool ok = blk >= 0 && (int64_t)blk < a.num_blocks;
+      const int row = ok ? blk * BS : rows_oob;
+      const uint32_t vs = sbase + OFF_V + st * TILE;
+      mbar_expect_tx(bar(B_VFULL + st), TILE);
+      tma_load_3d(vs, &tm_v, bar(B_VFULL + st), 0, c.g, row);
+      tma_load_3d(vs + HALF, &tm_v, bar(B_VFULL + st), 64, c.g, row);
+      pf_next(c, a);
+    }
+  } else if (ntiles > 0 && warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    // Order S(0), S(1), O(0), S(2), O(1), ...: the score product of the next block
+    // runs on the tensor cores while the softmax of the current one is computed.
+    constexpr uint32_t ID_S = idesc_bf16(M, 128, 0, 0);  // Q (K-major) x K^T (K-major)
+    constexpr uint32_t ID_O = idesc_bf16(M, 128, 0, 1);  // P (TMEM) x V (MN-major)
+    PfCursor c;
+    pf_seek(c, a, t0, t1);
+    int piece_s = -1, piece_o = -1;
+    bool first_s0 = false, first_s1 = false;
+    auto issue_s = [&](int j) -> bool {
+      const bool first = (j == 0) || (c.j == 0);
+      const bool last = (j + 1 == ntiles) || (c.j + 1 == c.n);
+      const int st = j % NK, sb = j & 1;
+      if (sb) first_s1 = first; else first_s0 = first;
+      if (first) ++piece_s;
+      const int qb = piece_s & 1;
+      if (first && !mbar_wait(bar(B_QFULL + qb), (piece_s >> 1) & 1)) return false;
+      if (!mbar_wait(bar(B_KFULL + st), (j / NK) & 1)) return false;
+      if (!mbar_wait(bar(B_SEMPTY + sb), ((j >> 1) & 1) ^ 1)) return false;
+      tc_fence_after();
+      const uint32_t ks = sbase + OFF_K + st * TILE, qs = sbase + OFF_Q + qb * TILE;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t ad = smem_desc(qs + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024, kSwizzle128);
+        const uint64_t bd = smem_desc(ks + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024, kSwizzle128);
+        mma_ss(tmem + s_col(sb), ad, bd, ID_S, kk > 0);
+      }
+      mma_commit(bar(B_SFULL + sb));
+      mma_commit(bar(B_KEMPTY + st));
+      if (last) mma_commit(bar(B_QEMPTY + qb));
+      pf_next(c, a);
+      return true;
+    };
+    auto issue_o = [&](int j) -> bool {
+      const int st = j % NV, sb = j & 1;
+      const bool first = sb ? first_s1 : first_s0;
+      if (!mbar_wait(bar(B_VFULL + st), (j / NV) & 1)) return false;
+      if (!mbar_wait(bar(B_PFULL + sb), (j >> 1) & 1)) return false;
+      if (first) {
+        ++piece_o;
+        if (!mbar_wait(bar(B_OFREE), (piece_o & 1) ^ 1)) return false;
+      }
+      tc_fence_after();
+      const uint32_t vs = sbase + OFF_V + st * TILE;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t bd = smem_desc(vs + kk * 2048, HALF, 1024, kSwizzle128);
+        mma_ts(tmem + O_COL, tmem + p_col(sb) + kk * 8, bd, ID_O, !(first && kk == 0));
+      }
+      mma_commit(bar(B_ODONE + sb));
+      mma_commit(bar(B_PEMPTY + sb));
+      mma_commit(bar(B_VEMPTY + st));
+      return true;
+    };
+    bool ok = issue_s(0);
+    for (int j = 0; ok && j < ntiles && !*abort_flag; ++j) {
+      const bool more = j + 1 < ntiles;
+      const bool next_first = more && c.j == 0;
+      if (more && !next_first && !issue_s(j + 1)) { ok = false; break; }
+      if (!issue_o(j)) { ok = false; break; }
+      if (more && next_first && !issue_s(j + 1)) { ok = false; break; }
+    }
+    if (!ok) fail();
+  } else if (ntiles > 0 && warp >= 4) {
+    // ------------------------------------------------------------ softmax / epilogue
+    // Two warps per TMEM lane quarter: warp w handles rows quarter*32 + lane and
+    // score columns [half*64, half*64 + 64). The halves of a row exchange their row
+    // max every block (and their normaliser at the end) through shared memory, with
+    // a 64-thread named barrier per quarter.
+    const int quarter = warp & 3;
+    const int half = (warp - 4) >> 2;
+    const int r = quarter * 32 + lane;  // row = token_local * n_rep + head
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int bar_id = 1 + quarter;
+    float* xch = reinterpret_cast<float*>(base + OFF_XCH);  // [2 halves][128 rows]
+    // Exchange one value with the other half of the row: write, sync the pair, read,
+    // sync again so that the next exchange cannot overwrite an unread value.
+    volatile int* afl = reinterpret_cast<volatile int*>(base + OFF_AFL);
+    bool stop = false;  // set identically in both warps of the pair by exchange()
+    auto exchange = [&](float v) -> float {
+      // Each warp also votes whether to stop, so that the pair leaves the loop at
+      // the same block and never waits alone at the pair barrier.
+      const bool ab = __any_sync(0xffffffffu, *abort_flag != 0);
+      if (lane == 0) afl[half * 4 + quarter] = ab ? 1 : 0;
+      xch[half * 128 + r] = v;
+      named_bar_sync(bar_id, 64);
+      const float other = xch[(half ^ 1) * 128 + r];
+      stop = (afl[quarter] | afl[4 + quarter]) != 0;
+      named_bar_sync(bar_id, 64);
+      return other;
+    };
+    const int tok_local = r / a.n_rep, hl = r % a.n_rep;
+    PfCursor c;
+    pf_seek(c, a, t0, t1);
+    float m_ref = -INFINITY, l = 0.f;
+    bool aborted = false;
+    int pqt = 0, pg = 0;
+    PfSeq ps{};
+    bool p_start = false, p_whole = false;
+
+    auto finalize = [&](int jl) {
+      // Row normaliser: sum of both halves.
+      const float lt = l + exchange(l);
+      if (!mbar_wait(bar(B_ODONE + (jl & 1)), (jl >> 1) & 1)) fail();
+      __syncwarp();
+      tc_fence_after();
+      const int tok = pqt * a.qt_tokens + tok_local;  // query index inside the sequence
+      const bool row_ok = tok < ps.qlen;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float lse2 = lt > 0.f ? m_ref + log2f(lt) : -INFINITY;
+      const int64_t grow = (int64_t)(ps.q0 + tok) * a.H + (int64_t)pg * a.n_rep + hl;  // [T, H] row
+      const int64_t slot = (int64_t)blockIdx.x * 2 + (p_start ? 1 : 0);
+      for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + O_COL + c0, v);
+        tmem_wait_ld();
+        if (p_whole) {
+          if (!row_ok) continue;
+          if (a.out_f32) {
+            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + grow * D + c0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              o[k] = make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
+                                 __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
+          } else {
+            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + grow * D + c0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[8 * k + 2 * e]) * inv,
+                                                          __uint_as_float(v[8 * k + 2 * e + 1]) * inv);
+                w[e] = *reinterpret_cast<uint32_t*>(&h2);
+              }
+              o[k] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        } else {
+          float4* o = reinterpret_cast<float4*>(a.ws_o + (slot * M + r) * D + c0);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            o[k] = make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
+                               __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
+        }
+      }
+      if (half == 0) {
+        if (p_whole) {
+          if (row_ok && a.lse) a.lse[grow] = lse2 * kLn2;
+        } else {
+          a.ws_lse[slot * M + r] = lse2;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(B_OFREE));
+    };
+
+    for (int j = 0; j < ntiles; ++j) {
+      const bool first = (j == 0) || (c.j == 0);
+      if (first) {
+        if (j > 0) finalize(j - 1);
+        m_ref = -INFINITY;
+        l = 0.f;
+        pqt = c.qt;
+        pg = c.g;
+        ps = c.s;
+        p_start = (c.t == c.seg_base);
+        p_whole = p_start && (c.seg_base + c.n <= t1);
+      }
+      const int sb = j & 1;
+      if (!mbar_wait(bar(B_SFULL + sb), (j >> 1) & 1)) fail();
+      __syncwarp();
+      tc_fence_after();
+      // Visible keys of this row in block c.j: key < kvlen and (causal) key <= c + tok.
+      const int tok = c.qt * a.qt_tokens + tok_local;
+      const int key_end = a.causal ? min(c.s.c + tok + 1, c.s.kvlen) : c.s.kvlen;
+      const int blk = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.j);
+      const bool blk_ok = blk >= 0 && (int64_t)blk < a.num_blocks;
+      // Visible columns of this half.
+      const int nvis = blk_ok ? max(0, min(64, key_end - c.j * BS - half * 64)) : 0;
+      uint32_t sv[64];
+      tmem_ld32(tmem + lane_off + s_col(sb) + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld32(tmem + lane_off + s_col(sb) + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(B_SEMPTY + sb));
+      if (!__all_sync(0xffffffffu, nvis >= 64)) {
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+          if (k >= nvis) sv[k] = __float_as_uint(-INFINITY);
+      }
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int k = 0; k < 64; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(sv[k]));
+      // Row max over both halves (raw scores; scale_log2 > 0 keeps the order).
+      const float mown = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      const float mt = fmaxf(mown, exchange(mown)) * a.scale_log2;
+      if (stop) {
+        aborted = true;
+        break;
+      }
+      const bool need = mt > m_ref + 8.f;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? mt : m_ref;
+        const float alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - m_new);
+        if (!first) {
+          if (!mbar_wait(bar(B_ODONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) fail();
+          __syncwarp();
+          tc_fence_after();
+          for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + O_COL + c0, v);
+            tmem_wait_ld();
+            uint32_t lo[16], hi[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              lo[k] = __float_as_uint(__uint_as_float(v[k]) * (need ? alpha : 1.f));
+              hi[k] = __float_as_uint(__uint_as_float(v[16 + k]) * (need ? alpha : 1.f));
+            }
+            tmem_st16(tmem + lane_off + O_COL + c0, lo);
+            tmem_st16(tmem + lane_off + O_COL + c0 + 16, hi);
+          }
+          tmem_wait_st();
+        }
+        if (need) {
+          l *= alpha;
+          m_ref = m_new;
+        }
+      }
+      if (!mbar_wait(bar(B_PEMPTY + sb), ((j >> 1) & 1) ^ 1)) fail();
+      __syncwarp();
+      tc_fence_after();
+      // p = exp2(s * scale_log2 - m_ref): one FMA and one exp2 per key. A row with no
+      // visible key so far keeps m_ref = -inf; its p are all 0 (exp2(-inf)).
+      const float mneg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float p0 = exp2f(fmaf(__uint_as_float(sv[c0 + k]), a.scale_log2, mneg));
+          const float p1 = exp2f(fmaf(__uint_as_float(sv[c0 + k + 1]), a.scale_log2, mneg));
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          const uint32_t w = *reinterpret_cast<uint32_t*>(&h2);
+          // The normaliser sums the bf16-rounded weights the MMA uses.
+          ps4[(k >> 1) & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+          pk[k / 2] = w;
+        }
+        tmem_st16(tmem + lane_off + p_col(sb) + half * 32 + c0 / 2, pk);
+      }
+      l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(B_PFULL + sb));
+      pf_next(c, a);
+    }
+    if (!aborted) finalize(ntiles - 1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// LSE merge of units cut by CTA boundaries. Block i looks at the boundary where CTA
+// i's range starts; if it falls inside a unit and i is the first non-empty CTA
+// after the one that started that unit, it merges the unit: the tail piece of that
+// CTA plus the head pieces of every later CTA the unit reaches. Warp = 16 rows,
+// lane = 4 output columns.
+__global__ void __launch_bounds__(256) prefill_merge_kernel(PrefillArgs a, int G) {
+  using namespace pf;
+  const int i = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t W = pf_total_work(a);
+  const int64_t start = cta_tile_start(i, W, G);
+  if (i == 0 || start >= W || cta_tile_start(i + 1, W, G) == start) return;
+  PfCursor c;
+  pf_seek(c, a, start, W);
+  if (c.b >= a.B || c.t == c.seg_base) return;  // boundary at a unit start: nothing cut here
+  const int64_t seg_end = c.seg_base + c.n;
+  const int64_t i0 = cta_of_tile(c.seg_base, W, G);
+  // First non-empty CTA after i0.
+  int64_t first_after = i0 + 1;
+  while (first_after < G && cta_tile_start(first_after + 1, W, G) == cta_tile_start(first_after, W, G))
+    ++first_after;
+  if (first_after != i) return;
+  const int64_t i1 = cta_of_tile(seg_end - 1, W, G);
+  for (int rr = warp; rr < M; rr += 8) {
+    const int tok = c.qt * a.qt_tokens + rr / a.n_rep;
+    if (tok >= c.s.qlen) continue;
+    float mx = a.ws_lse[(i0 * 2 + 1) * M + rr];
+    for (int64_t k = i0 + 1; k <= i1; ++k) {
+      if (cta_tile_start(k + 1, W, G) == cta_tile_start(k, W, G)) continue;
+      mx = fmaxf(mx, a.ws_lse[(k * 2) * M + rr]);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    for (int64_t k = i0; k <= i1; ++k) {
+      if (k > i0 && cta_tile_start(k + 1, W, G) == cta_tile_start(k, W, G)) continue;
+      const int64_t slot = k * 2 + (k == i0 ? 1 : 0);
+      const float l2 = a.ws_lse[slot * M + rr];
+      const float w = (l2 == -INFINITY) ? 0.f : exp2f(l2 - mx);
+      const float4 x = reinterpret_cast<const float4*>(a.ws_o + (slot * M + rr) * D)[lane];
+      acc.x += w * x.x;
+      acc.y += w * x.y;
+      acc.z += w * x.z;
+      acc.w += w * x.w;
+      wsum += w;
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const int64_t grow = (int64_t)(c.s.q0 + tok) * a.H + (int64_t)c.g * a.n_rep + rr % a.n_rep;
+    const float4 v = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (a.out_f32) {
+      reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + grow * D)[lane] = v;
+    } else {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+      reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + grow * D)[lane] =
+          make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    }
+    if (a.lse && lane == 0) a.lse[grow] = wsum > 0.f ? (mx + log2f(wsum)) * kLn2 : -INFINITY;
+  }
+}
+
+// Rows of queries that see no key at all (q_len > 0 with kv_len = 0 cannot occur
+// after the clamp; rows of a zero-length sequence have no queries) need no fill.
+
+size_t prefill_workspace_bytes(int G) {
+  const size_t o_bytes = (size_t)G * 2 * pf::M * pf::D * 4;
+  const size_t l_bytes = ((size_t)G * 2 * pf::M * 4 + 255) / 256 * 256;
+  return o_bytes + l_bytes;
+}
+
+cudaError_t launch_prefill(const void* q, const int32_t* cu_q, const void* k_cache,
+                           const void* v_cache, const int32_t* block_table, int max_blocks,
+                           const int32_t* seq_lens, void* out, int out_f32, float* lse, int T,
+                           int B, int H, int Hkv, int64_t num_blocks, float scale, int causal,
+                           void* ws, int* dev_status, int num_sms, cudaStream_t stream) {
+  using namespace pf;
+  PrefillArgs a{};
+  a.cu_q = cu_q;
+  a.seq_lens = seq_lens;
+  a.block_table = block_table;
+  a.out = out;
+  a.lse = lse;
+  a.dev_status = dev_status;
+  a.num_blocks = num_blocks;
+  a.B = B;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.n_rep = H / Hkv;
+  a.qt_tokens = M / a.n_rep;
+  a.max_blocks = max_blocks;
+  a.causal = causal;
+  a.out_f32 = out_f32;
+  a.T = T;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.ws_o = reinterpret_cast<float*>(ws);
+  a.ws_lse = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + (size_t)num_sms * 2 * M * D * 4);
+
+  CUtensorMap tq, tk, tv;
+  const uint64_t qdims[3] = {D, (uint64_t)H, (uint64_t)T};
+  const uint64_t qstr[2] = {D * 2, (uint64_t)H * D * 2};
+  const uint32_t qbox[3] = {64, (uint32_t)a.n_rep, (uint32_t)a.qt_tokens};
+  const uint64_t rows = (uint64_t)num_blocks * BS;
+  const uint64_t kdims[3] = {D, (uint64_t)Hkv, rows};
+  const uint64_t kstr[2] = {D * 2, (uint64_t)Hkv * D * 2};
+  const uint32_t kbox[3] = {64, 1, BS};
+  if (!make_tmap_bf16(&tq, q, 3, qdims, qstr, qbox) || !make_tmap_bf16(&tk, k_cache, 3, kdims, kstr, kbox) ||
+      !make_tmap_bf16(&tv, v_cache, 3, kdims, kstr, kbox))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  prefill_tc_kernel<<<num_sms, NTHREADS, SMEM_BYTES, stream>>>(a, tq, tk, tv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prefill_merge_kernel<<<num_sms, 256, 0, stream>>>(a, num_sms);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv
