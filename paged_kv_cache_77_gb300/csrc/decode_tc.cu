@@ -199,13 +199,13 @@ __global__ void __launch_bounds__(tcd::NTHREADS, 1)
       if (!mbar_wait(bar(B_KFULL + st), (j / NST) & 1)) return false;
       if (!mbar_wait(bar(B_SEMPTY + sb), ((j >> 1) & 1) ^ 1)) return false;
       tc_fence_after();
-      const uint32_t ks = sbase + OFF_K + st * TILE, qs = sbase + OFF_Q + qb * QBUF;
+      // Base descriptors once per tile; each K step only adds a constant offset.
+      const uint64_t kd = smem_desc(sbase + OFF_K + st * TILE, 16, 1024, kSwizzle128);
+      const uint64_t qd = smem_desc(sbase + OFF_Q + qb * QBUF, 16, 1024, kSwizzle128);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = smem_desc(ks + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024, kSwizzle128);
-        const uint64_t bd = smem_desc(qs + (kk >> 2) * (QBUF / 2) + (kk & 3) * 32, 16, 1024, kSwizzle128);
-        mma_ss(tmem + s_col(sb), ad, bd, ID_S, kk > 0);
-      }
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss(tmem + s_col(sb), desc_add(kd, (kk >> 2) * HALF + (kk & 3) * 32),
+               desc_add(qd, (kk >> 2) * (QBUF / 2) + (kk & 3) * 32), ID_S, kk > 0);
       mma_commit(bar(B_SFULL + sb));
       if (last) mma_commit(bar(B_QEMPTY + qb));
       cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
@@ -217,13 +217,12 @@ __global__ void __launch_bounds__(tcd::NTHREADS, 1)
       if (!mbar_wait(bar(B_PFULL + ob), (j >> 1) & 1)) return false;
       if (!mbar_wait(bar(B_OEMPTY + ob), ((j >> 1) & 1) ^ 1)) return false;
       tc_fence_after();
-      const uint32_t vs = sbase + OFF_V + st * TILE, ps = sbase + OFF_P + ob * PBUF;
+      const uint64_t vd = smem_desc(sbase + OFF_V + st * TILE, HALF, 1024, kSwizzle128);
+      const uint64_t pd = smem_desc(sbase + OFF_P + ob * PBUF, 16, 1024, kSwizzle128);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = smem_desc(vs + kk * 2048, HALF, 1024, kSwizzle128);
-        const uint64_t bd = smem_desc(ps + (kk >> 2) * (PBUF / 2) + (kk & 3) * 32, 16, 1024, kSwizzle128);
-        mma_ss(tmem + o_col(ob), ad, bd, ID_O, kk > 0);
-      }
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss(tmem + o_col(ob), desc_add(vd, kk * 2048),
+               desc_add(pd, (kk >> 2) * (PBUF / 2) + (kk & 3) * 32), ID_O, kk > 0);
       mma_commit(bar(B_OFULL + ob));
       mma_commit(bar(B_PEMPTY + ob));
       mma_commit(bar(B_KVEMPTY + st));

@@ -218,21 +218,22 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
       if (!mbar_wait(bar(B_KFULL + st), (j / NST) & 1)) return false;
       if (!mbar_wait(bar(B_SEMPTY + sb), ((j >> 1) & 1) ^ 1)) return false;
       tc_fence_after();
-      const uint32_t ks = sbase + OFF_K + st * NCH * KCH;
+      // Base descriptors once per tile; each K step only adds a constant offset.
+      const uint64_t kd = smem_desc(sbase + OFF_K + st * NCH * KCH, 16, 1024, kSwizzle128);
+      const uint64_t qd = smem_desc(sbase + OFF_Q, 16, 1024, kSwizzle128);
+      const uint32_t sd = tmem + s_col(sb), qt = tmem + Q_COL;
+#pragma unroll
       for (int ch = 0; ch < QSM; ++ch) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = smem_desc(sbase + OFF_Q + ch * QCH + kk * 32, 16, 1024, kSwizzle128);
-          const uint64_t bd = smem_desc(ks + ch * KCH + kk * 32, 16, 1024, kSwizzle128);
-          mma_ss(tmem + s_col(sb), ad, bd, ID_S, (ch | kk) != 0);
-        }
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(sd, desc_add(qd, ch * QCH + kk * 32), desc_add(kd, ch * KCH + kk * 32), ID_S,
+                 (ch | kk) != 0);
       }
+#pragma unroll
       for (int ch = QSM; ch < NCH; ++ch) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bd = smem_desc(ks + ch * KCH + kk * 32, 16, 1024, kSwizzle128);
-          mma_ts(tmem + s_col(sb), tmem + Q_COL + (ch - QSM) * 32 + kk * 8, bd, ID_S, 1);
-        }
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(sd, qt + (ch - QSM) * 32 + kk * 8, desc_add(kd, ch * KCH + kk * 32), ID_S, 1);
       }
       mma_commit(bar(B_SFULL + sb));
       if (last) mma_commit(bar(B_QEMPTY));
@@ -248,12 +249,12 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
         if (!mbar_wait(bar(B_OFREE), (piece_o & 1) ^ 1)) return false;
       }
       tc_fence_after();
-      const uint32_t vs = sbase + OFF_K + st * NCH * KCH + (4 * half) * KCH;
+      const uint64_t vd = smem_desc(sbase + OFF_K + st * NCH * KCH + (4 * half) * KCH, KCH, 1024,
+                                    kSwizzle128);
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const uint64_t bd = smem_desc(vs + kk * 2048, KCH, 1024, kSwizzle128);
-        mma_ts(tmem + O_COL, tmem + p_col(sb) + kk * 8, bd, ID_O, !(first && kk == 0));
-      }
+      for (int kk = 0; kk < 2; ++kk)
+        mma_ts(tmem + O_COL, tmem + p_col(sb) + kk * 8, desc_add(vd, kk * 2048), ID_O,
+               !(first && kk == 0));
       mma_commit(bar(B_ODONE + sb));
       mma_commit(bar(B_PEMPTY + sb));
       mma_commit(bar(B_KEMPTY + st));

@@ -18,8 +18,8 @@
 // Softmax: eight warps, two per TMEM lane quarter, each owning half of every row's
 // 128 scores; the running max is raised only when a block exceeds it by more than
 // 8 (log2 units), and O in TMEM is rescaled only then (warp-uniform).
-// Loads: warp 0 streams Q and K tiles (K ring 3 deep, a tile freed as soon as its
-// score product completes), warp 6 streams V tiles (2 deep). Warp 1 issues the
+// Loads: warp 0 streams Q and K tiles (K ring 2 deep, a tile freed as soon as its
+// score product completes), warp 2 streams V tiles (3 deep). Warp 1 issues the
 // score products and warp 7 the value products, so neither waits behind the other.
 // Work split: stream-K over all (unit, key block) tiles, one persistent CTA per SM
 // with an equal share; a unit cut by a CTA boundary leaves partial (o, lse) pieces
@@ -44,8 +44,8 @@ namespace pf {
 constexpr int D = 128;
 constexpr int BS = 128;
 constexpr int M = 128;
-constexpr int NK = 3;            // K ring: a K tile is released once its score product is done
-constexpr int NV = 2;            // V ring: a V tile is released after its value product
+constexpr int NK = 2;            // K ring: a K tile is released once its score product is done
+constexpr int NV = 3;            // V ring: a V tile is released after its value product
 constexpr int NTHREADS = 384;    // warp 0 Q/K loads, 1 MMAs, 2 V loads, 4-11 softmax
 constexpr int NSM = 256;         // softmax threads: two warps per TMEM lane quarter
 constexpr int HALF = 16384;      // [128 rows x 128 bytes]
@@ -319,13 +319,13 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       if (!mbar_wait(bar(B_KFULL + st), (j / NK) & 1)) return false;
       if (!mbar_wait(bar(B_SEMPTY + sb), ((j >> 1) & 1) ^ 1)) return false;
       tc_fence_after();
-      const uint32_t ks = sbase + OFF_K + st * TILE, qs = sbase + OFF_Q + qb * TILE;
+      // Base descriptors once per tile; each K step only adds a constant offset.
+      const uint64_t qd = smem_desc(sbase + OFF_Q + qb * TILE, 16, 1024, kSwizzle128);
+      const uint64_t kd = smem_desc(sbase + OFF_K + st * TILE, 16, 1024, kSwizzle128);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = smem_desc(qs + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024, kSwizzle128);
-        const uint64_t bd = smem_desc(ks + (kk >> 2) * HALF + (kk & 3) * 32, 16, 1024, kSwizzle128);
-        mma_ss(tmem + s_col(sb), ad, bd, ID_S, kk > 0);
-      }
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss(tmem + s_col(sb), desc_add(qd, (kk >> 2) * HALF + (kk & 3) * 32),
+               desc_add(kd, (kk >> 2) * HALF + (kk & 3) * 32), ID_S, kk > 0);
       mma_commit(bar(B_SFULL + sb));
       mma_commit(bar(B_KEMPTY + st));
       if (last) mma_commit(bar(B_QEMPTY + qb));
@@ -342,12 +342,11 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
         if (!mbar_wait(bar(B_OFREE), (piece_o & 1) ^ 1)) return false;
       }
       tc_fence_after();
-      const uint32_t vs = sbase + OFF_V + st * TILE;
+      const uint64_t vd = smem_desc(sbase + OFF_V + st * TILE, HALF, 1024, kSwizzle128);
+      const uint32_t pt = tmem + p_col(sb);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t bd = smem_desc(vs + kk * 2048, HALF, 1024, kSwizzle128);
-        mma_ts(tmem + O_COL, tmem + p_col(sb) + kk * 8, bd, ID_O, !(first && kk == 0));
-      }
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts(tmem + O_COL, pt + kk * 8, desc_add(vd, kk * 2048), ID_O, !(first && kk == 0));
       mma_commit(bar(B_ODONE + sb));
       mma_commit(bar(B_PEMPTY + sb));
       mma_commit(bar(B_VEMPTY + st));

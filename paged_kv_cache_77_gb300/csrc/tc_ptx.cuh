@@ -171,6 +171,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
   return d;
 }
 
+// Descriptor of the same matrix `byte_off` bytes further on: only the start-address
+// field (address >> 4, bits 0-13) moves. Shared-memory addresses stay below 256 KB,
+// so the field never carries into the next one.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_off) {
+  return desc + (uint64_t)(byte_off >> 4);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
 // a_mn / b_mn: 1 when that operand is MN-major (transposed) in shared memory.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
