@@ -21,11 +21,11 @@
 // Loads: warp 0 streams Q and K tiles (K ring 2 deep, a tile freed as soon as its
 // score product completes), warp 2 streams V tiles (3 deep). Warp 1 issues the
 // score products and warp 7 the value products, so neither waits behind the other.
-// Work split: stream-K over all (unit, key block) tiles, one persistent CTA per SM
-// with an equal share; a unit cut by a CTA boundary leaves partial (o, lse) pieces
-// that prefill_merge_kernel combines by LSE. A CTA owns at most two such pieces:
-// one that starts inside a unit ("head") and one that starts a unit it does not
-// finish ("tail").
+// Work split: stream-K over all (unit, key block) tiles in kRounds rounds (see
+// pf_vbound), one persistent CTA per SM with an equal share of every round; a unit
+// cut by a range boundary leaves partial (o, lse) pieces that prefill_merge_kernel
+// combines by LSE. Each range owns at most two such pieces: one that starts inside
+// a unit ("head") and one that starts a unit it does not finish ("tail").
 //
 // Roofline: tensor cores (dense contraction). Algorithmic flops per visible
 // (query row, key) pair = 4 * 128 (q.k and p.v).
@@ -85,8 +85,8 @@ struct PrefillArgs {
   const int32_t* block_table;
   void* out;                  // [T, H, D]
   float* lse;                 // [T, H] or null
-  float* ws_o;                // [G][2][128][128]
-  float* ws_lse;              // [G][2][128]
+  float* ws_o;                // [kRounds * G][2][128][128]
+  float* ws_lse;              // [kRounds * G][2][128]
   int* dev_status;
   int64_t num_blocks;
   int B, H, Hkv, n_rep, qt_tokens, max_blocks, causal, out_f32, T;
@@ -117,11 +117,50 @@ __device__ __forceinline__ int pf_nkv(const PrefillArgs& a, const PfSeq& s, int 
   return (keys + pf::BS - 1) / pf::BS;
 }
 
-// Cursor over one CTA's (unit, key block) tiles; units ordered b -> q tile -> g.
+// The (unit, key block) tile list is ordered b -> kv head g -> q tile -> block, so
+// the units of one (b, g) are adjacent and stream the same K/V blocks.
+//
+// Rounds: the list is cut into kRounds equal chunks and chunk c is split across
+// the G CTAs as in stream-K (CTA i takes [cb_c + i*W_c/G, cb_c + (i+1)*W_c/G)).
+// CTA i walks round 0, then round 1, ...; since every CTA does an equal share of a
+// round, all CTAs are inside the same chunk at any time, which keeps that chunk's
+// K/V resident in L2. The range of round c on CTA i is "virtual CTA" k = c*G + i;
+// pieces and merges work on virtual CTAs. Measured on GB300 (16 sequences, 10.7k
+// query rows, 0.33 GB of K/V), more rounds are slower: 1 round 742 TFLOP/s, 2: 730,
+// 4: 632, 8: 572, 16: 488. Every range boundary adds a partial piece (its O
+// epilogue stalls the MMA pipeline) and the K/V re-reads it saves are not what
+// limits this kernel, so the default is one round (plain stream-K).
+#ifndef PKV_PREFILL_ROUNDS
+#define PKV_PREFILL_ROUNDS 1
+#endif
+constexpr int kRounds = PKV_PREFILL_ROUNDS;
+
+__device__ __forceinline__ int64_t pf_chunk_base(int64_t c, int64_t W) { return (c * W) / kRounds; }
+
+// Start of virtual CTA k's range (k in [0, kRounds*G]).
+__device__ __forceinline__ int64_t pf_vbound(int64_t k, int64_t W, int64_t G) {
+  const int64_t c = k / G, i = k % G;
+  if (c >= kRounds) return W;
+  const int64_t cb = pf_chunk_base(c, W), wc = pf_chunk_base(c + 1, W) - cb;
+  return cb + (i * wc) / G;
+}
+
+// Virtual CTA whose range contains tile t (the last one starting at or before t).
+__device__ __forceinline__ int64_t pf_vcta_of_tile(int64_t t, int64_t W, int64_t G) {
+  int64_t c = ((t + 1) * kRounds + W - 1) / W - 1;  // chunk containing t
+  const int64_t cb = pf_chunk_base(c, W), wc = pf_chunk_base(c + 1, W) - cb;
+  return c * G + cta_of_tile(t - cb, wc, G);
+}
+
+// Cursor over one CTA's tiles: the concatenation of its kRounds ranges.
 struct PfCursor {
-  int b, qt, g, j, n;
+  int b, g, qt, j, n;
   PfSeq s;
-  int64_t seg_base, t, t_end;
+  int64_t seg_base;      // first tile of the current unit
+  int64_t t, t_end;      // current tile, end of the current range
+  int64_t W, G;
+  int round, cta;
+  bool range_start;      // t is the first tile of its range
 };
 
 __device__ inline int64_t pf_seq_work(const PrefillArgs& a, const PfSeq& s) {
@@ -130,54 +169,92 @@ __device__ inline int64_t pf_seq_work(const PrefillArgs& a, const PfSeq& s) {
   return w * a.Hkv;
 }
 
-__device__ inline void pf_seek(PfCursor& c, const PrefillArgs& a, int64_t t, int64_t t_end) {
+// Position on tile t of the flat list (b, g, q tile, block).
+__device__ inline void pf_locate(PfCursor& c, const PrefillArgs& a, int64_t t) {
   c.t = t;
-  c.t_end = t_end;
   c.b = a.B;
-  if (t >= t_end) return;
   int64_t base = 0;
   for (int b = 0; b < a.B; ++b) {
     const PfSeq s = pf_seq(a, b);
     const int64_t w = pf_seq_work(a, s);
     if (t < base + w) {
+      const int64_t wg = w / a.Hkv;  // work of one (b, g)
+      const int64_t off = t - base;
+      c.b = b;
+      c.s = s;
+      c.g = (int)(off / wg);
+      int64_t o2 = off - (int64_t)c.g * wg;
+      int64_t sb = base + (int64_t)c.g * wg;
       for (int qt = 0; qt < s.nqt; ++qt) {
         const int n = pf_nkv(a, s, qt);
-        const int64_t wq = (int64_t)n * a.Hkv;
-        if (t < base + wq) {
-          const int64_t off = t - base;
-          c.b = b;
-          c.s = s;
+        if (o2 < n) {
           c.qt = qt;
           c.n = n;
-          c.g = (int)(off / n);
-          c.j = (int)(off % n);
-          c.seg_base = base + (int64_t)c.g * n;
+          c.j = (int)o2;
+          c.seg_base = sb;
           return;
         }
-        base += wq;
+        o2 -= n;
+        sb += n;
       }
+      return;
     }
     base += w;
   }
 }
 
+// Move to the first non-empty range at or after `round`; false if none is left.
+__device__ inline bool pf_enter_round(PfCursor& c, const PrefillArgs& a, int round) {
+  for (; round < kRounds; ++round) {
+    const int64_t k = (int64_t)round * c.G + c.cta;
+    const int64_t lo = pf_vbound(k, c.W, c.G), hi = pf_vbound(k + 1, c.W, c.G);
+    if (lo < hi) {
+      c.round = round;
+      c.t_end = hi;
+      c.range_start = true;
+      pf_locate(c, a, lo);
+      return true;
+    }
+  }
+  c.round = kRounds;
+  return false;
+}
+
+__device__ inline bool pf_begin(PfCursor& c, const PrefillArgs& a, int64_t W, int64_t G, int cta) {
+  c.W = W;
+  c.G = G;
+  c.cta = cta;
+  return pf_enter_round(c, a, 0);
+}
+
+// Total tiles of CTA `cta` over all rounds.
+__device__ inline int pf_cta_tiles(int64_t W, int64_t G, int cta) {
+  int64_t n = 0;
+  for (int r = 0; r < kRounds; ++r) {
+    const int64_t k = (int64_t)r * G + cta;
+    n += pf_vbound(k + 1, W, G) - pf_vbound(k, W, G);
+  }
+  return (int)n;
+}
+
 __device__ inline bool pf_next(PfCursor& c, const PrefillArgs& a) {
   ++c.t;
-  if (c.t >= c.t_end) return false;
+  if (c.t >= c.t_end) return pf_enter_round(c, a, c.round + 1);
+  c.range_start = false;
   if (++c.j < c.n) return true;
   c.j = 0;
   c.seg_base += c.n;
-  if (++c.g < a.Hkv) return true;
-  c.g = 0;
   for (;;) {
     if (++c.qt < c.s.nqt) {
       c.n = pf_nkv(a, c.s, c.qt);
       if (c.n > 0) return true;
       continue;
     }
+    c.qt = -1;
+    if (++c.g < a.Hkv) continue;
+    c.g = 0;
     if (++c.b >= a.B) return false;
     c.s = pf_seq(a, c.b);
-    c.qt = -1;
   }
 }
 
@@ -245,8 +322,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem = misc[0];
   const int64_t W = *total_s, G = gridDim.x;
-  const int64_t t0 = cta_tile_start(blockIdx.x, W, G), t1 = cta_tile_start(blockIdx.x + 1, W, G);
-  const int ntiles = (int)(t1 - t0);
+  const int ntiles = pf_cta_tiles(W, G, blockIdx.x);
   auto fail = [&]() {
     *abort_flag = 1;
     flag_status(a.dev_status, PKV_DEV_TIMEOUT);
@@ -255,11 +331,11 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
   if (ntiles > 0 && warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     PfCursor c;
-    pf_seek(c, a, t0, t1);
+    pf_begin(c, a, W, G, blockIdx.x);
     int piece = 0;
     const int rows_oob = (int)(a.num_blocks * BS);
     for (int j = 0; j < ntiles && !*abort_flag; ++j) {
-      if (j == 0 || c.j == 0) {
+      if (j == 0 || c.j == 0 || c.range_start) {
         const int qb = piece & 1;
         if (!mbar_wait(bar(B_QEMPTY + qb), ((piece >> 1) & 1) ^ 1)) { fail(); break; }
         mbar_expect_tx(bar(B_QFULL + qb), TILE);
@@ -284,7 +360,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
   } else if (ntiles > 0 && warp == 2 && lane == 0) {
     // ------------------------------------------------------------ TMA producer (V)
     PfCursor c;
-    pf_seek(c, a, t0, t1);
+    pf_begin(c, a, W, G, blockIdx.x);
     const int rows_oob = (int)(a.num_blocks * BS);
     for (int j = 0; j < ntiles && !*abort_flag; ++j) {
       const int st = j % NV;
@@ -305,12 +381,12 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
     constexpr uint32_t ID_S = idesc_bf16(M, 128, 0, 0);  // Q (K-major) x K^T (K-major)
     constexpr uint32_t ID_O = idesc_bf16(M, 128, 0, 1);  // P (TMEM) x V (MN-major)
     PfCursor c;
-    pf_seek(c, a, t0, t1);
+    pf_begin(c, a, W, G, blockIdx.x);
     int piece_s = -1, piece_o = -1;
     bool first_s0 = false, first_s1 = false;
     auto issue_s = [&](int j) -> bool {
-      const bool first = (j == 0) || (c.j == 0);
-      const bool last = (j + 1 == ntiles) || (c.j + 1 == c.n);
+      const bool first = (j == 0) || (c.j == 0) || c.range_start;
+      const bool last = (j + 1 == ntiles) || (c.j + 1 == c.n) || (c.t + 1 == c.t_end);
       const int st = j % NK, sb = j & 1;
       if (sb) first_s1 = first; else first_s0 = first;
       if (first) ++piece_s;
@@ -355,7 +431,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
     bool ok = issue_s(0);
     for (int j = 0; ok && j < ntiles && !*abort_flag; ++j) {
       const bool more = j + 1 < ntiles;
-      const bool next_first = more && c.j == 0;
+      const bool next_first = more && (c.j == 0 || c.range_start);
       if (more && !next_first && !issue_s(j + 1)) { ok = false; break; }
       if (!issue_o(j)) { ok = false; break; }
       if (more && next_first && !issue_s(j + 1)) { ok = false; break; }
@@ -391,10 +467,11 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
     };
     const int tok_local = r / a.n_rep, hl = r % a.n_rep;
     PfCursor c;
-    pf_seek(c, a, t0, t1);
+    pf_begin(c, a, W, G, blockIdx.x);
     float m_ref = -INFINITY, l = 0.f;
     bool aborted = false;
     int pqt = 0, pg = 0;
+    int64_t p_vcta = 0;
     PfSeq ps{};
     bool p_start = false, p_whole = false;
 
@@ -409,7 +486,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const float lse2 = lt > 0.f ? m_ref + log2f(lt) : -INFINITY;
       const int64_t grow = (int64_t)(ps.q0 + tok) * a.H + (int64_t)pg * a.n_rep + hl;  // [T, H] row
-      const int64_t slot = (int64_t)blockIdx.x * 2 + (p_start ? 1 : 0);
+      const int64_t slot = p_vcta * 2 + (p_start ? 1 : 0);
       for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_off + O_COL + c0, v);
@@ -456,7 +533,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
     };
 
     for (int j = 0; j < ntiles; ++j) {
-      const bool first = (j == 0) || (c.j == 0);
+      const bool first = (j == 0) || (c.j == 0) || c.range_start;
       if (first) {
         if (j > 0) finalize(j - 1);
         m_ref = -INFINITY;
@@ -464,8 +541,9 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
         pqt = c.qt;
         pg = c.g;
         ps = c.s;
+        p_vcta = (int64_t)c.round * G + blockIdx.x;
         p_start = (c.t == c.seg_base);
-        p_whole = p_start && (c.seg_base + c.n <= t1);
+        p_whole = p_start && (c.seg_base + c.n <= c.t_end);
       }
       const int sb = j & 1;
       if (!mbar_wait(bar(B_SFULL + sb), (j >> 1) & 1)) fail();
@@ -566,42 +644,41 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
   }
 }
 
-// LSE merge of units cut by CTA boundaries. Block i looks at the boundary where CTA
-// i's range starts; if it falls inside a unit and i is the first non-empty CTA
-// after the one that started that unit, it merges the unit: the tail piece of that
-// CTA plus the head pieces of every later CTA the unit reaches. Warp = 16 rows,
-// lane = 4 output columns.
+// LSE merge of units cut by range boundaries. Block k looks at the boundary where
+// virtual CTA k's range starts; if it falls inside a unit and k is the first
+// non-empty virtual CTA after the one that started that unit, it merges the unit:
+// the tail piece of that virtual CTA plus the head pieces of every later virtual
+// CTA the unit reaches. Warp = 16 rows, lane = 4 output columns.
 __global__ void __launch_bounds__(256) prefill_merge_kernel(PrefillArgs a, int G) {
   using namespace pf;
-  const int i = blockIdx.x;
+  const int64_t k = blockIdx.x, V = (int64_t)kRounds * G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t W = pf_total_work(a);
-  const int64_t start = cta_tile_start(i, W, G);
-  if (i == 0 || start >= W || cta_tile_start(i + 1, W, G) == start) return;
+  auto empty = [&](int64_t v) { return pf_vbound(v + 1, W, G) == pf_vbound(v, W, G); };
+  const int64_t start = pf_vbound(k, W, G);
+  if (k == 0 || start >= W || empty(k)) return;
   PfCursor c;
-  pf_seek(c, a, start, W);
+  pf_locate(c, a, start);
   if (c.b >= a.B || c.t == c.seg_base) return;  // boundary at a unit start: nothing cut here
   const int64_t seg_end = c.seg_base + c.n;
-  const int64_t i0 = cta_of_tile(c.seg_base, W, G);
-  // First non-empty CTA after i0.
+  const int64_t i0 = pf_vcta_of_tile(c.seg_base, W, G);
   int64_t first_after = i0 + 1;
-  while (first_after < G && cta_tile_start(first_after + 1, W, G) == cta_tile_start(first_after, W, G))
-    ++first_after;
-  if (first_after != i) return;
-  const int64_t i1 = cta_of_tile(seg_end - 1, W, G);
+  while (first_after < V && empty(first_after)) ++first_after;
+  if (first_after != k) return;
+  const int64_t i1 = pf_vcta_of_tile(seg_end - 1, W, G);
   for (int rr = warp; rr < M; rr += 8) {
     const int tok = c.qt * a.qt_tokens + rr / a.n_rep;
     if (tok >= c.s.qlen) continue;
     float mx = a.ws_lse[(i0 * 2 + 1) * M + rr];
-    for (int64_t k = i0 + 1; k <= i1; ++k) {
-      if (cta_tile_start(k + 1, W, G) == cta_tile_start(k, W, G)) continue;
-      mx = fmaxf(mx, a.ws_lse[(k * 2) * M + rr]);
+    for (int64_t v = i0 + 1; v <= i1; ++v) {
+      if (empty(v)) continue;
+      mx = fmaxf(mx, a.ws_lse[(v * 2) * M + rr]);
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
-    for (int64_t k = i0; k <= i1; ++k) {
-      if (k > i0 && cta_tile_start(k + 1, W, G) == cta_tile_start(k, W, G)) continue;
-      const int64_t slot = k * 2 + (k == i0 ? 1 : 0);
+    for (int64_t v = i0; v <= i1; ++v) {
+      if (v > i0 && empty(v)) continue;
+      const int64_t slot = v * 2 + (v == i0 ? 1 : 0);
       const float l2 = a.ws_lse[slot * M + rr];
       const float w = (l2 == -INFINITY) ? 0.f : exp2f(l2 - mx);
       const float4 x = reinterpret_cast<const float4*>(a.ws_o + (slot * M + rr) * D)[lane];
@@ -629,8 +706,9 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(PrefillArgs a, int G
 // after the clamp; rows of a zero-length sequence have no queries) need no fill.
 
 size_t prefill_workspace_bytes(int G) {
-  const size_t o_bytes = (size_t)G * 2 * pf::M * pf::D * 4;
-  const size_t l_bytes = ((size_t)G * 2 * pf::M * 4 + 255) / 256 * 256;
+  const size_t slots = (size_t)kRounds * G * 2;
+  const size_t o_bytes = slots * pf::M * pf::D * 4;
+  const size_t l_bytes = (slots * pf::M * 4 + 255) / 256 * 256;
   return o_bytes + l_bytes;
 }
 
@@ -659,7 +737,8 @@ cudaError_t launch_prefill(const void* q, const int32_t* cu_q, const void* k_cac
   a.T = T;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.ws_o = reinterpret_cast<float*>(ws);
-  a.ws_lse = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + (size_t)num_sms * 2 * M * D * 4);
+  a.ws_lse = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) +
+                                      (size_t)kRounds * num_sms * 2 * M * D * 4);
 
   CUtensorMap tq, tk, tv;
   const uint64_t qdims[3] = {D, (uint64_t)H, (uint64_t)T};
@@ -677,7 +756,7 @@ cudaError_t launch_prefill(const void* q, const int32_t* cu_q, const void* k_cac
   prefill_tc_kernel<<<num_sms, NTHREADS, SMEM_BYTES, stream>>>(a, tq, tk, tv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  prefill_merge_kernel<<<num_sms, 256, 0, stream>>>(a, num_sms);
+  prefill_merge_kernel<<<kRounds * num_sms, 256, 0, stream>>>(a, num_sms);
   return cudaGetLastError();
 }
 
