@@ -82,9 +82,17 @@ int64_t pkv_pool_num_free(const pkv_pool* pool);
 /* Pop n ids from the head of the queue into ids_out[n]; all-or-nothing
  * (PKV_ERR_OUT_OF_BLOCKS leaves the pool unchanged). */
 int pkv_pool_alloc(pkv_pool* pool, int64_t n, int32_t* ids_out);
-/* Append ids[n] to the tail; PKV_ERR_DOUBLE_FREE (pool unchanged) if any id is
- * free already, is the null block, repeats, or is out of range. */
+/* Drop one reference per listed id; an id whose count reaches zero goes back to
+ * the queue tail, in the listed order. PKV_ERR_DOUBLE_FREE (pool unchanged) if an
+ * id is out of range, is the null block, or is listed more often than it is
+ * referenced (an unshared block: free already, or listed twice). */
 int pkv_pool_free(pkv_pool* pool, const int32_t* ids, int64_t n);
+/* One more reference to each of ids[n], all currently held (a block shared by a
+ * forked request, "KV Cache 笔记" fork_blocks). PKV_ERR_INVALID_ARG (pool
+ * unchanged) if an id is free, out of range or the null block. */
+int pkv_pool_share(pkv_pool* pool, const int32_t* ids, int64_t n);
+/* Reference count of one block (0 = free or the null block; -1 = bad id). */
+int32_t pkv_pool_ref_count(const pkv_pool* pool, int32_t id);
 
 /* Skipped tokens of a manager after n computed tokens: 0 for full attention
  * (window <= 0), max(0, n - window + 1) for a sliding window
@@ -119,6 +127,91 @@ int64_t pkv_block_num_full_online(int64_t available_bytes, int64_t per_token_byt
                                   int64_t block_size);
 
 /* ==========================================================================
+ * Request-level allocator ("KV Cache 管理设计文档" §2-§3; prefix sharing and
+ * fork from "KV Cache 笔记", HF continuous batching). Host memory only.
+ * ========================================================================== */
+
+/* KVCacheManager over one manager per attention type (§2.2-§2.3). Type i has
+ * window windows[i] (0 = full attention, > 0 = sliding window of that many
+ * tokens), its own BlockPool of num_blocks[i] ids whose queue starts as
+ * initial_orders[i] (NULL, or a NULL entry = 0,1,2,...), and group id i in block
+ * fingerprints. At most one full-attention and one sliding-window type
+ * (PKV_ERR_INVALID_ARG otherwise). prefix_caching != 0 turns on prefix sharing for
+ * full-attention types. Owned by the caller (pkv_manager_destroy). Not
+ * thread-safe. Request ids are any int64 values. */
+typedef struct pkv_kv_manager pkv_kv_manager;
+int pkv_manager_create(int32_t num_types, const int32_t* windows, const int64_t* num_blocks,
+                       const int32_t* const* initial_orders, int32_t block_size,
+                       int64_t max_model_len, int32_t prefix_caching, pkv_kv_manager** out);
+void pkv_manager_destroy(pkv_kv_manager* mgr);
+
+/* allocate_slots (§3): the request will hold K/V for positions
+ * [0, min(computed + num_new + lookahead, max_model_len)). Phase 1, type by type:
+ * give back the blocks of a sliding window that no query from position
+ * min(computed, max_model_len) on can see (remove_skipped_blocks: they become the
+ * null block), then count the new blocks the type needs; return 0 at the first
+ * type whose pool cannot supply them, with nothing allocated. Phase 2: append the
+ * new entries in every type (leading entries wholly before position
+ * computed - W + 1 are the null block, the rest come from the pool in FIFO order).
+ * Returns 1 (allocated), 0 (not enough blocks) or a negative error. */
+int pkv_manager_allocate_slots(pkv_kv_manager* mgr, int64_t request_id, int64_t computed_tokens,
+                               int64_t num_new_tokens, int64_t lookahead_tokens);
+/* Logical block list of a request in type `type` (get_block_ids): writes up to
+ * `capacity` ids and returns the list's length (0 for an unknown request). */
+int64_t pkv_manager_get_block_ids(const pkv_kv_manager* mgr, int64_t request_id, int32_t type,
+                                  int32_t* ids_out, int64_t capacity);
+/* Release every block of the request in every type (free); unknown ids are a no-op. */
+int pkv_manager_free(pkv_kv_manager* mgr, int64_t request_id);
+int64_t pkv_manager_num_free(const pkv_kv_manager* mgr, int32_t type);
+int32_t pkv_manager_null_block(const pkv_kv_manager* mgr, int32_t type);
+int32_t pkv_manager_ref_count(const pkv_kv_manager* mgr, int32_t type, int32_t block);
+/* format_usage: "full:used/total,sliding:used/total" in type order; used = blocks
+ * handed out (the null block not counted), total = the pool's size. Writes a
+ * NUL-terminated string (truncated to capacity) and returns its full length. */
+int64_t pkv_manager_format_usage(const pkv_kv_manager* mgr, char* buf, int64_t capacity);
+/* prepare_block_tables (§4.2.2) for type `type`: row b is request_ids[b]'s list,
+ * padded with the null block, into table_out[B, max_blocks_per_seq].
+ * PKV_ERR_INVALID_ARG if a list is longer than max_blocks_per_seq. */
+int pkv_manager_block_table(const pkv_kv_manager* mgr, int32_t type, const int64_t* request_ids,
+                            int32_t B, int32_t max_blocks_per_seq, int32_t* table_out);
+
+/* Block fingerprint: BLAKE2b (RFC 7693) with an 8-byte digest, read little-endian,
+ * over [parent_hash as 8 little-endian bytes, only when has_parent] + tokens as
+ * int32 little-endian + group_id as int32 little-endian. The same in every process
+ * (the pages' reason for not using a salted built-in hash). */
+uint64_t pkv_block_hash(uint64_t parent_hash, int32_t has_parent, const int32_t* tokens,
+                        int32_t num_tokens, int32_t group_id);
+/* Prefix match for a new request (search_prefix_match): the longest run of
+ * leading full blocks of tokens[num_tokens] whose fingerprint chain is held by a
+ * live request in every type, never including the block of the last token, is
+ * attached to request_id (one more reference per block). Returns the number of
+ * cached tokens (a multiple of block_size; 0 with prefix caching off or a
+ * sliding-window type present), or a negative error if request_id already holds
+ * blocks. Follow with allocate_slots(request_id, cached, num_tokens - cached). */
+int64_t pkv_manager_match_prefix(pkv_kv_manager* mgr, int64_t request_id, const int32_t* tokens,
+                                 int64_t num_tokens);
+/* Fingerprint the request's full blocks that are not fingerprinted yet, from its
+ * tokens (call after their K/V is computed). A fingerprint already taken by
+ * another block keeps that block. Fingerprints are forgotten when their block's
+ * last reference is released. No-op without prefix caching. */
+int pkv_manager_cache_blocks(pkv_kv_manager* mgr, int64_t request_id, const int32_t* tokens,
+                             int64_t num_tokens);
+/* fork_blocks: each of child_ids[num_children] (new requests) gets the first
+ * ceil(num_tokens / block_size) entries of the parent's list. shareable != 0:
+ * full blocks are shared (one more reference per child) and only an incomplete
+ * last block is replaced by a new block to be copied; shareable == 0: every real
+ * block is replaced by a new one to be copied. Null entries stay null. The copies
+ * (source, destination) are written type by type, child by child, to
+ * copy_src/copy_dst (capacity entries), and copies_per_type[num_types] gets each
+ * type's count; run pkv_copy_blocks on every cache of a type with its pairs.
+ * All-or-nothing: PKV_ERR_OUT_OF_BLOCKS or a too-small capacity
+ * (PKV_ERR_INVALID_ARG) leaves everything unchanged. Returns the total copies. */
+int64_t pkv_manager_fork(pkv_kv_manager* mgr, int64_t parent_id, const int64_t* child_ids,
+                         int32_t num_children, int64_t num_tokens, int32_t shareable,
+                         int32_t* copy_src, int32_t* copy_dst, int64_t capacity,
+                         int64_t* copies_per_type);
+
+/* ==========================================================================
  * Device calls
  * ========================================================================== */
 
@@ -137,6 +230,18 @@ int pkv_kv_cache_write(void* k_cache, void* v_cache, const void* k, const void* 
                        const int32_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
                        int32_t block_size, int32_t num_kv_heads, int32_t head_dim_k,
                        int32_t head_dim_v, int* dev_status, void* stream);
+
+/* Block copy for a fork ("KV Cache 笔记", fork_blocks: the incomplete last block
+ * of a forked request is copied, full blocks are shared). cache is one device
+ * cache tensor whose blocks are contiguous rows of block_bytes (any
+ * [num_blocks, block_size, heads, dim] cache: block_bytes = block_size * heads *
+ * dim * element size). For i in [0, n): block dst[i] becomes a bit copy of block
+ * src[i]; src and dst are device int32 arrays. Sources must not be destinations of
+ * the same call (pkv_manager_fork's pairs never are). A pair with an id outside
+ * [0, num_blocks) is skipped and sets PKV_DEV_BAD_BLOCK. block_bytes must be a
+ * positive multiple of 16 and cache 16-byte aligned (PKV_ERR_INVALID_ARG). */
+int pkv_copy_blocks(void* cache, int64_t num_blocks, int64_t block_bytes, const int32_t* src,
+                    const int32_t* dst, int64_t n, int* dev_status, void* stream);
 
 /* Decode attention, one query token per sequence (sparse_mode 0 / band 4).
  * For each b, h: o = softmax(scale * q[b,h] . K^T) V over positions

@@ -20,6 +20,23 @@ SIGNATURES = {
     "pkv_pool_num_free": (i64, [vp]),
     "pkv_pool_alloc": (C.c_int, [vp, i64, vp]),
     "pkv_pool_free": (C.c_int, [vp, vp, i64]),
+    "pkv_pool_share": (C.c_int, [vp, vp, i64]),
+    "pkv_pool_ref_count": (i32, [vp, i32]),
+    "pkv_manager_create": (C.c_int, [i32, vp, vp, vp, i32, i64, i32, C.POINTER(vp)]),
+    "pkv_manager_destroy": (None, [vp]),
+    "pkv_manager_allocate_slots": (C.c_int, [vp, i64, i64, i64, i64]),
+    "pkv_manager_get_block_ids": (i64, [vp, i64, i32, vp, i64]),
+    "pkv_manager_free": (C.c_int, [vp, i64]),
+    "pkv_manager_num_free": (i64, [vp, i32]),
+    "pkv_manager_null_block": (i32, [vp, i32]),
+    "pkv_manager_ref_count": (i32, [vp, i32, i32]),
+    "pkv_manager_format_usage": (i64, [vp, C.c_char_p, i64]),
+    "pkv_manager_block_table": (C.c_int, [vp, i32, vp, i32, i32, vp]),
+    "pkv_block_hash": (C.c_uint64, [C.c_uint64, i32, vp, i32, i32]),
+    "pkv_manager_match_prefix": (i64, [vp, i64, vp, i64]),
+    "pkv_manager_cache_blocks": (C.c_int, [vp, i64, vp, i64]),
+    "pkv_manager_fork": (i64, [vp, i64, vp, i32, i64, i32, vp, vp, i64, vp]),
+    "pkv_copy_blocks": (C.c_int, [vp, i64, i64, vp, vp, i64, vp, vp]),
     "pkv_num_skipped_tokens": (i64, [i64, i64]),
     "pkv_build_block_table": (C.c_int, [vp, vp, i32, i32, i32, i32, vp]),
     "pkv_build_block_table_arange": (C.c_int, [i32, i32, vp]),

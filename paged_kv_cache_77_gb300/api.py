@@ -77,6 +77,13 @@ class BlockPool:
         ids = np.ascontiguousarray(ids, dtype=np.int32)
         check(load().pkv_pool_free(self._h, _np_ptr(ids), len(ids)), "pkv_pool_free")
 
+    def share(self, ids) -> None:
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        check(load().pkv_pool_share(self._h, _np_ptr(ids), len(ids)), "pkv_pool_share")
+
+    def ref_count(self, block: int) -> int:
+        return load().pkv_pool_ref_count(self._h, block)
+
     def build_block_table(self, seq_lens, block_size: int, window: int,
                           max_blocks_per_seq: int) -> np.ndarray:
         lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
@@ -85,6 +92,113 @@ class BlockPool:
                                            max_blocks_per_seq, _np_ptr(table)),
               "pkv_build_block_table")
         return table
+
+
+class KVCacheManager:
+    """Handle on the library's request-level allocator (pkv_manager_*).
+
+    windows[i] = 0: full attention; > 0: sliding window. One pool per type."""
+
+    def __init__(self, windows, num_blocks, block_size: int, max_model_len: int,
+                 prefix_caching: bool = False, initial_orders=None):
+        lib = load()
+        self.num_types = len(windows)
+        w = np.ascontiguousarray(windows, dtype=np.int32)
+        n = np.ascontiguousarray(num_blocks, dtype=np.int64)
+        self._orders = None
+        orders_arg = None
+        if initial_orders is not None:
+            self._orders = [None if o is None else np.ascontiguousarray(o, dtype=np.int32)
+                            for o in initial_orders]
+            arr = (C.c_void_p * self.num_types)(*[None if o is None else o.ctypes.data
+                                                 for o in self._orders])
+            self._orders_arr = arr
+            orders_arg = C.cast(arr, C.c_void_p)
+        self._h = C.c_void_p()
+        check(lib.pkv_manager_create(self.num_types, _np_ptr(w), _np_ptr(n), orders_arg, block_size,
+                                     max_model_len, int(prefix_caching), C.byref(self._h)),
+              "pkv_manager_create")
+        self.block_size = block_size
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            load().pkv_manager_destroy(self._h)
+            self._h = None
+
+    def allocate_slots(self, request_id: int, computed_tokens: int, num_new_tokens: int,
+                       lookahead_tokens: int = 0) -> bool:
+        return check(load().pkv_manager_allocate_slots(self._h, request_id, computed_tokens,
+                                                       num_new_tokens, lookahead_tokens),
+                     "pkv_manager_allocate_slots") == 1
+
+    def get_block_ids(self, request_id: int) -> list[list[int]]:
+        out = []
+        for t in range(self.num_types):
+            n = check(load().pkv_manager_get_block_ids(self._h, request_id, t, None, 0),
+                      "pkv_manager_get_block_ids")
+            buf = np.empty(max(n, 1), dtype=np.int32)
+            load().pkv_manager_get_block_ids(self._h, request_id, t, _np_ptr(buf), n)
+            out.append(buf[:n].tolist())
+        return out
+
+    def free(self, request_id: int) -> None:
+        check(load().pkv_manager_free(self._h, request_id), "pkv_manager_free")
+
+    def num_free(self, type_idx: int = 0) -> int:
+        return load().pkv_manager_num_free(self._h, type_idx)
+
+    def null_block(self, type_idx: int = 0) -> int:
+        return load().pkv_manager_null_block(self._h, type_idx)
+
+    def ref_count(self, type_idx: int, block: int) -> int:
+        return load().pkv_manager_ref_count(self._h, type_idx, block)
+
+    def format_usage(self) -> str:
+        n = check(load().pkv_manager_format_usage(self._h, None, 0), "pkv_manager_format_usage")
+        buf = C.create_string_buffer(n + 1)
+        load().pkv_manager_format_usage(self._h, buf, n + 1)
+        return buf.value.decode()
+
+    def block_table(self, type_idx: int, request_ids, max_blocks_per_seq: int) -> np.ndarray:
+        ids = np.ascontiguousarray(request_ids, dtype=np.int64)
+        table = np.empty((len(ids), max_blocks_per_seq), dtype=np.int32)
+        check(load().pkv_manager_block_table(self._h, type_idx, _np_ptr(ids), len(ids),
+                                             max_blocks_per_seq, _np_ptr(table)),
+              "pkv_manager_block_table")
+        return table
+
+    def match_prefix(self, request_id: int, tokens) -> int:
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        return check(load().pkv_manager_match_prefix(self._h, request_id, _np_ptr(toks), len(toks)),
+                     "pkv_manager_match_prefix")
+
+    def cache_blocks(self, request_id: int, tokens) -> None:
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        check(load().pkv_manager_cache_blocks(self._h, request_id, _np_ptr(toks), len(toks)),
+              "pkv_manager_cache_blocks")
+
+    def fork(self, parent_id: int, child_ids, num_tokens: int, shareable: bool):
+        """Returns one list of (src, dst) copies per type."""
+        kids = np.ascontiguousarray(child_ids, dtype=np.int64)
+        held = max(len(r) for r in self.get_block_ids(parent_id))
+        cap = max(1, held * len(kids) * self.num_types)
+        src = np.empty(cap, dtype=np.int32)
+        dst = np.empty(cap, dtype=np.int32)
+        per = np.zeros(self.num_types, dtype=np.int64)
+        check(load().pkv_manager_fork(self._h, parent_id, _np_ptr(kids), len(kids), num_tokens,
+                                      int(shareable), _np_ptr(src), _np_ptr(dst), cap, _np_ptr(per)),
+              "pkv_manager_fork")
+        out, k = [], 0
+        for t in range(self.num_types):
+            out.append([(int(src[i]), int(dst[i])) for i in range(k, k + int(per[t]))])
+            k += int(per[t])
+        return out
+
+
+def block_hash(parent, tokens, group_id: int) -> int:
+    toks = np.ascontiguousarray(tokens, dtype=np.int32)
+    return int(load().pkv_block_hash(0 if parent is None else parent, int(parent is not None),
+                                     _np_ptr(toks), len(toks), group_id))
 
 
 def build_block_table_arange(batch: int, blocks_per_seq: int) -> np.ndarray:
@@ -141,6 +255,21 @@ def kv_cache_write(k_cache, v_cache, k, v, slot_mapping, dev_status=None, stream
 
 
 KERNEL_AUTO, KERNEL_CUDA_CORE, KERNEL_TENSOR_CORE = 0, 1, 2
+
+
+def copy_blocks(cache, src, dst, dev_status=None, stream=None) -> None:
+    """Block dst[i] of `cache` ([num_blocks, ...], contiguous, CUDA) becomes a bit copy
+    of block src[i] (the device side of a fork)."""
+    if not (cache.is_cuda and cache.is_contiguous()):
+        raise ValueError("cache must be a contiguous CUDA tensor")
+    _dev_i32(src, "src")
+    _dev_i32(dst, "dst")
+    if src.numel() != dst.numel():
+        raise ValueError("src and dst differ in length")
+    block_bytes = cache[0].numel() * cache.element_size()
+    check(load().pkv_copy_blocks(_ptr(cache), cache.shape[0], block_bytes, _ptr(src), _ptr(dst),
+                                 src.numel(), _ptr(dev_status), _stream(stream)),
+          "pkv_copy_blocks")
 
 
 def set_decode_kernel(kernel: int) -> None:

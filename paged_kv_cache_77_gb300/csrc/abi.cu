@@ -62,6 +62,18 @@ int pkv_kv_cache_write(void* k_cache, void* v_cache, const void* k, const void* 
                        "pkv_kv_cache_write");
 }
 
+int pkv_copy_blocks(void* cache, int64_t num_blocks, int64_t block_bytes, const int32_t* src,
+                    const int32_t* dst, int64_t n, int* dev_status, void* stream) {
+  PKV_REQUIRE(num_blocks > 0 && n >= 0 && block_bytes > 0 && block_bytes % 16 == 0,
+              PKV_ERR_INVALID_ARG, "pkv_copy_blocks: bad sizes");
+  PKV_REQUIRE(cache && aligned16(cache) && (n == 0 || (src && dst)), PKV_ERR_INVALID_ARG,
+              "pkv_copy_blocks: null or misaligned pointer");
+  clear_error();
+  return launch_status(launch_copy_blocks(cache, num_blocks, block_bytes, src, dst, n, dev_status,
+                                          (cudaStream_t)stream, current_num_sms()),
+                       "pkv_copy_blocks");
+}
+
 int pkv_set_decode_kernel(int32_t kernel) {
   PKV_REQUIRE(kernel >= PKV_KERNEL_AUTO && kernel <= PKV_KERNEL_TENSOR_CORE, PKV_ERR_INVALID_ARG,
               "pkv_set_decode_kernel: unknown kernel %d", kernel);

@@ -6,12 +6,10 @@
 // prepare_slot_mapping; and "KVCache 优化技能" §3.1-3.3 for the slot formula and
 // the static arange table.
 #include <cstring>
-#include <deque>
-#include <mutex>
-#include <unordered_set>
 #include <vector>
 
 #include "abi_common.h"
+#include "host_pool.h"
 
 namespace pkv {
 
@@ -30,13 +28,6 @@ void clear_error() { g_last_error.clear(); }
 
 }  // namespace pkv
 
-struct pkv_pool {
-  int64_t num_blocks = 0;
-  int32_t null_block = 0;
-  std::deque<int32_t> queue;          // free ids, FIFO
-  std::vector<uint8_t> is_free;       // membership set, O(1) double-free check
-};
-
 extern "C" {
 
 const char* pkv_last_error(void) { return pkv::g_last_error.c_str(); }
@@ -49,19 +40,19 @@ int pkv_pool_create(int64_t num_blocks, const int32_t* initial_order, pkv_pool**
               "pkv_pool_create: num_blocks %lld out of range", (long long)num_blocks);
   auto* p = new pkv_pool();
   p->num_blocks = num_blocks;
-  p->is_free.assign(num_blocks, 0);
+  std::vector<uint8_t> seen(num_blocks, 0);
   for (int64_t i = 0; i < num_blocks; ++i) {
     int32_t id = initial_order ? initial_order[i] : (int32_t)i;
-    if (id < 0 || id >= num_blocks || p->is_free[id]) {
+    if (id < 0 || id >= num_blocks || seen[id]) {
       delete p;
       PKV_FAIL(PKV_ERR_INVALID_ARG, "pkv_pool_create: initial_order is not a permutation");
     }
-    p->is_free[id] = 1;
+    seen[id] = 1;
     p->queue.push_back(id);
   }
+  p->ref.assign(num_blocks, 0);
   p->null_block = p->queue.front();  // first popped id: the placeholder block
   p->queue.pop_front();
-  p->is_free[p->null_block] = 0;
   *out = p;
   pkv::clear_error();
   return PKV_OK;
@@ -78,32 +69,34 @@ int pkv_pool_alloc(pkv_pool* pool, int64_t n, int32_t* ids_out) {
   PKV_REQUIRE((int64_t)pool->queue.size() >= n, PKV_ERR_OUT_OF_BLOCKS,
               "pkv_pool_alloc: need %lld blocks, %lld free", (long long)n,
               (long long)pool->queue.size());
-  for (int64_t i = 0; i < n; ++i) {
-    int32_t id = pool->queue.front();
-    pool->queue.pop_front();
-    pool->is_free[id] = 0;
-    ids_out[i] = id;
-  }
+  pkv::pool_take(pool, n, ids_out);
   return PKV_OK;
 }
 
 int pkv_pool_free(pkv_pool* pool, const int32_t* ids, int64_t n) {
   PKV_REQUIRE(pool && (n == 0 || ids) && n >= 0, PKV_ERR_INVALID_ARG, "pkv_pool_free: bad args");
   // Validate everything first so that a failing call leaves the pool unchanged.
-  std::unordered_set<int32_t> seen;
-  for (int64_t i = 0; i < n; ++i) {
-    int32_t id = ids[i];
-    PKV_REQUIRE(id >= 0 && id < pool->num_blocks, PKV_ERR_DOUBLE_FREE,
-                "pkv_pool_free: id %d out of range", id);
-    PKV_REQUIRE(id != pool->null_block, PKV_ERR_DOUBLE_FREE, "pkv_pool_free: null block %d", id);
-    PKV_REQUIRE(!pool->is_free[id] && seen.insert(id).second, PKV_ERR_DOUBLE_FREE,
-                "pkv_pool_free: block %d is already free", id);
-  }
-  for (int64_t i = 0; i < n; ++i) {
-    pool->queue.push_back(ids[i]);
-    pool->is_free[ids[i]] = 1;
-  }
+  PKV_REQUIRE(pkv::pool_release_ok(pool, ids, n), PKV_ERR_DOUBLE_FREE,
+              "pkv_pool_free: an id is out of range, the null block, or released more often "
+              "than it is referenced");
+  pkv::pool_release(pool, ids, n, nullptr);
   return PKV_OK;
+}
+
+int pkv_pool_share(pkv_pool* pool, const int32_t* ids, int64_t n) {
+  PKV_REQUIRE(pool && (n == 0 || ids) && n >= 0, PKV_ERR_INVALID_ARG, "pkv_pool_share: bad args");
+  for (int64_t i = 0; i < n; ++i) {
+    const int32_t id = ids[i];
+    PKV_REQUIRE(id >= 0 && id < pool->num_blocks && id != pool->null_block && pool->ref[id] > 0,
+                PKV_ERR_INVALID_ARG, "pkv_pool_share: block %d is not held", id);
+  }
+  for (int64_t i = 0; i < n; ++i) ++pool->ref[ids[i]];
+  return PKV_OK;
+}
+
+int32_t pkv_pool_ref_count(const pkv_pool* pool, int32_t id) {
+  if (!pool || id < 0 || id >= pool->num_blocks) return -1;
+  return pool->ref[id];
 }
 
 int64_t pkv_num_skipped_tokens(int64_t num_computed_tokens, int64_t window) {
@@ -139,12 +132,8 @@ int pkv_build_block_table(pkv_pool* pool, const int32_t* seq_lens, int32_t B, in
     int32_t* row = table_out + (int64_t)b * max_blocks_per_seq;
     int64_t j = 0;
     for (; j < n_null[b]; ++j) row[j] = pool->null_block;
-    for (int64_t k = 0; k < n_live[b]; ++k, ++j) {
-      int32_t id = pool->queue.front();
-      pool->queue.pop_front();
-      pool->is_free[id] = 0;
-      row[j] = id;
-    }
+    pkv::pool_take(pool, n_live[b], row + j);
+    j += n_live[b];
     for (; j < max_blocks_per_seq; ++j) row[j] = pool->null_block;
   }
   return PKV_OK;

@@ -63,4 +63,45 @@ cudaError_t launch_kv_write(void* k_cache, void* v_cache, const void* k, const v
   return cudaGetLastError();
 }
 
+// copy_blocks: block dst[i] of one cache becomes a bit copy of block src[i] (the
+// copied incomplete last block of a forked request, "KV Cache 笔记" fork_blocks).
+// One thread moves one 16-byte chunk of the flattened (pair, chunk) space, so a
+// few large blocks still spread over the whole GPU. Sources are never destinations
+// of the same call, so the non-coherent loads see unchanged data.
+// Roofline: HBM; algorithmic bytes per pair = 2 * block_bytes + 8 bytes of ids.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint8_t* __restrict__ cache,
+                                                          int64_t num_blocks, int64_t chunks,
+                                                          const int32_t* __restrict__ src,
+                                                          const int32_t* __restrict__ dst,
+                                                          int64_t n, int* dev_status) {
+  const int64_t total = n * chunks;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = idx / chunks;
+    const int64_t c = idx - i * chunks;
+    const int32_t s = __ldg(src + i), d = __ldg(dst + i);
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+      if (c == 0) flag_status(dev_status, PKV_DEV_BAD_BLOCK);
+      continue;
+    }
+    const uint4 w = ld_nc_v4(cache + ((int64_t)s * chunks + c) * 16);
+    *reinterpret_cast<uint4*>(cache + ((int64_t)d * chunks + c) * 16) = w;
+  }
+}
+
+cudaError_t launch_copy_blocks(void* cache, int64_t num_blocks, int64_t block_bytes,
+                               const int32_t* src, const int32_t* dst, int64_t n, int* dev_status,
+                               cudaStream_t stream, int num_sms) {
+  const int64_t chunks = block_bytes / 16;
+  const int64_t total = n * chunks;
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = (int64_t)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  copy_blocks_kernel<<<(unsigned)blocks, threads, 0, stream>>>((uint8_t*)cache, num_blocks, chunks,
+                                                              src, dst, n, dev_status);
+  return cudaGetLastError();
+}
+
 }  // namespace pkv

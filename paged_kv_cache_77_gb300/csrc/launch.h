@@ -10,6 +10,9 @@ cudaError_t launch_kv_write(void* k_cache, void* v_cache, const void* k, const v
                             const int32_t* slots, int64_t num_tokens, int64_t num_slots,
                             int64_t row_k_bytes, int64_t row_v_bytes, int* dev_status,
                             cudaStream_t stream, int num_sms);
+cudaError_t launch_copy_blocks(void* cache, int64_t num_blocks, int64_t block_bytes,
+                               const int32_t* src, const int32_t* dst, int64_t n, int* dev_status,
+                               cudaStream_t stream, int num_sms);
 
 // Arguments of the split-KV decode kernels and their LSE merge.
 struct DecodeArgs {
