@@ -237,6 +237,10 @@ def run_ours(args):
                            "tensor_core": api.KERNEL_TENSOR_CORE}[args.decode_kernel])
     if args.workload == "scatter":
         return run_scatter(args, dev)
+    if args.workload == "fork":
+        return run_fork(args, dev)
+    if args.workload == "mla_write":
+        return run_mla_write(args, dev)
     if args.workload == "mla":
         return run_mla(args, dev)
     if args.workload == "mixed_prefill":
@@ -588,6 +592,129 @@ def run_scatter(args, dev):
         "gpu_launches": args.steps, "clocks": clocks}), flush=True)
 
 
+def run_fork(args, dev):
+    """Fork of 512 parent requests (prompt ~ U[1, 4096] tokens, H_kv 8, d 128, bs 128)
+    into 4 children each through the library's allocator with shared full blocks:
+    the timed step is the device copy of every incomplete last block in the K and
+    the V cache (pkv_copy_blocks). Host costs of the allocator are reported beside."""
+    import torch
+
+    from paged_kv_cache_77_gb300 import api
+
+    parents, kids, hkv, d, bs = args.batch or 512, 4, 8, 128, 128
+    rng = np.random.default_rng(1006)
+    prompts = rng.integers(1, 4097, size=parents)
+    nb = int(sum(-(-int(n) // bs) for n in prompts)) + parents * kids + 1
+    mgr = api.KVCacheManager([0], [nb], bs, 1 << 20, initial_orders=[rng.permutation(nb)])
+    t_alloc = time.perf_counter()
+    for i, n in enumerate(prompts):
+        assert mgr.allocate_slots(i, 0, int(n))
+    t_alloc = (time.perf_counter() - t_alloc) / parents
+    pairs = []
+    t_fork = time.perf_counter()
+    for i, n in enumerate(prompts):
+        pairs += mgr.fork(i, [parents + kids * i + c for c in range(kids)], int(n), True)[0]
+    t_fork = (time.perf_counter() - t_fork) / parents
+    t_dec = time.perf_counter()
+    ndec = 0
+    for i, n in enumerate(prompts[:64]):
+        for step in range(32):
+            mgr.allocate_slots(i, int(n) + step, 1)
+            ndec += 1
+    t_dec = (time.perf_counter() - t_dec) / ndec
+    g = torch.Generator(device=dev)
+    g.manual_seed(1006)
+    kc = torch.randn((nb, bs, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    vc = torch.randn((nb, bs, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    src = torch.tensor([a for a, _ in pairs], dtype=torch.int32, device=dev)
+    dst = torch.tensor([b for _, b in pairs], dtype=torch.int32, device=dev)
+    block_bytes = bs * hkv * d * 2
+    # K and V: each distinct source block read once (a parent's last block feeds all
+    # of its children; the repeats come from L2), every destination written, ids.
+    n_src = len({a for a, _ in pairs})
+    nbytes = 2 * block_bytes * (n_src + len(pairs)) + 8 * len(pairs)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        api.copy_blocks(kc, src, dst)
+        api.copy_blocks(vc, src, dst)
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(args.steps):
+        api.copy_blocks(kc, src, dst)
+        api.copy_blocks(vc, src, dst)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    hbm, _, peak_kind = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "fork block copy: achieved HBM GB/s", "value": gbs, "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"fork: {parents} parents x {kids} children, prompt U[1,4096], "
+                               f"H_kv {hkv} d {d}, {len(pairs)} copied blocks per cache "
+                               f"from {n_src} distinct sources",
+                   "l2": "inputs larger than L2 (%.2f GB moved per step)" % (nbytes / 1e9),
+                   "host_us_per_fork": t_fork * 1e6, "host_us_per_prefill_allocate": t_alloc * 1e6,
+                   "host_us_per_decode_allocate": t_dec * 1e6},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": gbs / hbm, "traffic": None, "peak_kind": peak_kind},
+        "gpu_launches": 2 * args.steps, "clocks": clocks}), flush=True)
+
+
+def run_mla_write(args, dev):
+    """Fused MLA cache write at bandwidth scale: 262,144 tokens of latent (512) + rope
+    (64) rows, RMSNorm + RoPE, written to distinct random slots of a 2,056-block
+    cache (pkv_mla_rmsnorm_rope_write, no k_nope / k_rope copies)."""
+    import torch
+
+    import synth
+    from paged_kv_cache_77_gb300 import api
+
+    T = args.batch or 262144
+    nb = -(-T // 128) + 8
+    v = synth.draw_mla_write(T, nb, 1007, device=dev)
+    nbytes = T * (1152 + 512 + 1152 + 4)  # latent read, cos+sin read, rows written, slot
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        api.mla_rmsnorm_rope_write(v["cache_nope"], v["cache_rope"], v["latent"], v["gamma"],
+                                   v["cos"], v["sin"], v["slots"], 1e-6)
+
+    for _ in range(args.warmup):
+        step()
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    hbm, _, peak_kind = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "fused MLA RMSNorm+RoPE cache write: achieved HBM GB/s", "value": gbs,
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"mla_write: {T} tokens x (latent 512 + rope 64), random slots",
+                   "l2": "inputs larger than L2 (%.2f GB moved per step)" % (nbytes / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": gbs / hbm, "traffic": None, "peak_kind": peak_kind},
+        "gpu_launches": args.steps, "clocks": clocks}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -595,7 +722,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa_long",
-                    choices=["gqa_long", "swa", "mha_tiny", "scatter", "mla", "mixed_prefill"])
+                    choices=["gqa_long", "swa", "mha_tiny", "scatter", "mla", "mixed_prefill",
+                             "fork", "mla_write"])
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

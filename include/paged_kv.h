@@ -243,6 +243,29 @@ int pkv_kv_cache_write(void* k_cache, void* v_cache, const void* k, const void* 
 int pkv_copy_blocks(void* cache, int64_t num_blocks, int64_t block_bytes, const int32_t* src,
                     const int32_t* dst, int64_t n, int* dev_status, void* stream);
 
+/* Fused MLA cache write (standalone guide 模式三: the kv_a projection output goes
+ * through kv_a_layernorm RMSNorm and RoPE and into nope_cache / rope_cache in one
+ * step, optionally returning k_nope / k_rope). For each token t:
+ *   k_nope[t] = bf16(x[0:512] / sqrt(mean(x[0:512]^2) + epsilon) * gamma)
+ *   k_rope[t] = bf16(x[512:576] * cos[t] + rotate_half(x[512:576]) * sin[t]),
+ *   rotate_half(r) = [-r[32:64], r[0:32]] (the Llama forward's RoPE, "KV Cache 笔记"),
+ * with x = latent[t], arithmetic in fp32 and round-to-nearest-even results;
+ * k_nope[t] goes to cache_nope row slot_mapping[t] and k_rope[t] to cache_rope.
+ *   cache_nope [num_blocks, block_size, 1, 512] bf16, cache_rope [.., 1, 64] bf16
+ *   k_nope_out [T, 512], k_rope_out [T, 64] bf16: optional copies (NULL = none)
+ *   latent [T, 576] bf16 (512 latent + 64 rope), gamma [512] bf16
+ *   cos, sin [T, 64] fp32 (per token, every rope element)
+ *   slot_mapping [T] int32: negative skips the cache write of the row; a slot
+ *   >= num_blocks * block_size is skipped and sets PKV_DEV_BAD_SLOT.
+ * kv_lora_rank must be 512 and rope_dim 64 (PKV_ERR_UNSUPPORTED). All pointers
+ * 16-byte aligned. Device pointers; asynchronous on `stream`. */
+int pkv_mla_rmsnorm_rope_write(void* cache_nope, void* cache_rope, void* k_nope_out,
+                               void* k_rope_out, const void* latent, const void* gamma,
+                               const float* cos, const float* sin, const int32_t* slot_mapping,
+                               int64_t num_tokens, int64_t num_blocks, int32_t block_size,
+                               int32_t kv_lora_rank, int32_t rope_dim, float epsilon,
+                               int* dev_status, void* stream);
+
 /* Decode attention, one query token per sequence (sparse_mode 0 / band 4).
  * For each b, h: o = softmax(scale * q[b,h] . K^T) V over positions
  * [max(0, len_b - window), len_b) (window <= 0: [0, len_b)) of sequence b, read

@@ -272,6 +272,26 @@ def copy_blocks(cache, src, dst, dev_status=None, stream=None) -> None:
           "pkv_copy_blocks")
 
 
+def mla_rmsnorm_rope_write(cache_nope, cache_rope, latent, gamma, cos, sin, slot_mapping,
+                           epsilon: float, k_nope_out=None, k_rope_out=None, dev_status=None,
+                           stream=None) -> None:
+    """Fused RMSNorm (latent 512) + RoPE (rope 64) + paged write of MLA rows."""
+    for t, n in ((cache_nope, "cache_nope"), (cache_rope, "cache_rope"), (latent, "latent"),
+                 (gamma, "gamma")):
+        _dev_bf16(t, n)
+    for t, n in ((cos, "cos"), (sin, "sin")):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+            raise ValueError(f"{n} must be a contiguous fp32 CUDA tensor")
+    _dev_i32(slot_mapping, "slot_mapping")
+    T = latent.shape[0]
+    nb, bs = cache_nope.shape[0], cache_nope.shape[1]
+    check(load().pkv_mla_rmsnorm_rope_write(
+        _ptr(cache_nope), _ptr(cache_rope), _ptr(k_nope_out), _ptr(k_rope_out), _ptr(latent),
+        _ptr(gamma), _ptr(cos), _ptr(sin), _ptr(slot_mapping), T, nb, bs, cache_nope.shape[-1],
+        cache_rope.shape[-1], epsilon, _ptr(dev_status), _stream(stream)),
+        "pkv_mla_rmsnorm_rope_write")
+
+
 def set_decode_kernel(kernel: int) -> None:
     """Select the decode kernel process-wide (KERNEL_AUTO / _CUDA_CORE / _TENSOR_CORE)."""
     check(load().pkv_set_decode_kernel(kernel), "pkv_set_decode_kernel")

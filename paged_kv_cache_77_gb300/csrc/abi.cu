@@ -74,6 +74,33 @@ int pkv_copy_blocks(void* cache, int64_t num_blocks, int64_t block_bytes, const 
                        "pkv_copy_blocks");
 }
 
+int pkv_mla_rmsnorm_rope_write(void* cache_nope, void* cache_rope, void* k_nope_out,
+                               void* k_rope_out, const void* latent, const void* gamma,
+                               const float* cos, const float* sin, const int32_t* slot_mapping,
+                               int64_t num_tokens, int64_t num_blocks, int32_t block_size,
+                               int32_t kv_lora_rank, int32_t rope_dim, float epsilon,
+                               int* dev_status, void* stream) {
+  PKV_REQUIRE(num_tokens >= 0 && num_blocks > 0 && block_size > 0, PKV_ERR_INVALID_ARG,
+              "pkv_mla_rmsnorm_rope_write: bad sizes");
+  PKV_REQUIRE(kv_lora_rank == 512 && rope_dim == 64, PKV_ERR_UNSUPPORTED,
+              "pkv_mla_rmsnorm_rope_write: only kv_lora_rank 512 and rope_dim 64 are implemented");
+  PKV_REQUIRE(std::isfinite(epsilon) && epsilon >= 0.f, PKV_ERR_INVALID_ARG,
+              "pkv_mla_rmsnorm_rope_write: epsilon must be finite and >= 0");
+  PKV_REQUIRE(cache_nope && cache_rope && gamma &&
+                  (num_tokens == 0 || (latent && cos && sin && slot_mapping)),
+              PKV_ERR_INVALID_ARG, "pkv_mla_rmsnorm_rope_write: null pointer");
+  PKV_REQUIRE(aligned16(cache_nope) && aligned16(cache_rope) && aligned16(k_nope_out) &&
+                  aligned16(k_rope_out) && aligned16(latent) && aligned16(gamma) && aligned16(cos) &&
+                  aligned16(sin),
+              PKV_ERR_INVALID_ARG, "pkv_mla_rmsnorm_rope_write: pointers must be 16-byte aligned");
+  clear_error();
+  return launch_status(
+      launch_mla_rmsnorm_rope_write(cache_nope, cache_rope, k_nope_out, k_rope_out, latent, gamma,
+                                    cos, sin, slot_mapping, num_tokens, num_blocks * block_size,
+                                    epsilon, dev_status, (cudaStream_t)stream, current_num_sms()),
+      "pkv_mla_rmsnorm_rope_write");
+}
+
 int pkv_set_decode_kernel(int32_t kernel) {
   PKV_REQUIRE(kernel >= PKV_KERNEL_AUTO && kernel <= PKV_KERNEL_TENSOR_CORE, PKV_ERR_INVALID_ARG,
               "pkv_set_decode_kernel: unknown kernel %d", kernel);

@@ -13,6 +13,12 @@ cudaError_t launch_kv_write(void* k_cache, void* v_cache, const void* k, const v
 cudaError_t launch_copy_blocks(void* cache, int64_t num_blocks, int64_t block_bytes,
                                const int32_t* src, const int32_t* dst, int64_t n, int* dev_status,
                                cudaStream_t stream, int num_sms);
+cudaError_t launch_mla_rmsnorm_rope_write(void* cache_nope, void* cache_rope, void* k_nope_out,
+                                          void* k_rope_out, const void* latent, const void* gamma,
+                                          const float* cosv, const float* sinv,
+                                          const int32_t* slots, int64_t num_tokens,
+                                          int64_t num_slots, float eps, int* dev_status,
+                                          cudaStream_t stream, int num_sms);
 
 // Arguments of the split-KV decode kernels and their LSE merge.
 struct DecodeArgs {

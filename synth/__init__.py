@@ -2,7 +2,7 @@
 
 Holds no addressing or attention arithmetic (see ``workloads``)."""
 from .workloads import (BF16_NAN_BITS, WORKLOADS, Draw, Workload, bf16_bits, draw, draw_explicit,
-                        values)
+                        draw_mla_write, values)
 
 __all__ = ["BF16_NAN_BITS", "WORKLOADS", "Draw", "Workload", "bf16_bits", "draw", "draw_explicit",
-           "values"]
+           "draw_mla_write", "values"]

@@ -203,3 +203,39 @@ def draw_explicit(wl: Workload, seq_lens, num_new=None, extra_blocks: int = 0) -
     num_blocks = int(nblk.sum()) + 1 + extra_blocks
     order = np.concatenate([[0], 1 + rng.permutation(num_blocks - 1)]).astype(np.int32)
     return Draw(seq_lens, num_new, start_pos, order, num_blocks, max(int(nblk.max()), 1))
+
+
+def draw_mla_write(num_tokens: int, num_blocks: int, seed: int, device="cpu", block_size: int = 128,
+                   rank: int = 512, rope: int = 64, neg_slots: int = 0) -> dict:
+    """Inputs of a fused MLA cache write (all drawn here, none computed by the op):
+
+    * latent [T, rank + rope] bf16: N(0,1) rows times a per-row scale exp(U[-2, 2]),
+      so the normalisation has work to do;
+    * gamma [rank] bf16: 1 + 0.1 N(0,1);
+    * cos, sin [T, rope] fp32: the usual RoPE tables of positions ~ U[0, 8192) with
+      frequencies 10000^(-2i/rope), i < rope/2, repeated for both halves;
+    * slots [T] int32: distinct slots of a [num_blocks, block_size] cache (a random
+      permutation), the first ``neg_slots`` replaced by -1;
+    * cache_nope [num_blocks, block_size, 1, rank], cache_rope [.., 1, rope] bf16 N(0,1).
+    Seeded with numpy default_rng(seed) and a torch generator seeded with seed."""
+    rng = np.random.default_rng(seed)
+    scale = np.exp(rng.uniform(-2.0, 2.0, size=(num_tokens, 1))).astype(np.float32)
+    pos = rng.integers(0, 8192, size=num_tokens).astype(np.float64)
+    inv_freq = 10000.0 ** (-np.arange(0, rope, 2, dtype=np.float64) / rope)
+    ang = pos[:, None] * inv_freq[None, :]
+    ang = np.concatenate([ang, ang], axis=1)
+    slots = rng.permutation(num_blocks * block_size)[:num_tokens].astype(np.int32)
+    slots[:neg_slots] = -1
+    g = _gen(device, seed)
+    latent = (torch.randn((num_tokens, rank + rope), generator=g, device=device)
+              * torch.from_numpy(scale).to(device)).to(torch.bfloat16)
+    gamma = (1.0 + 0.1 * torch.randn((rank,), generator=g, device=device)).to(torch.bfloat16)
+    cache_nope = _randn_bf16((num_blocks, block_size, 1, rank), g, device)
+    cache_rope = _randn_bf16((num_blocks, block_size, 1, rope), g, device)
+    return {
+        "latent": latent, "gamma": gamma,
+        "cos": torch.from_numpy(np.cos(ang).astype(np.float32)).to(device),
+        "sin": torch.from_numpy(np.sin(ang).astype(np.float32)).to(device),
+        "slots": torch.from_numpy(slots).to(device),
+        "cache_nope": cache_nope, "cache_rope": cache_rope,
+    }
