@@ -235,6 +235,10 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     api.set_decode_kernel({"auto": api.KERNEL_AUTO, "cuda_core": api.KERNEL_CUDA_CORE,
                            "tensor_core": api.KERNEL_TENSOR_CORE}[args.decode_kernel])
+    if args.kv_dtype == "fp8":
+        if args.workload not in ("gqa_long", "swa"):
+            raise SystemExit("--kv-dtype fp8 applies to the gqa_long and swa workloads")
+        return run_fp8(args, dev)
     if args.workload == "scatter":
         return run_scatter(args, dev)
     if args.workload == "fork":
@@ -383,6 +387,95 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_fp8(args, dev):
+    """Decode step over an FP8 (E4M3) cache: quantising write of the new rows +
+    paged_attention_decode_fp8. The cache is the workload's bf16 cache quantised once
+    before timing. Bytes: codes (1 per element) + one fp32 scale per (token, kv
+    head) row for K and V, read for the visible keys only."""
+    import torch
+
+    from paged_kv_cache_77_gb300 import api
+
+    wl = synth.WORKLOADS[args.workload]
+    if args.batch:
+        wl = wl.scaled(batch=args.batch)
+    d = synth.draw(wl)
+    v = synth.values(wl, d, dev)
+    pool = api.BlockPool(d.num_blocks, d.pool_order)
+    table_np = pool.build_block_table(d.seq_lens, wl.block_size, wl.window, d.max_blocks_per_seq)
+    slots_np = api.build_slot_mapping(table_np, d.start_pos, d.num_new, wl.block_size)
+    table = torch.from_numpy(table_np).to(dev)
+    slots = torch.from_numpy(slots_np).to(dev)
+    seq_lens = torch.from_numpy(d.seq_lens).to(dev)
+    nb, bs, hkv, dh = v["k_cache"].shape
+    kc = torch.empty((nb, bs, hkv, dh), dtype=torch.uint8, device=dev)
+    vc = torch.empty_like(kc)
+    ks = torch.empty((nb, hkv, bs), dtype=torch.float32, device=dev)
+    vs = torch.empty_like(ks)
+    every = torch.arange(nb * bs, dtype=torch.int32, device=dev)
+    api.kv_cache_write_fp8(kc, vc, ks, vs, v["k_cache"].view(nb * bs, hkv, dh),
+                           v["v_cache"].view(nb * bs, hkv, dh), every)
+    del v["k_cache"], v["v_cache"]
+    torch.cuda.synchronize()
+    out = torch.empty((wl.batch, wl.num_heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(api.decode_workspace_size(wl.batch, wl.num_heads, hkv, dh), dtype=torch.uint8,
+                     device=dev)
+    lens = d.seq_lens.astype(np.int64)
+    vis = np.minimum(lens, wl.window) if wl.window > 0 else lens
+    kv = int(vis.sum()) * hkv * (dh + 4) * 2            # codes + scales, K and V
+    nblk = -(-lens // wl.block_size)
+    live = nblk - (np.maximum(lens - wl.window, 0) // wl.block_size if wl.window > 0 else 0)
+    attn = kv + wl.batch * wl.num_heads * dh * 4 + int(live.sum()) * 4 + wl.batch * 4
+    new_rows = int(d.num_new.sum())
+    write = new_rows * hkv * (dh * 2 + dh + 4) * 2 + new_rows * 4
+    bf16_kv = int(vis.sum()) * hkv * dh * 2 * 2
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        api.kv_cache_write_fp8(kc, vc, ks, vs, v["k_new"], v["v_new"], slots)
+        if ev:
+            ev[0].record(stream)
+        api.paged_attention_decode_fp8(v["q"], kc, vc, ks, vs, table, seq_lens, wl.scale, wl.window,
+                                       out=out, workspace=ws)
+        if ev:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    hbm, _, peak_kind = peaks()
+    achieved = attn / (dec_ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "paged decode over an FP8 E4M3 cache: achieved HBM GB/s", "impl": "ours",
+        "value": (attn + write) / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 cache, f16 tensor-core operands",
+        "data": "synthetic", "seq_steps_per_s": wl.batch / (ms * 1e-3),
+        "config": {"workload": f"{wl.name} (fp8 cache): B={wl.batch} H={wl.num_heads} "
+                               f"H_kv={wl.num_kv_heads} d={wl.head_dim} window={wl.window}",
+                   "kv_bytes": kv, "kv_bytes_if_bf16": bf16_kv,
+                   "decode_us_per_call": dec_ms * 1e3,
+                   "l2": "inputs larger than L2 (%.2f GB of codes and scales)" % (kv / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None, "peak_kind": peak_kind,
+                     "kernel": f"paged_attention_decode_fp8 (attention + merge), {dec_ms * 1e3:.1f} us"},
+        "gpu_launches": 3 * args.steps, "clocks": clocks}), flush=True)
 
 
 def run_mla(args, dev):
@@ -728,6 +821,8 @@ def main():
                     help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-kernel", default="auto", choices=["auto", "cuda_core", "tensor_core"])
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
+                    help="fp8: decode workloads over an E4M3 cache with per-row scales")
     ap.add_argument("--cpu-baseline-child", action="store_true")
     args = ap.parse_args()
     if args.cpu_baseline_child:

@@ -344,6 +344,41 @@ int pkv_mla_paged_decode(void* out, int32_t out_dtype, float* lse, const void* q
                          int32_t rope_dim, int32_t block_size, int64_t num_blocks, float scale,
                          void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
 
+/* FP8 (E4M3) KV cache: write and decode. A quantised cache halves the bytes a decode
+ * step reads. The pages list KV quantisation (skill note 高阶特性: INT8 / W8A8C8;
+ * "KV Cache 笔记": KIVI-style grouped quantisation) and warn that dequantising into
+ * temporary tensors every step eats the saving; here the decode kernel widens the
+ * codes on chip and nothing is materialised.
+ * Format: one fp32 scale per (token, kv head) row of head_dim values,
+ * scale = amax / 448 (IEEE fp32 division), code = E4M3(x / scale) rounded to nearest
+ * even with saturation to +-448 (the "fn" variant: no infinities, S.1111.111 =
+ * NaN); an all-zero row has scale 0 and zero codes. value = code * scale.
+ *   k_cache, v_cache [num_blocks, block_size, H_kv, head_dim] uint8 codes
+ *   k_scale, v_scale [num_blocks, H_kv, block_size] fp32 (a block's scales of one
+ *                    kv head are contiguous)
+ * head_dim must be 128 (PKV_ERR_UNSUPPORTED). */
+
+/* Quantise new rows k, v [num_tokens, H_kv, head_dim] bf16 and write codes and
+ * scales through slot_mapping (negative slot: skipped; slot >= num_blocks *
+ * block_size: skipped and PKV_DEV_BAD_SLOT). Caches 16-byte aligned, scales 4. */
+int pkv_kv_cache_write_fp8(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                           const void* k, const void* v, const int32_t* slot_mapping,
+                           int64_t num_tokens, int64_t num_blocks, int32_t block_size,
+                           int32_t num_kv_heads, int32_t head_dim, int* dev_status, void* stream);
+/* pkv_paged_attention_decode over an FP8 cache: same arguments, result, workspace
+ * (pkv_decode_workspace_size) and error behaviour, plus the two scale arrays
+ * (16-byte aligned). The attention is that of the dequantised cache; q stays bf16.
+ * Rows of positions outside [max(0, len - window), len) are never used, whatever
+ * bytes they hold. Always runs on the tensor cores. */
+int pkv_paged_attention_decode_fp8(void* out, int32_t out_dtype, float* lse, const void* q,
+                                   const void* k_cache, const void* v_cache, const float* k_scale,
+                                   const float* v_scale, const int32_t* block_table,
+                                   int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t B,
+                                   int32_t H, int32_t H_kv, int32_t head_dim, int32_t block_size,
+                                   int64_t num_blocks, float scale, int32_t window,
+                                   void* workspace, size_t workspace_bytes, int* dev_status,
+                                   void* stream);
+
 /* Decode without any caller-provided scratch. The paper has no counterpart for
  * this call; it exists for callers that cannot allocate device memory (a plugin
  * inside a runtime that owns the allocator, a serving loop whose HBM is already

@@ -37,6 +37,11 @@ SIGNATURES = {
     "pkv_manager_cache_blocks": (C.c_int, [vp, i64, vp, i64]),
     "pkv_manager_fork": (i64, [vp, i64, vp, i32, i64, i32, vp, vp, i64, vp]),
     "pkv_copy_blocks": (C.c_int, [vp, i64, i64, vp, vp, i64, vp, vp]),
+    "pkv_kv_cache_write_fp8": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, i32, vp,
+                                         vp]),
+    "pkv_paged_attention_decode_fp8": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32,
+                                                 i32, i32, i32, i32, i64, f32, i32, vp, sz, vp,
+                                                 vp]),
     "pkv_mla_rmsnorm_rope_write": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32,
                                              i32, f32, vp, vp]),
     "pkv_num_skipped_tokens": (i64, [i64, i64]),

@@ -292,6 +292,52 @@ def mla_rmsnorm_rope_write(cache_nope, cache_rope, latent, gamma, cos, sin, slot
         "pkv_mla_rmsnorm_rope_write")
 
 
+def kv_cache_write_fp8(k_cache, v_cache, k_scale, v_scale, k, v, slot_mapping, dev_status=None,
+                       stream=None) -> None:
+    """Quantise new K/V rows to FP8 E4M3 codes + per-row scales and scatter them."""
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        if not (t.is_cuda and t.dtype == torch.uint8 and t.is_contiguous()):
+            raise ValueError(f"{n} must be a contiguous uint8 CUDA tensor")
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+            raise ValueError(f"{n} must be a contiguous fp32 CUDA tensor")
+    _dev_bf16(k, "k")
+    _dev_bf16(v, "v")
+    _dev_i32(slot_mapping, "slot_mapping")
+    nb, bs, hkv, d = k_cache.shape
+    check(load().pkv_kv_cache_write_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                        _ptr(k), _ptr(v), _ptr(slot_mapping), k.shape[0], nb, bs,
+                                        hkv, d, _ptr(dev_status), _stream(stream)),
+          "pkv_kv_cache_write_fp8")
+
+
+def paged_attention_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
+                               scale: float, window: int = 0, out=None, lse=None,
+                               out_dtype=torch.float32, workspace=None, dev_status=None,
+                               stream=None):
+    """Decode attention over an FP8 cache (codes + per-row scales); returns out [B, H, d]."""
+    _dev_bf16(q, "q")
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        if not (t.is_cuda and t.dtype == torch.uint8 and t.is_contiguous()):
+            raise ValueError(f"{n} must be a contiguous uint8 CUDA tensor")
+    _dev_i32(block_table, "block_table")
+    _dev_i32(seq_lens, "seq_lens")
+    B, H, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty((B, H, d), dtype=out_dtype, device=q.device)
+    code = PKV_F32 if out.dtype == torch.float32 else PKV_BF16
+    if workspace is None:
+        workspace = torch.empty(max(decode_workspace_size(B, H, hkv, d), 256), dtype=torch.uint8,
+                                device=q.device)
+    check(load().pkv_paged_attention_decode_fp8(
+        _ptr(out), code, _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, H, hkv, d, bs, nb,
+        scale, window, _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream)),
+        "pkv_paged_attention_decode_fp8")
+    return out
+
+
 def set_decode_kernel(kernel: int) -> None:
     """Select the decode kernel process-wide (KERNEL_AUTO / _CUDA_CORE / _TENSOR_CORE)."""
     check(load().pkv_set_decode_kernel(kernel), "pkv_set_decode_kernel")

@@ -115,41 +115,50 @@ size_t pkv_decode_workspace_size(int32_t B, int32_t H, int32_t H_kv, int32_t hea
   return decode_workspace_bytes(B, H, H_kv, head_dim, current_num_sms());
 }
 
-int pkv_paged_attention_decode(void* out, int32_t out_dtype, float* lse, const void* q,
-                               const void* k_cache, const void* v_cache,
-                               const int32_t* block_table, int32_t max_blocks_per_seq,
-                               const int32_t* seq_lens, int32_t B, int32_t H, int32_t H_kv,
-                               int32_t head_dim, int32_t block_size, int64_t num_blocks,
-                               float scale, int32_t window, void* workspace,
-                               size_t workspace_bytes, int* dev_status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Validation and argument set-up shared by the decode entry points. `what` names
+// the caller in error messages; *empty is set when B == 0 (nothing to launch).
+int decode_setup(pkv::DecodeArgs& a, bool* empty, const char* what, void* out, int32_t out_dtype,
+                 float* lse, const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                 int32_t B, int32_t H, int32_t H_kv, int32_t head_dim, int32_t block_size,
+                 int64_t num_blocks, float scale, int32_t window, void* workspace,
+                 size_t workspace_bytes, int* dev_status) {
+  using namespace pkv;
+  *empty = false;
   PKV_REQUIRE(B >= 0 && H > 0 && H_kv > 0 && max_blocks_per_seq > 0 && num_blocks > 0,
-              PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode: bad sizes");
-  PKV_REQUIRE(H % H_kv == 0, PKV_ERR_INVALID_ARG,
-              "pkv_paged_attention_decode: H (%d) not a multiple of H_kv (%d)", H, H_kv);
+              PKV_ERR_INVALID_ARG, "%s: bad sizes", what);
+  PKV_REQUIRE(H % H_kv == 0, PKV_ERR_INVALID_ARG, "%s: H (%d) not a multiple of H_kv (%d)", what,
+              H, H_kv);
   const int n_rep = H / H_kv;
   PKV_REQUIRE(head_dim == 128 && block_size == 128, PKV_ERR_UNSUPPORTED,
-              "pkv_paged_attention_decode: only head_dim 128 and block_size 128 are implemented");
+              "%s: only head_dim 128 and block_size 128 are implemented", what);
   PKV_REQUIRE(n_rep == 1 || n_rep == 2 || n_rep == 4 || n_rep == 8 || n_rep == 16,
-              PKV_ERR_UNSUPPORTED, "pkv_paged_attention_decode: H / H_kv = %d unsupported", n_rep);
+              PKV_ERR_UNSUPPORTED, "%s: H / H_kv = %d unsupported", what, n_rep);
   PKV_REQUIRE(out_dtype == PKV_BF16 || out_dtype == PKV_F32, PKV_ERR_INVALID_ARG,
-              "pkv_paged_attention_decode: bad out_dtype");
+              "%s: bad out_dtype", what);
   PKV_REQUIRE(std::isfinite(scale) && scale > 0.f, PKV_ERR_INVALID_ARG,
-              "pkv_paged_attention_decode: scale must be a positive finite number");
-  PKV_REQUIRE(window >= 0, PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode: negative window");
+              "%s: scale must be a positive finite number", what);
+  PKV_REQUIRE(window >= 0, PKV_ERR_INVALID_ARG, "%s: negative window", what);
   PKV_REQUIRE(num_blocks * block_size <= INT32_MAX, PKV_ERR_UNSUPPORTED,
-              "pkv_paged_attention_decode: num_blocks * block_size must fit in int32");
-  if (B == 0) return PKV_OK;
+              "%s: num_blocks * block_size must fit in int32", what);
+  if (B == 0) {
+    *empty = true;
+    return PKV_OK;
+  }
   PKV_REQUIRE(out && q && k_cache && v_cache && block_table && seq_lens, PKV_ERR_INVALID_ARG,
-              "pkv_paged_attention_decode: null pointer");
+              "%s: null pointer", what);
   PKV_REQUIRE(aligned16(out) && aligned16(q) && aligned16(k_cache) && aligned16(v_cache),
-              PKV_ERR_INVALID_ARG, "pkv_paged_attention_decode: pointers must be 16-byte aligned");
+              PKV_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", what);
   const int G = current_num_sms();
-  PKV_REQUIRE(G > 0, PKV_ERR_LAUNCH, "pkv_paged_attention_decode: no CUDA device");
+  PKV_REQUIRE(G > 0, PKV_ERR_LAUNCH, "%s: no CUDA device", what);
   const size_t need = decode_workspace_bytes(B, H, H_kv, head_dim, G);
   PKV_REQUIRE(workspace && workspace_bytes >= need && (((uintptr_t)workspace) & 255) == 0,
-              PKV_ERR_WORKSPACE, "pkv_paged_attention_decode: workspace needs %zu bytes, 256-aligned",
-              need);
-  DecodeArgs a{};
+              PKV_ERR_WORKSPACE, "%s: workspace needs %zu bytes, 256-aligned", what, need);
+  a = DecodeArgs{};
   a.q = (const uint16_t*)q;
   a.k_cache = (const uint8_t*)k_cache;
   a.v_cache = (const uint8_t*)v_cache;
@@ -169,14 +178,81 @@ int pkv_paged_attention_decode(void* out, int32_t out_dtype, float* lse, const v
   a.num_ctas = G;
   a.scale_log2 = scale * 1.4426950408889634f;
   decode_workspace_carve(a, workspace);
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_paged_attention_decode(void* out, int32_t out_dtype, float* lse, const void* q,
+                               const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, int32_t max_blocks_per_seq,
+                               const int32_t* seq_lens, int32_t B, int32_t H, int32_t H_kv,
+                               int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                               float scale, int32_t window, void* workspace,
+                               size_t workspace_bytes, int* dev_status, void* stream) {
+  DecodeArgs a;
+  bool empty;
+  const int rc0 = decode_setup(a, &empty, "pkv_paged_attention_decode", out, out_dtype, lse, q,
+                               k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, B, H,
+                               H_kv, head_dim, block_size, num_blocks, scale, window, workspace,
+                               workspace_bytes, dev_status);
+  if (rc0 != PKV_OK || empty) return rc0;
   clear_error();
   cudaStream_t s = (cudaStream_t)stream;
   const bool tensor_cores = g_decode_kernel == PKV_KERNEL_TENSOR_CORE ||
-                            (g_decode_kernel == PKV_KERNEL_AUTO && n_rep >= 4);
+                            (g_decode_kernel == PKV_KERNEL_AUTO && a.n_rep >= 4);
   int rc = launch_status(tensor_cores ? launch_decode_tc(a, s) : launch_decode_simt(a, s),
                          "pkv_paged_attention_decode (attention)");
   if (rc != PKV_OK) return rc;
   return launch_status(launch_decode_merge(a, s), "pkv_paged_attention_decode (merge)");
+}
+
+int pkv_kv_cache_write_fp8(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                           const void* k, const void* v, const int32_t* slot_mapping,
+                           int64_t num_tokens, int64_t num_blocks, int32_t block_size,
+                           int32_t num_kv_heads, int32_t head_dim, int* dev_status, void* stream) {
+  PKV_REQUIRE(num_tokens >= 0 && num_blocks > 0 && block_size > 0 && num_kv_heads > 0,
+              PKV_ERR_INVALID_ARG, "pkv_kv_cache_write_fp8: bad sizes");
+  PKV_REQUIRE(head_dim == 128, PKV_ERR_UNSUPPORTED,
+              "pkv_kv_cache_write_fp8: only head_dim 128 is implemented");
+  PKV_REQUIRE(k_cache && v_cache && k_scale && v_scale && (num_tokens == 0 || (k && v && slot_mapping)),
+              PKV_ERR_INVALID_ARG, "pkv_kv_cache_write_fp8: null pointer");
+  PKV_REQUIRE(aligned16(k_cache) && aligned16(v_cache) && aligned16(k) && aligned16(v) &&
+                  (((uintptr_t)k_scale) & 3) == 0 && (((uintptr_t)v_scale) & 3) == 0,
+              PKV_ERR_INVALID_ARG, "pkv_kv_cache_write_fp8: misaligned pointer");
+  clear_error();
+  return launch_status(launch_kv_write_fp8(k_cache, v_cache, k_scale, v_scale, k, v, slot_mapping,
+                                           num_tokens, num_blocks, block_size, num_kv_heads,
+                                           dev_status, (cudaStream_t)stream, current_num_sms()),
+                       "pkv_kv_cache_write_fp8");
+}
+
+int pkv_paged_attention_decode_fp8(void* out, int32_t out_dtype, float* lse, const void* q,
+                                   const void* k_cache, const void* v_cache, const float* k_scale,
+                                   const float* v_scale, const int32_t* block_table,
+                                   int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t B,
+                                   int32_t H, int32_t H_kv, int32_t head_dim, int32_t block_size,
+                                   int64_t num_blocks, float scale, int32_t window,
+                                   void* workspace, size_t workspace_bytes, int* dev_status,
+                                   void* stream) {
+  DecodeArgs a;
+  bool empty;
+  const int rc0 = decode_setup(a, &empty, "pkv_paged_attention_decode_fp8", out, out_dtype, lse, q,
+                               k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, B, H,
+                               H_kv, head_dim, block_size, num_blocks, scale, window, workspace,
+                               workspace_bytes, dev_status);
+  if (rc0 != PKV_OK || empty) return rc0;
+  PKV_REQUIRE(k_scale && v_scale && aligned16(k_scale) && aligned16(v_scale), PKV_ERR_INVALID_ARG,
+              "pkv_paged_attention_decode_fp8: scale arrays must be set and 16-byte aligned");
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  clear_error();
+  cudaStream_t s = (cudaStream_t)stream;
+  int rc = launch_status(launch_decode_fp8(a, s), "pkv_paged_attention_decode_fp8 (attention)");
+  if (rc != PKV_OK) return rc;
+  return launch_status(launch_decode_merge(a, s), "pkv_paged_attention_decode_fp8 (merge)");
 }
 
 size_t pkv_prefill_workspace_size(void) { return prefill_workspace_bytes(current_num_sms()); }

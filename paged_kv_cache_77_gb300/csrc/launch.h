@@ -10,6 +10,10 @@ cudaError_t launch_kv_write(void* k_cache, void* v_cache, const void* k, const v
                             const int32_t* slots, int64_t num_tokens, int64_t num_slots,
                             int64_t row_k_bytes, int64_t row_v_bytes, int* dev_status,
                             cudaStream_t stream, int num_sms);
+cudaError_t launch_kv_write_fp8(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                                const void* k, const void* v, const int32_t* slots,
+                                int64_t num_tokens, int64_t num_blocks, int block_size, int hkv,
+                                int* dev_status, cudaStream_t stream, int num_sms);
 cudaError_t launch_copy_blocks(void* cache, int64_t num_blocks, int64_t block_bytes,
                                const int32_t* src, const int32_t* dst, int64_t n, int* dev_status,
                                cudaStream_t stream, int num_sms);
@@ -36,6 +40,8 @@ struct DecodeArgs {
   int B, H, Hkv, n_rep, max_blocks, window, out_f32;
   int num_ctas;               // G: CTAs of the attention kernel (one per SM)
   float scale_log2;           // scale * log2(e)
+  const float* k_scale;       // FP8 cache only: [nb, Hkv, bs] per-row scales
+  const float* v_scale;
 };
 
 size_t decode_workspace_bytes(int B, int H, int Hkv, int D, int G);
@@ -46,6 +52,9 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream);
 // tcgen05 split-KV decode for head groups (n_rep 1..16), same partials as above.
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream);
+// tcgen05 split-KV decode over an FP8 (E4M3) cache with per-row scales; same
+// partials and merge as above.
+cudaError_t launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream);
 
 // Absorbed MLA decode (tcgen05) plus its merge. Workspace: mla_workspace_bytes.
 size_t mla_workspace_bytes(int B, int g_half);
