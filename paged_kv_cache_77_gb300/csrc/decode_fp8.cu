@@ -22,17 +22,18 @@
 //
 // Work split and merge: the balanced (b, kv head, block) tile list and partial
 // pieces of the bf16 kernels (device_common.cuh), one persistent CTA per SM.
-// Warp roles (448 threads):
+// Warp roles (576 threads):
 //   warp 0       TMA: Q (bf16) per piece; per tile the K and V code tiles
 //                (box {128 bytes, 1 head, 128 tokens}, 128-byte swizzle) and the
 //                two 512-byte scale rows (bulk copy), 4-deep ring;
 //   warp 1       MMA issuer (S^T of tile j+1 before O^T of tile j; two commits
 //                and three waits per tile);
-//   warps 2-5    softmax: converts Q at each piece start, then per tile thread =
-//                token lane of S^T / d lane of O^T as in the bf16 kernel;
-//   warps 6-9    K converters: thread = token row; 128 codes -> 64 f16 pairs ->
+//   warps 2-9    softmax, two groups of four warps: group g owns half of the heads
+//                of every token row (thread = token lane of S^T / d lane of O^T);
+//                both groups convert Q at each piece start;
+//   warps 10-13  K converters: thread = token row; 128 codes -> 64 f16 pairs ->
 //                tcgen05.st into the K' ring in tensor memory;
-//   warps 10-13  V converters: thread = token row; codes -> f16 rows of V' in the
+//   warps 14-17  V converters: thread = token row; codes -> f16 rows of V' in the
 //                128-byte-swizzled layout the MMA reads, zero for invalid rows.
 // All waits are bounded (tc_ptx.cuh); a timeout sets PKV_DEV_TIMEOUT.
 //
@@ -66,7 +67,8 @@ constexpr int NSTG = PKV_F8_NSTG;      // code / scale staging ring
 // on, so the MMA thread commits only SFULL and OFULL per tile.
 constexpr int NKOP = 2;
 constexpr int NVOP = 2;
-constexpr int NTHREADS = 448;
+constexpr int NTHREADS = 576;
+constexpr int NSOFT = 256;             // softmax threads: two warps per TMEM lane quarter
 constexpr int CTILE = BS * D;          // 16 KB of codes: [128 tokens x 128 bytes], swizzled
 constexpr int HALF = 16384;            // f16 [128 rows x 64], one d half, swizzled
 constexpr int VOPB = 2 * HALF;         // one V' tile
@@ -185,7 +187,7 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       mbar_init(bar(B_VSTF + i), 1);
       mbar_init(bar(B_VSTE + i), 128);
       mbar_init(bar(B_SCF + i), 1);
-      mbar_init(bar(B_SCE + i), 128);
+      mbar_init(bar(B_SCE + i), NSOFT);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_KOPF + i), 128);
@@ -193,11 +195,11 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_QSTF + i), 1);
-      mbar_init(bar(B_QSTE + i), 128);
-      mbar_init(bar(B_QOPF + i), 128);
+      mbar_init(bar(B_QSTE + i), NSOFT);
+      mbar_init(bar(B_QOPF + i), NSOFT);
       mbar_init(bar(B_QOPE + i), 1);
       mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_PFULL + i), 128);
+      mbar_init(bar(B_PFULL + i), NSOFT);
       mbar_init(bar(B_OFULL + i), 1);
     }
     *abort_flag = 0;
@@ -319,7 +321,7 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       if (!issue_o(j)) { ok = false; break; }
     }
     if (!ok) fail();
-  } else if (ntiles > 0 && warp >= 6 && warp < 10) {
+  } else if (ntiles > 0 && warp >= 10 && warp < 14) {
     // ------------------------------------------------------------ K converters
     // Thread = token row r: 128 codes -> 64 f16 pairs in columns k_col(kb)..+63 of
     // TMEM lane r (the A operand of the score product). Warp-uniform decisions only:
@@ -355,7 +357,7 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(B_KOPF + kb));
     }
-  } else if (ntiles > 0 && warp >= 10) {
+  } else if (ntiles > 0 && warp >= 14) {
     // ------------------------------------------------------------ V converters
     // Thread = token row r: codes -> f16 row r of V' (two 64-wide swizzled halves);
     // rows of positions the softmax masks are written as zeros.
@@ -363,14 +365,15 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
     const int r = quarter * 32 + lane;
     TileCursor c;
     cursor_seek(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap, t0, t1);
+    int blk_next = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.jlo + c.j);
     for (int j = 0; j < ntiles; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      const int blk = blk_next;
       const int st = j % NSTG, vb = j % NVOP;
       bool ok = mbar_wait(bar(B_VSTF + st), (j / NSTG) & 1);
       ok = ok && (j < 2 || mbar_wait(bar(B_OFULL + vb), ((j >> 1) & 1) ^ 1));  // O(j-2) done
       tc_fence_after();
       if (!__all_sync(0xffffffffu, ok)) { fail(); break; }
-      const int blk = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.jlo + c.j);
       const int lo = (a.window > 0 && c.len > a.window) ? c.len - a.window : 0;
       const int pos = (c.jlo + c.j) * BS + r;
       const bool valid = blk >= 0 && (int64_t)blk < a.num_blocks && pos < c.len && pos >= lo;
@@ -392,66 +395,69 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       fence_proxy_async_smem();
       mbar_arrive(bar(B_VOPF + vb));
       cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
+      if (j + 1 < ntiles) blk_next = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.jlo + c.j);
     }
   } else if (ntiles > 0 && warp >= 2) {
     // ------------------------------------------------------------ softmax / epilogue
+    constexpr int HG = NREP > 1 ? NREP / 2 : 1;   // heads per group
     const int quarter = warp & 3;                 // TMEM lane quarter this warp may access
+    const int grp = (warp - 2) >> 2;              // head group
+    const int h0 = grp * HG;                      // first head of the group
+    const bool has_heads = h0 < NREP;             // false only for group 1 when NREP == 1
     const int r = quarter * 32 + lane;            // token row of S^T, d row of O^T
+    const int ts = grp * 128 + r;                 // thread index among the 256
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int sw = warp - 2;                      // slot in the reduction arrays
     float* red = reinterpret_cast<float*>(base + OFF_RED);
     float* fred = reinterpret_cast<float*>(base + OFF_FRED);
     float* lred = reinterpret_cast<float*>(base + OFF_LRED);
     float* qm = reinterpret_cast<float*>(base + OFF_QM);
     TileCursor c;
     cursor_seek(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap, t0, t1);
-    float m_run[NREP], l_part[NREP], o_reg[NREP], alpha_prev[NREP], qmul[NREP];
+    float m_run[HG], l_part[HG], o_reg[HG], alpha_prev[HG], qmul[HG];
     float f_prev = 1.f;
     int pb = 0, pg = 0, piece = -1;
     int64_t p_first = t0, p_segbase = 0;
     bool p_whole = false, aborted = false;
 
-    // Q' of a new piece: row h = r / 8 (thread: 16 of its 128 values) is scaled by
-    // 2^e_h with the row max near 2^14, widened exactly to f16 and written in the
+    // Q' of a new piece: thread ts converts 8 values of row h = ts / 16; the row is
+    // scaled by 2^e_h with its max near 2^14, widened exactly to f16 and written in the
     // layout the score product reads; 2^-e_h goes to qm[h].
     auto convert_q = [&]() -> bool {
       const int qb = piece & 1;
       bool ok = mbar_wait(bar(B_QSTF + qb), (piece >> 1) & 1);
       ok = mbar_wait(bar(B_QOPE + qb), ((piece >> 1) & 1) ^ 1) && ok;
-      const int h = r >> 3, cq = r & 7, kc = 2 * (cq & 3);
-      const uint8_t* src = base + OFF_QST + qb * QBUF + (cq >> 2) * (QBUF / 2);
-      uint8_t* dst = base + OFF_QOP + qb * QBUF + (cq >> 2) * (QBUF / 2);
+      const int h = ts >> 4, c16 = ts & 15, kc = c16 & 7;
+      const uint8_t* src = base + OFF_QST + qb * QBUF + (c16 >> 3) * (QBUF / 2);
+      uint8_t* dst = base + OFF_QOP + qb * QBUF + (c16 >> 3) * (QBUF / 2);
       const uint4 x0 = *reinterpret_cast<const uint4*>(src + sw_chunk(h, kc));
-      const uint4 x1 = *reinterpret_cast<const uint4*>(src + sw_chunk(h, kc + 1));
       mbar_arrive(bar(B_QSTE + qb));
-      const uint32_t u[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const uint32_t u[4] = {x0.x, x0.y, x0.z, x0.w};
       float amax = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 4; ++i)
         amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(u[i] << 16)),
                                  fabsf(__uint_as_float(u[i] & 0xffff0000u))));
 #pragma unroll
-      for (int o = 4; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      for (int o = 8; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       int e = 0;
       if (amax > 0.f) {
         const int ex = (int)((__float_as_uint(amax) >> 23) & 0xff) - 127;  // floor(log2 amax)
         e = min(127, max(-126, 14 - ex));
       }
       const float mul = __uint_as_float((uint32_t)(127 + e) << 23);
-      uint32_t y[8];
+      uint32_t y[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 4; ++i) {
         const __half2 hv = __floats2half2_rn(__uint_as_float(u[i] << 16) * mul,
                                              __uint_as_float(u[i] & 0xffff0000u) * mul);
         y[i] = *reinterpret_cast<const uint32_t*>(&hv);
       }
       *reinterpret_cast<uint4*>(dst + sw_chunk(h, kc)) = make_uint4(y[0], y[1], y[2], y[3]);
-      *reinterpret_cast<uint4*>(dst + sw_chunk(h, kc + 1)) = make_uint4(y[4], y[5], y[6], y[7]);
-      if (cq == 0) qm[h] = __uint_as_float((uint32_t)(127 - e) << 23);
+      if (c16 == 0) qm[h] = __uint_as_float((uint32_t)(127 - e) << 23);
       fence_proxy_async_smem();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, NSOFT);
 #pragma unroll
-      for (int hh = 0; hh < NREP; ++hh) qmul[hh] = qm[hh];
+      for (int hh = 0; hh < HG; ++hh) qmul[hh] = has_heads ? qm[h0 + hh] : 0.f;
       mbar_arrive(bar(B_QOPF + qb));
       return ok;
     };
@@ -465,24 +471,27 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       tmem_wait_ld();
       tc_fence_before();  // ordered before the next PFULL arrive, which frees O^T(jj)
 #pragma unroll
-      for (int h = 0; h < NREP; ++h) o_reg[h] = o_reg[h] * alpha_prev[h] + f_prev * __uint_as_float(v[h]);
+      for (int h = 0; h < HG; ++h)
+        o_reg[h] = o_reg[h] * alpha_prev[h] + f_prev * __uint_as_float(grp ? v[(HG + h) & 15] : v[h]);
     };
     auto finalize = [&]() {
 #pragma unroll
-      for (int h = 0; h < NREP; ++h) {
+      for (int h = 0; h < HG; ++h) {
         float l = l_part[h];
 #pragma unroll
         for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) lred[sw * 16 + h] = l;
+        if (lane == 0 && has_heads) lred[quarter * 16 + h0 + h] = l;
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, NSOFT);
       const int64_t slot = (p_first == p_segbase) ? (int64_t)pb * a.Hkv + pg
                                                   : (int64_t)a.B * a.Hkv + blockIdx.x;
 #pragma unroll
-      for (int h = 0; h < NREP; ++h) {
+      for (int hh = 0; hh < HG; ++hh) {
+        const int h = h0 + hh;
+        if (!has_heads || h >= NREP) continue;
         const float l = lred[h] + lred[16 + h] + lred[32 + h] + lred[48 + h];
-        const float ov = l > 0.f ? o_reg[h] / l : 0.f;
-        const float lse2 = l > 0.f ? m_run[h] + log2f(l) : -INFINITY;
+        const float ov = l > 0.f ? o_reg[hh] / l : 0.f;
+        const float lse2 = l > 0.f ? m_run[hh] + log2f(l) : -INFINITY;
         if (p_whole) {
           const int64_t row = (int64_t)pb * a.H + (int64_t)pg * NREP + h;
           if (a.out_f32)
@@ -495,11 +504,15 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
           if (r == 0) a.ws_lse[slot * NREP + h] = lse2;
         }
       }
-      named_bar_sync(1, 128);  // lred reused by the next piece
+      named_bar_sync(1, NSOFT);  // lred reused by the next piece
     };
 
+    // The tile's block id is loaded one tile ahead, so that its latency is not on
+    // the path from S^T to P'.
+    int blk_next = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.jlo + c.j);
     for (int j = 0; j < ntiles; ++j) {
       const bool first = (j == 0) || (c.j == 0);
+      const int blk = blk_next;
       if (first) {
         ++piece;
         if (!convert_q()) fail();
@@ -508,7 +521,7 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
           finalize();
         }
 #pragma unroll
-        for (int h = 0; h < NREP; ++h) {
+        for (int h = 0; h < HG; ++h) {
           m_run[h] = -INFINITY;
           l_part[h] = 0.f;
           o_reg[h] = 0.f;
@@ -535,26 +548,30 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       tmem_wait_ld();
       tc_fence_before();  // ordered before PFULL(j), which frees S^T(j)
 
-      const int blk = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.jlo + c.j);
       const bool blk_ok = blk >= 0 && (int64_t)blk < a.num_blocks;
       const int lo = (a.window > 0 && c.len > a.window) ? c.len - a.window : 0;
       const int pos = (c.jlo + c.j) * BS + r;
       const bool valid = blk_ok && pos < c.len && pos >= lo;
-      float x[NREP];
+      const float smul = sk * kWidenScale * a.scale_log2;
+      float x[HG];
 #pragma unroll
-      for (int h = 0; h < NREP; ++h) {
-        x[h] = valid ? __uint_as_float(svr[h]) * (sk * kWidenScale * qmul[h] * a.scale_log2) : -INFINITY;
+      for (int h = 0; h < HG; ++h) {
+        // Column h0 + h, chosen between two compile-time indices (no local memory).
+        const uint32_t sx = grp ? svr[(HG + h) & 15] : svr[h];
+        x[h] = (valid && has_heads) ? __uint_as_float(sx) * (smul * qmul[h]) : -INFINITY;
         float m = x[h];
 #pragma unroll
         for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) red[(sb * 4 + sw) * 16 + h] = m;
+        if (lane == 0 && has_heads) red[(sb * 4 + quarter) * 16 + h0 + h] = m;
       }
-      float fv = valid ? sv : 0.f;
+      if (grp == 0) {
+        float fv = valid ? sv : 0.f;
 #pragma unroll
-      for (int o = 16; o; o >>= 1) fv = fmaxf(fv, __shfl_xor_sync(0xffffffffu, fv, o));
-      if (lane == 0) fred[sb * 4 + sw] = fv;
-      if (r == 0) abort_snap[sb] = *abort_flag;
-      named_bar_sync(1, 128);
+        for (int o = 16; o; o >>= 1) fv = fmaxf(fv, __shfl_xor_sync(0xffffffffu, fv, o));
+        if (lane == 0) fred[sb * 4 + quarter] = fv;
+      }
+      if (ts == 0) abort_snap[sb] = *abort_flag;
+      named_bar_sync(1, NSOFT);
       if (abort_snap[sb]) {
         aborted = true;
         break;
@@ -562,11 +579,11 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       float f = fmaxf(fmaxf(fred[sb * 4], fred[sb * 4 + 1]), fmaxf(fred[sb * 4 + 2], fred[sb * 4 + 3]));
       f = f > 0.f ? f : 1.f;
       const float vmul = valid ? __fdividef(sv, f) : 0.f;
-      float alpha[NREP];
+      float alpha[HG];
 #pragma unroll
-      for (int h = 0; h < NREP; ++h) {
-        const float* rr = red + sb * 64 + h;
-        const float mb = fmaxf(fmaxf(rr[0], rr[16]), fmaxf(rr[32], rr[48]));
+      for (int h = 0; h < HG; ++h) {
+        const float* rr = red + sb * 64 + h0 + h;
+        const float mb = has_heads ? fmaxf(fmaxf(rr[0], rr[16]), fmaxf(rr[32], rr[48])) : -INFINITY;
         const float mn = fmaxf(m_run[h], mb);
         alpha[h] = (mn == -INFINITY) ? 1.f : exp2f(m_run[h] - mn);
         const float p = (x[h] == -INFINITY) ? 0.f : exp2f(x[h] - mn);
@@ -574,23 +591,26 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
         m_run[h] = mn;
         x[h] = p * vmul;  // P' = p * v_scale / f
       }
-      // ---- P'^T (f16) into the B operand of the value product (O(j-2), its last
-      // reader, is complete: acc_o(j-2) waited for it)
+      // ---- P'^T (f16) of the group's heads into the B operand of the value product
+      // (O(j-2), its last reader, is complete: acc_o(j-2) waited for it). Columns of
+      // heads >= NREP only feed O^T columns that are never read.
       uint8_t* ps = base + OFF_P + sb * PBUF + (r >> 6) * (PBUF / 2);
       const int k = r & 63;
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
-        const float p = h < NREP ? x[h < NREP ? h : 0] : 0.f;
-        *reinterpret_cast<__half*>(ps + (h >> 3) * 1024 + sw128(h & 7, k)) = __float2half_rn(p);
+      for (int hh = 0; hh < HG; ++hh) {
+        const int h = h0 + hh;
+        if (h < NREP) *reinterpret_cast<__half*>(ps + (h >> 3) * 1024 + sw128(h & 7, k)) = __float2half_rn(x[hh]);
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(B_PFULL + sb));
+      // Tile j's values are all computed; advance and start the next block-id load.
+      cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
+      if (j + 1 < ntiles) blk_next = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.jlo + c.j);
       // ---- fold the previous tile's O^T into the registers
       if (!first) acc_o(j - 1);
 #pragma unroll
-      for (int h = 0; h < NREP; ++h) alpha_prev[h] = alpha[h];
+      for (int h = 0; h < HG; ++h) alpha_prev[h] = alpha[h];
       f_prev = f * kWidenScale;  // O^T of this tile carries V' = value * code factor / f
-      cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
     }
     if (!aborted) {
       acc_o(ntiles - 1);
