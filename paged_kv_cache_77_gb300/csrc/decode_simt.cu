@@ -145,6 +145,13 @@ __global__ void __launch_bounds__(simt::THREADS, 1) decode_simt_kernel(DecodeArg
                 qb.y * kf[5] + qb.z * kf[6] + qb.w * kf[7];
       }
     }
+    // A masked position's V row may hold any bytes (an unwritten tail slot): zero it,
+    // so that its weight 0 cannot meet a NaN in the value loop below.
+    if (!valid) {
+      uint8_t* vrow = const_cast<uint8_t*>(vt);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) *reinterpret_cast<uint4*>(vrow + swz(tid, c)) = make_uint4(0, 0, 0, 0);
+    }
     float mx[NREP];
 #pragma unroll
     for (int h = 0; h < NREP; ++h) {

@@ -363,6 +363,19 @@ __global__ void __launch_bounds__(tcd::NTHREADS, 1)
         m_run[h] = mn;
         x[h] = p;
       }
+      // A masked position's V row may hold any bytes (an unwritten tail slot): once the
+      // tile has landed, zero it so that its weight 0 cannot meet a NaN in the value
+      // product (made visible to the MMA by the proxy fence before PFULL).
+      if (!valid) {
+        const int st = j % NST;
+        if (!mbar_wait(bar(B_VFULL + st), (j / NST) & 1)) { bad = true; fail(); }
+        uint8_t* vrow = base + OFF_V + st * TILE + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vrow + HALF + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
       // ---- P^T (bf16) into the B operand of the value product
       if (!mbar_wait(bar(B_PEMPTY + sb), ((j >> 1) & 1) ^ 1)) { bad = true; fail(); }
       uint8_t* ps = base + OFF_P + sb * PBUF + (r >> 6) * (PBUF / 2);

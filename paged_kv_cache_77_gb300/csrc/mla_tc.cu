@@ -452,6 +452,20 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
         pk[i / 2] = *reinterpret_cast<uint32_t*>(&h2);
       }
       l += psum;
+      // Tokens past the sequence's end (the tile's tail) hold any bytes: the score
+      // product is done with this tile (SFULL), so zero those rows of the nope chunks
+      // this CTA's value product reads, so that a weight 0 cannot meet a NaN there.
+      if (nvalid < TT) {
+        uint8_t* kt = base + OFF_K + (j % NST) * NCH * KCH + (4 * half) * KCH;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int pidx = r + 128 * k;           // 32 rows x 4 chunks x 8 pieces of 16 B
+          const int row = pidx >> 5, ch = (pidx >> 3) & 3, q = pidx & 7;
+          if (row >= nvalid)
+            *reinterpret_cast<uint4*>(kt + ch * KCH + row * 128 + q * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
       if (!mbar_wait(bar(B_PEMPTY + sb), ((j >> 1) & 1) ^ 1)) fail();
       __syncwarp();
       tc_fence_after();

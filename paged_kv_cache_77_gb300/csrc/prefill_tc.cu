@@ -616,6 +616,17 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
           m_ref = m_new;
         }
       }
+      // Keys past the sequence's end in this block hold any bytes (unwritten tail
+      // slots): zero their V rows (this thread: row r, d half `half`) once the tile
+      // has landed, so that a weight 0 cannot meet a NaN in the value product.
+      if (c.j * BS + r >= c.s.kvlen) {
+        const int vst = j % NV;
+        if (!mbar_wait(bar(B_VFULL + vst), (j / NV) & 1)) fail();
+        uint8_t* vrow = base + OFF_V + vst * TILE + half * HALF + r * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(vrow + q * 16) = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+      }
       if (!mbar_wait(bar(B_PEMPTY + sb), ((j >> 1) & 1) ^ 1)) fail();
       __syncwarp();
       tc_fence_after();

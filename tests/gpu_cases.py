@@ -64,6 +64,21 @@ class DecodeCase:
         self.post = {c: ref.cache_write(self.pre[c], synth.bf16_bits(self.v[r]), self.slots_np)
                      for c, r in pairs}
 
+    def poison_tails(self):
+        """NaN in every cache row past a sequence's length inside its last block, on
+        the GPU and in the oracle's copy (which never reads them). Such rows hold
+        whatever the memory held before; attention must not depend on them."""
+        bs = self.wl.block_size
+        names = list(self.post)
+        for b, n in enumerate(self.d.seq_lens):
+            n = int(n)
+            if n == 0 or n % bs == 0:
+                continue
+            blk, off = int(self.table_np[b, n // bs]), n % bs
+            for name in names:
+                self.v[name][blk, off:] = float("nan")
+                self.post[name][blk, off:] = synth.BF16_NAN_BITS
+
     def check_write_bit_exact(self):
         for name, expect in self.post.items():
             got = synth.bf16_bits(self.v[name])

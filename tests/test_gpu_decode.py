@@ -50,6 +50,27 @@ def test_decode_small_edge_cases(H, Hkv, window, kernel):
     assert out[5].abs().max().item() == 0.0 and torch.isinf(lse[5]).all()  # empty sequence
 
 
+def test_decode_ignores_nan_in_unwritten_rows(kernel):
+    # Rows past each sequence's end in its last block are NaN: a masked weight of 0
+    # times NaN must not reach the output.
+    lens = [1, 129, 700, 3000, 255, 4097]
+    wl = BASE.scaled(batch=len(lens), num_heads=32, num_kv_heads=8, window=0, seed=9)
+    case = DecodeCase(wl, synth.draw_explicit(wl, lens))
+    case.gpu_write()
+    case.oracle_write()
+    case.check_write_bit_exact()
+    case.poison_tails()
+    for window in (0, 200):
+        lse = torch.full((wl.batch, wl.num_heads), float("nan"), device="cuda")
+        out = api.paged_attention_decode(case.v["q"], case.v["k_cache"], case.v["v_cache"], case.table,
+                                         case.seq_lens, wl.scale, window, lse=lse)
+        torch.cuda.synchronize()
+        q64 = case.v["q"].double().cpu().numpy()
+        o_ref, lse_ref = ref.paged_decode(q64, case.post["k_cache"], case.post["v_cache"], case.table_np,
+                                          case.d.seq_lens, wl.block_size, wl.scale, window)
+        compare(out, lse, o_ref, lse_ref, list(range(len(lens))), f"{kernel} NaN tails W{window}")
+
+
 def test_decode_bf16_output_and_many_splits(kernel):
     lens = [5000, 3, 4096, 12000]
     wl = BASE.scaled(batch=4, num_heads=64, num_kv_heads=8, seed=8)

@@ -13,10 +13,14 @@ pytestmark = pytest.mark.gpu
 MLA = synth.WORKLOADS["mla"]
 
 
-def _run(case: DecodeCase, rows, out_dtype=torch.float32):
+def _run(case: DecodeCase, rows, out_dtype=torch.float32, poison_tails=False):
     wl = case.wl
     case.gpu_write()
     case.oracle_write()
+    if poison_tails:
+        torch.cuda.synchronize()
+        case.check_write_bit_exact()
+        case.poison_tails()
     lse = torch.full((wl.batch, wl.num_heads), float("nan"), device="cuda")
     out = api.mla_paged_decode(case.v["q_nope"], case.v["q_rope"], case.v["cache_nope"],
                                case.v["cache_rope"], case.table, case.seq_lens, wl.scale, lse=lse,
@@ -38,6 +42,14 @@ def test_mla_small_edge_cases(H):
     out, lse, o_ref, lse_ref = _run(case, list(range(len(lens))))
     compare(out, lse, o_ref, lse_ref, list(range(len(lens))), f"mla H{H}")
     assert out[7].abs().max().item() == 0.0 and torch.isinf(lse[7]).all()
+
+
+def test_mla_ignores_nan_in_unwritten_rows():
+    lens = [1, 31, 33, 129, 1000, 4095]
+    wl = MLA.scaled(batch=len(lens), num_heads=128, seed=33)
+    case = DecodeCase(wl, synth.draw_explicit(wl, lens))
+    out, lse, o_ref, lse_ref = _run(case, list(range(len(lens))), poison_tails=True)
+    compare(out, lse, o_ref, lse_ref, list(range(len(lens))), "mla NaN tails")
 
 
 def test_mla_bf16_output_long_sequences():

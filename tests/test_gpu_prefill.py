@@ -19,10 +19,14 @@ def _case(wl, prior, qlen, poison=True):
     return DecodeCase(wl, d, poison=poison)
 
 
-def _run(case: DecodeCase, rows, causal=True, out_dtype=torch.float32):
+def _run(case: DecodeCase, rows, causal=True, out_dtype=torch.float32, poison_tails=False):
     wl = case.wl
     case.gpu_write()
     case.oracle_write()
+    if poison_tails:
+        torch.cuda.synchronize()
+        case.check_write_bit_exact()
+        case.poison_tails()
     cu = torch.from_numpy(np.cumsum(case.d.num_new).astype(np.int32)).cuda()
     T = int(case.d.num_new.sum())
     lse = torch.full((T, wl.num_heads), float("nan"), device="cuda")
@@ -61,6 +65,16 @@ def test_prefill_non_causal_differs_and_matches_oracle():
                                case.post["k_cache"], case.post["v_cache"], case.table_np,
                                case.d.seq_lens, 128, wl.scale, causal=True, rows=[0])
     assert np.abs(o_c[0] - out[0].cpu().numpy()).max() > 1e-2
+
+
+def test_prefill_ignores_nan_in_unwritten_rows():
+    prior, qlen = [0, 5, 200, 1000, 127], [3, 130, 33, 300, 1]
+    wl = MIX.scaled(batch=len(prior), num_heads=32, num_kv_heads=8, seed=46)
+    T = sum(qlen)
+    for causal in (True, False):
+        case = _case(wl, prior, qlen)
+        out, lse, o_ref, lse_ref = _run(case, None, causal=causal, poison_tails=True)
+        compare(out, lse, o_ref, lse_ref, list(range(T)), f"prefill NaN tails causal={causal}")
 
 
 def test_prefill_bf16_output():
