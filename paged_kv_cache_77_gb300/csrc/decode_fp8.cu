@@ -50,7 +50,8 @@
 namespace pkv {
 
 bool make_tmap_sw128(CUtensorMap* m, CUtensorMapDataType dtype, const void* ptr, int rank,
-                     const uint64_t* dims, const uint64_t* strides, const uint32_t* box);
+                     const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                     CUtensorMapL2promotion promo);
 
 namespace f8d {
 
@@ -638,9 +639,14 @@ static cudaError_t launch_fp8_n(const DecodeArgs& a, cudaStream_t stream) {
   const uint64_t qdims[2] = {D, (uint64_t)a.B * a.H};
   const uint64_t qstr[1] = {D * 2};
   const uint32_t qbox[2] = {64, 16};
-  if (!make_tmap_sw128(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.k_cache, 3, kdims, kstr, kbox) ||
-      !make_tmap_sw128(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.v_cache, 3, kdims, kstr, kbox) ||
-      !make_tmap_sw128(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, 2, qdims, qstr, qbox))
+  // A code row of one kv head is 128 bytes and the next head's row follows it: a
+  // 256-byte L2 promotion would fetch that neighbour, which this CTA does not read.
+  if (!make_tmap_sw128(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.k_cache, 3, kdims, kstr, kbox,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_128B) ||
+      !make_tmap_sw128(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.v_cache, 3, kdims, kstr, kbox,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_128B) ||
+      !make_tmap_sw128(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, 2, qdims, qstr, qbox,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(decode_fp8_kernel<NREP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);

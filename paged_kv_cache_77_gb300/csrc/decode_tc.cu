@@ -431,20 +431,24 @@ EncodeTiledFn encode_tiled_fn() {
 // Tensor map with a 128-byte swizzle. dims/strides innermost first; strides in
 // bytes for dims 1..rank-1.
 bool make_tmap_sw128(CUtensorMap* m, CUtensorMapDataType dtype, const void* ptr, int rank,
-                     const uint64_t* dims, const uint64_t* strides, const uint32_t* box) {
+                     const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                     CUtensorMapL2promotion promo) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = fn(m, dtype, (cuuint32_t)rank, const_cast<void*>(ptr),
                   (const cuuint64_t*)dims, (const cuuint64_t*)strides, (const cuuint32_t*)box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
+// bf16 maps fetch 256 bytes into L2 per request: a 256-byte K/V row of one kv head
+// is read as two 128-byte boxes, and the promotion brings the second in with the first.
 bool make_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
                     const uint64_t* strides, const uint32_t* box) {
-  return make_tmap_sw128(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, rank, dims, strides, box);
+  return make_tmap_sw128(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, rank, dims, strides, box,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 template <int NREP>
