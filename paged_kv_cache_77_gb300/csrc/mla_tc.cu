@@ -6,21 +6,26 @@
 //
 //   s_j = scale * (q_nope . nope_j + q_rope . rope_j),   o = softmax(s) . nope
 //
-// Tiles are 32 tokens of one sequence, streamed by TMA through a 4-deep ring. Per
-// tile, with the 128 query heads on the M = 128 side of the MMA:
+// Tiles are 64 tokens of one sequence, streamed by TMA through a 2-deep ring (72 KB
+// a stage). Per tile, with the 128 query heads on the M = 128 side of the MMA:
 //
-//   S [128 heads x 32] = [Q_nope | Q_rope] [128 x 576] . [nope | rope]_tile^T
-//   O_half [128 x 256] += P [128 x 32] . nope_tile[:, half]      (P read from TMEM)
+//   S [128 heads x 64] = [Q_nope | Q_rope] [128 x 576] . [nope | rope]_tile^T
+//   O_half [128 x 256] += P [128 x 64] . nope_tile[:, half]      (P read from TMEM)
+//
+// 64-token tiles halve the MMA issues per token of 32-token tiles (an N=64 MMA costs
+// about what an N=32 one does) and the handoffs per token; shared memory and tensor
+// memory are then full, so S has a single buffer (the next score product waits only
+// until the softmax has read S into registers).
 //
 // O for all 512 latent columns (128 x 512 fp32) would fill the whole 512-column
 // tensor memory, so the 512 columns are split across two CTAs ("halves"); each CTA
 // computes the full S of its tiles (1.5x the minimum tensor work) and half of O.
 // CTA i and CTA i + G/2 walk the same tile range, so the second read of a tile
 // usually hits L2. To leave shared memory for the ring, the A operand Q is split:
-// columns 0..255 stay in shared memory, columns 256..511 and the rope part are
+// columns 0..319 stay in shared memory, columns 320..511 and the rope part are
 // written by the softmax warps into tensor memory and read from there by the MMA.
 //
-// Softmax: thread = head row of S (all 32 scores of a tile in one thread, no
+// Softmax: thread = head row of S (all 64 scores of a tile in one thread, no
 // shuffles); exp2 in fp32 with the scale folded into log2 units; P rounded to bf16
 // and stored into TMEM as the A operand of the value product; the normaliser sums
 // the rounded weights. The running max is only raised when a tile's max exceeds it
@@ -44,21 +49,22 @@ namespace mla {
 
 constexpr int DC = 512;          // latent (nope) width
 constexpr int DR = 64;           // rope width
-constexpr int TT = 32;           // tokens per tile
+constexpr int TT = 64;           // tokens per tile (MMA N of the score product)
 constexpr int BS = 128;          // block size
 constexpr int M = 128;           // query heads per MMA (rows)
 constexpr int DH = 256;          // latent columns per CTA half
 constexpr int NCH = 9;           // 64-wide chunks of [nope | rope]
-constexpr int QSM = 4;           // Q chunks 0-3 (nope 0..255) live in shared memory,
-                                 // chunks 4-8 (nope 256..511 and rope) in tensor memory
+constexpr int QSM = 5;           // Q chunks 0-4 (nope 0..319) live in shared memory,
+                                 // chunks 5-8 (nope 320..511 and rope) in tensor memory
 constexpr int QCH = M * 128;     // one Q chunk: 128 rows x 128 bytes
-constexpr int KCH = TT * 128;    // one K chunk: 32 rows x 128 bytes
-constexpr int NST = 4;
+constexpr int KCH = TT * 128;    // one K chunk: TT rows x 128 bytes
+constexpr int NST = 2;           // K stages (72 KB each)
+constexpr int NSB = 1;           // S buffers in tensor memory
 constexpr int NTHREADS = 192;
 
 constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + QSM * QCH;           // 65536
-constexpr int OFF_BAR = OFF_K + NST * NCH * KCH;   // 212992
+constexpr int OFF_K = OFF_Q + QSM * QCH;           // 81920
+constexpr int OFF_BAR = OFF_K + NST * NCH * KCH;   // 229376
 enum {
   B_KFULL = 0,
   B_KEMPTY = B_KFULL + NST,
@@ -66,8 +72,8 @@ enum {
   B_QEMPTY = B_QFULL + 1,
   B_QTFULL = B_QEMPTY + 1,
   B_SFULL = B_QTFULL + 1,
-  B_SEMPTY = B_SFULL + 2,
-  B_PFULL = B_SEMPTY + 2,
+  B_SEMPTY = B_SFULL + NSB,
+  B_PFULL = B_SEMPTY + NSB,
   B_PEMPTY = B_PFULL + 2,
   B_ODONE = B_PEMPTY + 2,
   B_OFREE = B_ODONE + 2,
@@ -75,14 +81,16 @@ enum {
 };
 constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 
-// TMEM columns: S 0..63 (two buffers), P 64..95 (two buffers), Q chunks 4-8
-// 96..255 (32 columns each: 64 bf16 packed in pairs), O half 256..511.
+// TMEM columns: S 0..63 (one buffer, TT fp32 columns), P 64..127 (two buffers of TT
+// bf16 packed in pairs), Q chunks 5-8 128..255 (32 columns each), O half 256..511.
 constexpr uint32_t TMEM_COLS = 512;
-__device__ __forceinline__ uint32_t s_col(int b) { return b * 32; }
-__device__ __forceinline__ uint32_t p_col(int b) { return 64 + b * 16; }
-constexpr uint32_t Q_COL = 96;
+__device__ __forceinline__ uint32_t s_col(int b) { return b * TT; }
+__device__ __forceinline__ uint32_t p_col(int b) { return NSB * TT + b * (TT / 2); }
+constexpr uint32_t Q_COL = NSB * TT + TT;
 constexpr uint32_t O_COL = 256;
+static_assert(Q_COL + (NCH - QSM) * 32 <= O_COL, "tensor memory");
 
 }  // namespace mla
 
@@ -130,9 +138,11 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QEMPTY), 1);
     mbar_init(bar(B_QTFULL), 128);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NSB; ++i) {
       mbar_init(bar(B_SFULL + i), 1);
       mbar_init(bar(B_SEMPTY + i), 128);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_PFULL + i), 128);
       mbar_init(bar(B_PEMPTY + i), 1);
       mbar_init(bar(B_ODONE + i), 1);
@@ -142,7 +152,7 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
     fence_mbar_init();
   }
   if (warp == 0) {
-    // Tiles of 32 tokens: the cursor runs with "block size" 32 and one kv head.
+    // Tiles of TT tokens: the cursor runs with "block size" TT and one kv head.
     const int64_t tot = total_live_blocks(a.seq_lens, a.B, TT, 0, cap, a.dev_status);
     if (lane == 0) {
       *total_s = tot;
@@ -204,19 +214,19 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
     TileCursor c;
     cursor_seek(c, a.seq_lens, a.B, 1, TT, 0, cap, t0, t1);
     int piece_s = -1, piece_o = -1;
-    bool first_of[2] = {false, false};  // per S buffer: tile started a piece
+    bool first_of[2] = {false, false};  // per P buffer (tile parity): tile started a piece
     auto issue_s = [&](int j) -> bool {
       const bool first = (j == 0) || (c.j == 0);
       const bool last = (j + 1 == ntiles) || (c.j + 1 == c.n);
-      const int st = j % NST, sb = j & 1;
-      first_of[sb] = first;
+      const int st = j % NST, sb = j % NSB;
+      first_of[j & 1] = first;
       if (first) {
         ++piece_s;
         if (!mbar_wait(bar(B_QFULL), piece_s & 1)) return false;
         if (!mbar_wait(bar(B_QTFULL), piece_s & 1)) return false;
       }
       if (!mbar_wait(bar(B_KFULL + st), (j / NST) & 1)) return false;
-      if (!mbar_wait(bar(B_SEMPTY + sb), ((j >> 1) & 1) ^ 1)) return false;
+      if (!mbar_wait(bar(B_SEMPTY + sb), ((j / NSB) & 1) ^ 1)) return false;
       tc_fence_after();
       // Base descriptors once per tile; each K step only adds a constant offset.
       const uint64_t kd = smem_desc(sbase + OFF_K + st * NCH * KCH, 16, 1024, kSwizzle128);
@@ -241,7 +251,7 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
       return true;
     };
     auto issue_o = [&](int j) -> bool {
-      const int st = j % NST, sb = j & 1;
+      const int st = j % NST, sb = j & 1;  // sb: P buffer
       const bool first = first_of[sb];
       if (!mbar_wait(bar(B_PFULL + sb), (j >> 1) & 1)) return false;
       if (first) {
@@ -252,7 +262,7 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
       const uint64_t vd = smem_desc(sbase + OFF_K + st * NCH * KCH + (4 * half) * KCH, KCH, 1024,
                                     kSwizzle128);
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk)
+      for (int kk = 0; kk < TT / 16; ++kk)
         mma_ts(tmem + O_COL, tmem + p_col(sb) + kk * 8, desc_add(vd, kk * 2048), ID_O,
                !(first && kk == 0));
       mma_commit(bar(B_ODONE + sb));
@@ -289,8 +299,9 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
       const bool have = r < a.H;
       const int64_t qrow = (int64_t)b * a.H + r;
       for (int ch = 0; ch < NCH - QSM; ++ch) {
-        const uint4* src = (ch < 4)
-            ? reinterpret_cast<const uint4*>(a.q_nope + qrow * DC + 256 + ch * 64)
+        const int gch = QSM + ch;  // chunk of [nope | rope]: 0-7 nope, 8 rope
+        const uint4* src = (gch < 8)
+            ? reinterpret_cast<const uint4*>(a.q_nope + qrow * DC + gch * 64)
             : reinterpret_cast<const uint4*>(a.q_rope + qrow * DR);
         uint32_t w[32];
 #pragma unroll
@@ -386,15 +397,17 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
         p_segbase = c.seg_base;
         p_whole = (c.t == c.seg_base) && (c.t + c.n <= t1);
       }
-      const int sb = j & 1;
-      if (!mbar_wait(bar(B_SFULL + sb), (j >> 1) & 1)) fail();
+      const int ssb = j % NSB, sb = j & 1;  // S buffer, P buffer
+      if (!mbar_wait(bar(B_SFULL + ssb), (j / NSB) & 1)) fail();
       __syncwarp();
       tc_fence_after();
-      uint32_t sv[32];
-      tmem_ld32(tmem + lane_off + s_col(sb), sv);
+      uint32_t sv[TT];
+#pragma unroll
+      for (int c0 = 0; c0 < TT; c0 += 32)
+        tmem_ld32(tmem + lane_off + s_col(ssb) + c0, *reinterpret_cast<uint32_t(*)[32]>(&sv[c0]));
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bar(B_SEMPTY + sb));
+      mbar_arrive(bar(B_SEMPTY + ssb));
 
       const int tok0 = c.j * TT;
       const int blk = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + tok0 / BS);
@@ -440,7 +453,7 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
           m_ref = m_new;
         }
       }
-      uint32_t pk[16];
+      uint32_t pk[TT / 2];
       float psum = 0.f;
 #pragma unroll
       for (int i = 0; i < TT; i += 2) {
@@ -458,8 +471,8 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
       if (nvalid < TT) {
         uint8_t* kt = base + OFF_K + (j % NST) * NCH * KCH + (4 * half) * KCH;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int pidx = r + 128 * k;           // 32 rows x 4 chunks x 8 pieces of 16 B
+        for (int k = 0; k < TT / 4; ++k) {
+          const int pidx = r + 128 * k;           // TT rows x 4 chunks x 8 pieces of 16 B
           const int row = pidx >> 5, ch = (pidx >> 3) & 3, q = pidx & 7;
           if (row >= nvalid)
             *reinterpret_cast<uint4*>(kt + ch * KCH + row * 128 + q * 16) = make_uint4(0, 0, 0, 0);
@@ -469,7 +482,9 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
       if (!mbar_wait(bar(B_PEMPTY + sb), ((j >> 1) & 1) ^ 1)) fail();
       __syncwarp();
       tc_fence_after();
-      tmem_st16(tmem + lane_off + p_col(sb), pk);
+#pragma unroll
+      for (int c0 = 0; c0 < TT / 2; c0 += 16)
+        tmem_st16(tmem + lane_off + p_col(sb) + c0, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c0]));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + sb));
