@@ -213,20 +213,30 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
     constexpr uint32_t ID_O = idesc_bf16(M, DH, 0, 1);  // P (TMEM) x nope half (MN-major)
     TileCursor c;
     cursor_seek(c, a.seq_lens, a.B, 1, TT, 0, cap, t0, t1);
-    int piece_s = -1, piece_o = -1;
-    bool first_of[2] = {false, false};  // per P buffer (tile parity): tile started a piece
-    auto issue_s = [&](int j) -> bool {
+    int piece_s = -1;
+    // Dynamic issue order: the thread polls (non-blocking) and issues whichever
+    // product is ready. With two K stages the load of tile j+2 can only start when
+    // O(j) has completed, so O(j) must not wait behind a score product that is itself
+    // waiting for its tile; a fixed order exposed the whole TMA latency every tile.
+    // Phases cannot alias: S(js) needs the softmax to have read S(js-1), and its K
+    // stage is refilled only after O(js-2), so js <= jo + 2 while O(jo) is pending.
+    bool first_of[4] = {false, false, false, false};  // by tile index mod 4
+    int piece_o = -1;
+    auto ready_s = [&](int j) -> bool {
+      const bool first = (j == 0) || (c.j == 0);
+      const int st = j % NST, sb = j % NSB;
+      if (first && (!mbar_try(bar(B_QFULL), (piece_s + 1) & 1) ||
+                    !mbar_try(bar(B_QTFULL), (piece_s + 1) & 1)))
+        return false;
+      return mbar_try(bar(B_KFULL + st), (j / NST) & 1) &&
+             mbar_try(bar(B_SEMPTY + sb), ((j / NSB) & 1) ^ 1);
+    };
+    auto issue_s = [&](int j) {
       const bool first = (j == 0) || (c.j == 0);
       const bool last = (j + 1 == ntiles) || (c.j + 1 == c.n);
       const int st = j % NST, sb = j % NSB;
-      first_of[j & 1] = first;
-      if (first) {
-        ++piece_s;
-        if (!mbar_wait(bar(B_QFULL), piece_s & 1)) return false;
-        if (!mbar_wait(bar(B_QTFULL), piece_s & 1)) return false;
-      }
-      if (!mbar_wait(bar(B_KFULL + st), (j / NST) & 1)) return false;
-      if (!mbar_wait(bar(B_SEMPTY + sb), ((j / NSB) & 1) ^ 1)) return false;
+      first_of[j & 3] = first;
+      if (first) ++piece_s;
       tc_fence_after();
       // Base descriptors once per tile; each K step only adds a constant offset.
       const uint64_t kd = smem_desc(sbase + OFF_K + st * NCH * KCH, 16, 1024, kSwizzle128);
@@ -248,16 +258,16 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
       mma_commit(bar(B_SFULL + sb));
       if (last) mma_commit(bar(B_QEMPTY));
       cursor_next(c, a.seq_lens, a.B, 1, TT, 0, cap);
-      return true;
     };
-    auto issue_o = [&](int j) -> bool {
-      const int st = j % NST, sb = j & 1;  // sb: P buffer
-      const bool first = first_of[sb];
-      if (!mbar_wait(bar(B_PFULL + sb), (j >> 1) & 1)) return false;
-      if (first) {
-        ++piece_o;
-        if (!mbar_wait(bar(B_OFREE), (piece_o & 1) ^ 1)) return false;
-      }
+    auto ready_o = [&](int j) -> bool {
+      const int sb = j & 1;  // P buffer
+      if (!mbar_try(bar(B_PFULL + sb), (j >> 1) & 1)) return false;
+      return !first_of[j & 3] || mbar_try(bar(B_OFREE), ((piece_o + 1) & 1) ^ 1);
+    };
+    auto issue_o = [&](int j) {
+      const int st = j % NST, sb = j & 1;
+      const bool first = first_of[j & 3];
+      if (first) ++piece_o;
       tc_fence_after();
       const uint64_t vd = smem_desc(sbase + OFF_K + st * NCH * KCH + (4 * half) * KCH, KCH, 1024,
                                     kSwizzle128);
@@ -268,17 +278,25 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
       mma_commit(bar(B_ODONE + sb));
       mma_commit(bar(B_PEMPTY + sb));
       mma_commit(bar(B_KEMPTY + st));
-      return true;
     };
-    bool ok = issue_s(0);
-    for (int j = 0; ok && j < ntiles && !*abort_flag; ++j) {
-      const bool more = j + 1 < ntiles;
-      const bool next_first = more && c.j == 0;  // cursor already sits on tile j + 1
-      if (more && !next_first && !issue_s(j + 1)) { ok = false; break; }
-      if (!issue_o(j)) { ok = false; break; }
-      if (more && next_first && !issue_s(j + 1)) { ok = false; break; }
+    int js = 0, jo = 0;
+    long long idle_since = clock64();
+    while (jo < ntiles) {
+      bool done = false;
+      if (jo < js && ready_o(jo)) {
+        issue_o(jo++);
+        done = true;
+      } else if (js < ntiles && ready_s(js)) {
+        issue_s(js++);
+        done = true;
+      }
+      if (done) {
+        idle_since = clock64();
+      } else if (*abort_flag || clock64() - idle_since > kWaitCycles) {
+        fail();
+        break;
+      }
     }
-    if (!ok) fail();
   } else if (ntiles > 0 && warp >= 2) {
     // ------------------------------------------------------------ softmax / epilogue
     const int quarter = warp & 3;
