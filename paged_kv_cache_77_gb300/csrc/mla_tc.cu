@@ -185,7 +185,24 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
     cursor_seek(c, a.seq_lens, a.B, 1, TT, 0, cap, t0, t1);
     int piece = 0;
     const int rows_oob = (int)(a.num_blocks * BS);
+    // L2 prefetch runs kPrefetch tiles ahead of the loads (second cursor `pc`): a
+    // stage frees only when O(j-2) completes, and the load then finds its tile in L2.
+    constexpr int kPrefetch = 2;
+    TileCursor pc = c;
+    auto prefetch_next = [&](int jp) {
+      if (jp >= ntiles) return;
+      const int ptok = pc.j * TT;
+      const int pblk = __ldg(a.block_table + (int64_t)pc.b * a.max_blocks + ptok / BS);
+      if (pblk >= 0 && (int64_t)pblk < a.num_blocks) {
+        const int prow = pblk * BS + (ptok % BS);
+        for (int ch = 0; ch < 8; ++ch) tma_prefetch_2d(&tm_cn, ch * 64, prow);
+        tma_prefetch_2d(&tm_cr, 0, prow);
+      }
+      cursor_next(pc, a.seq_lens, a.B, 1, TT, 0, cap);
+    };
+    for (int jp = 0; jp < kPrefetch; ++jp) prefetch_next(jp);
     for (int j = 0; j < ntiles && !*abort_flag; ++j) {
+      prefetch_next(j + kPrefetch);
       if (j == 0 || c.j == 0) {
         if (!mbar_wait(bar(B_QEMPTY), (piece & 1) ^ 1)) { fail(); break; }
         mbar_expect_tx(bar(B_QFULL), QSM * QCH);
@@ -195,12 +212,12 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
         ++piece;
       }
       const int st = j % NST;
-      if (!mbar_wait(bar(B_KEMPTY + st), ((j / NST) & 1) ^ 1)) { fail(); break; }
       const int tok0 = c.j * TT;  // first token of the tile within the sequence
       const int blk = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + tok0 / BS);
       const bool ok = blk >= 0 && (int64_t)blk < a.num_blocks;
-      if (!ok) flag_status(a.dev_status, PKV_DEV_BAD_BLOCK);
       const int row = ok ? blk * BS + (tok0 % BS) : rows_oob;
+      if (!mbar_wait(bar(B_KEMPTY + st), ((j / NST) & 1) ^ 1)) { fail(); break; }
+      if (!ok) flag_status(a.dev_status, PKV_DEV_BAD_BLOCK);
       const uint32_t ks = sbase + OFF_K + st * NCH * KCH;
       mbar_expect_tx(bar(B_KFULL + st), NCH * KCH);
       for (int ch = 0; ch < 8; ++ch) tma_load_2d(ks + ch * KCH, &tm_cn, bar(B_KFULL + st), ch * 64, row);
