@@ -543,8 +543,11 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       mbar_arrive(bar(B_OFREE));
     };
 
+    // The block id of a tile is loaded one tile ahead, off the path from S to P.
+    int blk_next = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.j);
     for (int j = 0; j < ntiles; ++j) {
       const bool first = (j == 0) || (c.j == 0) || c.range_start;
+      const int blk = blk_next;
       if (first) {
         if (j > 0) finalize(j - 1);
         m_ref = -INFINITY;
@@ -563,7 +566,6 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       // Visible keys of this row in block c.j: key < kvlen and (causal) key <= c + tok.
       const int tok = c.qt * a.qt_tokens + tok_local;
       const int key_end = a.causal ? min(c.s.c + tok + 1, c.s.kvlen) : c.s.kvlen;
-      const int blk = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.j);
       const bool blk_ok = blk >= 0 && (int64_t)blk < a.num_blocks;
       // Visible columns of this half.
       const int nvis = blk_ok ? max(0, min(64, key_end - c.j * BS - half * 64)) : 0;
@@ -654,6 +656,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + sb));
       pf_next(c, a);
+      if (j + 1 < ntiles) blk_next = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.j);
     }
     if (!aborted) finalize(ntiles - 1);
   }
