@@ -20,6 +20,9 @@ passage it follows:
   doc §2.3.2 skip count max(0, n - W + 1));
 * causal prefill with a cache offset is bottom-right aligned (same page, sdpa
   section and "手写40行" mask m; standalone guide sparse_mode 3);
+* speculative decode: q_len > 1 new rows per sequence under the same bottom-right
+  mask (standalone guide appendix C: a multi-token decode step takes the same mask
+  branch as prefill);
 * MLA absorbed: key = value = cache_nope, and q_rope . cache_rope adds to the
   scores ("KVCache 优化技能" 模式三; standalone guide 模式三; "KV Cache 笔记" MLA).
 
@@ -168,6 +171,45 @@ def paged_prefill(q, cu_seqlens_q, k_cache, v_cache, block_table, seq_lens_kv, b
                     o[begin + r, h], lse[begin + r, h], _ = attend(
                         q[begin + r, h], K[:, kv], V[:, kv], visible, scale)
         begin = end
+    return o, lse
+
+
+# --------------------------------------------------------------------------
+# Speculative (multi-token) decode: q_len new rows per sequence, causal
+# --------------------------------------------------------------------------
+def paged_spec_decode(q, k_cache, v_cache, block_table, seq_lens, block_size: int, scale: float,
+                      window: int = 0, batch_indices=None):
+    """Decode of q_len new query rows per sequence, all rows already written to the
+    cache (MTP / speculative verification; standalone guide, appendix C: q_len > 1
+    takes sparse_mode 3, the bottom-right causal mask; design doc, allocate_slots'
+    lookahead_tokens reserved for speculative decoding).
+
+    q [B, Q, H, d]; seq_lens [B] total lengths including the Q new rows. Query row
+    i of sequence b sits at position len_b - Q + i and sees keys at positions
+    p <= len_b - Q + i, and with a window W > 0 only p > len_b - Q + i - W: each row
+    is the decode step of the prefix that ends at its own position (reading of the
+    pages, which state the window for one query row only). A row whose position is
+    negative (len_b < Q) sees no key: o = 0, lse = -inf.
+    Returns o [B, Q, H, d] and lse [B, Q, H] (rows not in ``batch_indices`` NaN).
+    """
+    B, Q, H, _ = q.shape
+    Hkv = k_cache.shape[2]
+    n_rep = H // Hkv
+    o = np.full((B, Q, H, v_cache.shape[3]), np.nan)
+    lse = np.full((B, Q, H), np.nan)
+    for b in (range(B) if batch_indices is None else batch_indices):
+        n = int(seq_lens[b])
+        K = gather_sequence(k_cache, block_table[b], n, block_size)
+        V = gather_sequence(v_cache, block_table[b], n, block_size)
+        pos = np.arange(n)
+        for i in range(Q):
+            qpos = n - Q + i
+            visible = pos <= qpos
+            if window > 0:
+                visible &= pos > qpos - window
+            for h in range(H):
+                kv = h // n_rep
+                o[b, i, h], lse[b, i, h], _ = attend(q[b, i, h], K[:, kv], V[:, kv], visible, scale)
     return o, lse
 
 
