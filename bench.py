@@ -45,15 +45,27 @@ def peaks():
 
 
 # ---------------------------------------------------------------- byte accounting
+def q_len(wl: synth.Workload) -> int:
+    return wl.q_hi if wl.kind == "spec_decode" else 1
+
+
+def table_window(wl: synth.Workload) -> int:
+    """Window the block table is built with: a speculative step keeps the blocks
+    from the first new row's window start (W + q_len - 1)."""
+    return wl.window + q_len(wl) - 1 if wl.window > 0 else 0
+
+
 def decode_bytes(wl: synth.Workload, d: synth.Draw, out_bytes: int = 2) -> dict:
-    """Algorithmic bytes of one decode step (visible keys only, no block overread)."""
+    """Algorithmic bytes of one decode step (keys visible to some query row, read
+    once per kv head; no block overread)."""
     lens = d.seq_lens.astype(np.int64)
-    vis = np.minimum(lens, wl.window) if wl.window > 0 else lens
+    span = table_window(wl)
+    vis = np.minimum(lens, span) if span > 0 else lens
     row = wl.num_kv_heads * wl.head_dim * 2  # bytes of one token's K (or V) row
     kv = int(vis.sum()) * row * 2
     nblk = -(-lens // wl.block_size)
-    live = nblk - (np.maximum(lens - wl.window, 0) // wl.block_size if wl.window > 0 else 0)
-    qo = wl.batch * wl.num_heads * wl.head_dim * (2 + out_bytes)
+    live = nblk - (np.maximum(lens - span, 0) // wl.block_size if span > 0 else 0)
+    qo = wl.batch * q_len(wl) * wl.num_heads * wl.head_dim * (2 + out_bytes)
     meta = int(live.sum()) * 4 + wl.batch * 4
     attn = kv + qo + meta
     new_rows = int(d.num_new.sum())
@@ -113,8 +125,9 @@ def oracle_sample_step(wl, d, vals, seqs):
 
     post_k = ref.cache_write(vals["k_cache"], vals["k_new"], vals["slots"])
     post_v = ref.cache_write(vals["v_cache"], vals["v_new"], vals["slots"])
-    ref.paged_decode(vals["q"], post_k, post_v, vals["table"], d.seq_lens, wl.block_size, wl.scale,
-                     wl.window, batch_indices=seqs)
+    fn = ref.paged_spec_decode if wl.kind == "spec_decode" else ref.paged_decode
+    fn(vals["q"], post_k, post_v, vals["table"], d.seq_lens, wl.block_size, wl.scale, wl.window,
+       batch_indices=seqs)
 
 
 def oracle_sub_instance(wl: synth.Workload, d: synth.Draw, nseq: int):
@@ -123,13 +136,13 @@ def oracle_sub_instance(wl: synth.Workload, d: synth.Draw, nseq: int):
 
     sub = wl.scaled(batch=nseq)
     lens = d.seq_lens[:nseq]
-    sd = synth.draw_explicit(sub, lens) if wl.layout == "pool" else synth.Draw(
+    sd = synth.draw_explicit(sub, lens, d.num_new[:nseq]) if wl.layout == "pool" else synth.Draw(
         lens, d.num_new[:nseq], d.start_pos[:nseq], None, nseq * d.max_blocks_per_seq,
         d.max_blocks_per_seq)
     v = synth.values(sub, sd, "cpu")
     if wl.layout == "pool":
         table = bp.prepare_block_tables(bp.BlockPool(sd.num_blocks, sd.pool_order), lens,
-                                        wl.block_size, wl.window, sd.max_blocks_per_seq)
+                                        wl.block_size, table_window(wl), sd.max_blocks_per_seq)
     else:
         table = bp.block_table_arange(nseq, d.max_blocks_per_seq)
     slots = bp.slot_mapping(table, sd.start_pos, sd.num_new, wl.block_size)
@@ -256,22 +269,36 @@ def run_ours(args):
     v = synth.values(wl, d, dev)
     if wl.layout == "pool":
         pool = api.BlockPool(d.num_blocks, d.pool_order)
-        table_np = pool.build_block_table(d.seq_lens, wl.block_size, wl.window, d.max_blocks_per_seq)
+        table_np = pool.build_block_table(d.seq_lens, wl.block_size, table_window(wl),
+                                          d.max_blocks_per_seq)
     else:
         table_np = api.build_block_table_arange(wl.batch, d.max_blocks_per_seq)
     slots_np = api.build_slot_mapping(table_np, d.start_pos, d.num_new, wl.block_size)
     table = torch.from_numpy(table_np).to(dev)
     slots = torch.from_numpy(slots_np).to(dev)
     seq_lens = torch.from_numpy(d.seq_lens).to(dev)
-    out = torch.empty((wl.batch, wl.num_heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(api.decode_workspace_size(wl.batch, wl.num_heads, wl.num_kv_heads,
-                                               wl.head_dim), dtype=torch.uint8, device=dev)
+    spec = wl.kind == "spec_decode"
+    out = torch.empty(tuple(v["q"].shape), dtype=torch.bfloat16, device=dev)
+    if spec:
+        ws = torch.empty(api.decode_spec_workspace_size(wl.batch, q_len(wl), wl.num_heads,
+                                                        wl.num_kv_heads, wl.head_dim),
+                         dtype=torch.uint8, device=dev)
+    else:
+        ws = torch.empty(api.decode_workspace_size(wl.batch, wl.num_heads, wl.num_kv_heads,
+                                                   wl.head_dim), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def attend(q):
+        if spec:
+            api.paged_attention_decode_spec(q, v["k_cache"], v["v_cache"], table, seq_lens,
+                                            wl.scale, wl.window, out=out, workspace=ws)
+        else:
+            api.paged_attention_decode(q, v["k_cache"], v["v_cache"], table, seq_lens, wl.scale,
+                                       wl.window, out=out, workspace=ws)
 
     def step():
         api.kv_cache_write(v["k_cache"], v["v_cache"], v["k_new"], v["v_new"], slots)
-        api.paged_attention_decode(v["q"], v["k_cache"], v["v_cache"], table, seq_lens, wl.scale,
-                                   wl.window, out=out, workspace=ws)
+        attend(v["q"])
 
     nbytes = decode_bytes(wl, d, out_bytes=2)
     for _ in range(args.warmup):
@@ -292,8 +319,7 @@ def run_ours(args):
     for i in range(args.steps):
         api.kv_cache_write(v["k_cache"], v["v_cache"], v["k_new"], v["v_new"], slots)
         ev_dec[i][0].record(stream)
-        api.paged_attention_decode(v["q"], v["k_cache"], v["v_cache"], table, seq_lens, wl.scale,
-                                   wl.window, out=out, workspace=ws)
+        attend(v["q"])
         ev_dec[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -327,8 +353,7 @@ def run_ours(args):
         seq_lens.copy_(lens_pin, non_blocking=True)
         slots_dev.copy_(sm_pin, non_blocking=False)
         api.kv_cache_write(v["k_cache"], v["v_cache"], dk, dv, slots_dev)
-        api.paged_attention_decode(dq, v["k_cache"], v["v_cache"], table, seq_lens, wl.scale,
-                                   wl.window, out=out, workspace=ws)
+        attend(dq)
         out_host.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -356,15 +381,18 @@ def run_ours(args):
         "seq_steps_per_s": wl.batch * world / (ms_step * 1e-3),
         "pct_of_peak": value / world / hbm,
         "config": {"workload": f"{wl.name}: B={wl.batch} H={wl.num_heads} H_kv={wl.num_kv_heads} "
-                               f"d={wl.head_dim} bs={wl.block_size} window={wl.window}",
+                               f"d={wl.head_dim} bs={wl.block_size} window={wl.window}"
+                               + (f" q_len={q_len(wl)}" if spec else ""),
                    "seq_lens": f"U[{wl.len_lo},{wl.len_hi}] (sum {int(d.seq_lens.sum())})",
-                   "step": "kv_cache_write + paged_attention_decode (attention + LSE merge)",
+                   "step": "kv_cache_write + paged_attention_decode%s (attention + LSE merge)"
+                           % ("_spec" if spec else ""),
                    "step_bytes": nbytes["step"],
                    "l2": "inputs larger than L2 (KV cache %.2f GB vs 129 MB L2)" % (nbytes["kv"] / 1e9),
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic_from_profiles(f"decode:{wl.name}"),
-                     "kernel": "paged_attention_decode (split-KV attention + merge), "
+                     "kernel": f"paged_attention_decode{'_spec' if spec else ''} "
+                               "(split-KV attention + merge), "
                                f"{dec_ms * 1e3:.1f} us per call",
                      "decode_kernel": ["auto", "cuda_core", "tensor_core"][api.get_decode_kernel()],
                      "peak_kind": peak_kind},
@@ -815,7 +843,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa_long",
-                    choices=["gqa_long", "swa", "mha_tiny", "scatter", "mla", "mixed_prefill",
+                    choices=["gqa_long", "swa", "mha_tiny", "spec_decode", "scatter", "mla",
+                             "mixed_prefill",
                              "fork", "mla_write"])
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller cases for profiling)")

@@ -299,6 +299,36 @@ int pkv_paged_attention_decode(void* out, int32_t out_dtype, float* lse, const v
                                float scale, int32_t window, void* workspace,
                                size_t workspace_bytes, int* dev_status, void* stream);
 
+/* Speculative (multi-token) decode: q_len new query rows per sequence, all already
+ * written to the cache (MTP verification; standalone guide appendix C: a decode
+ * step with q_len > 1 takes the prefill branch, sparse_mode 3, the bottom-right
+ * causal mask; design doc: allocate_slots' lookahead_tokens reserve the slots of
+ * the draft rows). Query row i of sequence b sits at position len_b - q_len + i
+ * and, for each head h (kv head h / (H / H_kv)), attends to the keys at positions
+ * p <= len_b - q_len + i, and with window > 0 only to p > len_b - q_len + i - window:
+ * each row is the decode step of the prefix that ends at its own position. A row
+ * whose position is negative (len_b < q_len) returns o = 0, lse = -inf. With a
+ * window, block_table must keep the blocks from position len_b - q_len + 1 - window
+ * on (the generator's window is window + q_len - 1).
+ *   out [B, q_len, H, head_dim] (bf16 or fp32), lse [B, q_len, H] fp32 (nullable)
+ *   q   [B, q_len, H, head_dim] bf16
+ *   k_cache, v_cache [num_blocks, block_size, H_kv, head_dim] bf16
+ *   block_table [B, max_blocks_per_seq] int32; seq_lens [B] int32 totals (device)
+ * Supported: head_dim 128, block_size 128, q_len 1..4, q_len * H / H_kv <= 32
+ * (PKV_ERR_UNSUPPORTED otherwise). q_len = 1 is pkv_paged_attention_decode.
+ * Workspace: pkv_decode_spec_workspace_size(B, q_len, H, H_kv, head_dim) bytes,
+ * 256-byte aligned. Device pointers; asynchronous on `stream`. */
+size_t pkv_decode_spec_workspace_size(int32_t B, int32_t q_len, int32_t H, int32_t H_kv,
+                                      int32_t head_dim);
+int pkv_paged_attention_decode_spec(void* out, int32_t out_dtype, float* lse, const void* q,
+                                    const void* k_cache, const void* v_cache,
+                                    const int32_t* block_table, int32_t max_blocks_per_seq,
+                                    const int32_t* seq_lens, int32_t B, int32_t q_len, int32_t H,
+                                    int32_t H_kv, int32_t head_dim, int32_t block_size,
+                                    int64_t num_blocks, float scale, int32_t window,
+                                    void* workspace, size_t workspace_bytes, int* dev_status,
+                                    void* stream);
+
 /* Prefill attention over TND-packed queries (standalone guide: sparse_mode 3 for
  * TND paged prefill, q in cumulative form, kv in direct form; "KV Cache 笔记"
  * "手写40行": the causal mask is bottom-right aligned when a cache precedes the new

@@ -57,6 +57,10 @@ SIGNATURES = {
     "pkv_get_decode_kernel": (i32, []),
     "pkv_paged_attention_decode": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
                                              i32, i32, i64, f32, i32, vp, sz, vp, vp]),
+    "pkv_decode_spec_workspace_size": (sz, [i32, i32, i32, i32, i32]),
+    "pkv_paged_attention_decode_spec": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, i32,
+                                                  i32, i32, i32, i32, i64, f32, i32, vp, sz, vp,
+                                                  vp]),
     "pkv_prefill_workspace_size": (sz, []),
     "pkv_paged_attention_prefill": (C.c_int, [vp, i32, vp, vp, vp, i32, vp, vp, vp, i32, vp, i32,
                                               i32, i32, i32, i32, i64, f32, i32, vp, sz, vp, vp]),

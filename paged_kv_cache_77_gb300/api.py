@@ -375,6 +375,35 @@ def paged_attention_decode(q, k_cache, v_cache, block_table, seq_lens, scale: fl
     return out
 
 
+def decode_spec_workspace_size(B: int, q_len: int, H: int, H_kv: int, head_dim: int) -> int:
+    return load().pkv_decode_spec_workspace_size(B, q_len, H, H_kv, head_dim)
+
+
+def paged_attention_decode_spec(q, k_cache, v_cache, block_table, seq_lens, scale: float,
+                                window: int = 0, out=None, lse=None, out_dtype=torch.float32,
+                                workspace=None, dev_status=None, stream=None):
+    """Speculative decode: q [B, q_len, H, d], the q_len new rows of each sequence
+    already in the cache, bottom-right causal; returns out [B, q_len, H, d]."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _dev_bf16(t, n)
+    _dev_i32(block_table, "block_table")
+    _dev_i32(seq_lens, "seq_lens")
+    B, Q, H, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty((B, Q, H, d), dtype=out_dtype, device=q.device)
+    code = PKV_F32 if out.dtype == torch.float32 else PKV_BF16
+    if workspace is None:
+        need = decode_spec_workspace_size(B, Q, H, hkv, d)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    check(load().pkv_paged_attention_decode_spec(
+        _ptr(out), code, _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), B, Q, H, hkv, d, bs, nb, float(scale), int(window),
+        _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream)),
+        "pkv_paged_attention_decode_spec")
+    return out
+
+
 def prefill_workspace_size() -> int:
     return load().pkv_prefill_workspace_size()
 

@@ -126,7 +126,7 @@ int decode_setup(pkv::DecodeArgs& a, bool* empty, const char* what, void* out, i
                  const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
                  int32_t B, int32_t H, int32_t H_kv, int32_t head_dim, int32_t block_size,
                  int64_t num_blocks, float scale, int32_t window, void* workspace,
-                 size_t workspace_bytes, int* dev_status) {
+                 size_t workspace_bytes, int* dev_status, int32_t q_len = 1) {
   using namespace pkv;
   *empty = false;
   PKV_REQUIRE(B >= 0 && H > 0 && H_kv > 0 && max_blocks_per_seq > 0 && num_blocks > 0,
@@ -143,6 +143,11 @@ int decode_setup(pkv::DecodeArgs& a, bool* empty, const char* what, void* out, i
   PKV_REQUIRE(std::isfinite(scale) && scale > 0.f, PKV_ERR_INVALID_ARG,
               "%s: scale must be a positive finite number", what);
   PKV_REQUIRE(window >= 0, PKV_ERR_INVALID_ARG, "%s: negative window", what);
+  PKV_REQUIRE(q_len >= 1 && q_len <= 4, PKV_ERR_UNSUPPORTED, "%s: q_len %d outside 1..4", what,
+              q_len);
+  PKV_REQUIRE(q_len * n_rep <= 32, PKV_ERR_UNSUPPORTED,
+              "%s: q_len * H / H_kv = %d exceeds 32 query rows per kv head", what, q_len * n_rep);
+  PKV_REQUIRE(window <= INT32_MAX - 4, PKV_ERR_INVALID_ARG, "%s: window too large", what);
   PKV_REQUIRE(num_blocks * block_size <= INT32_MAX, PKV_ERR_UNSUPPORTED,
               "%s: num_blocks * block_size must fit in int32", what);
   if (B == 0) {
@@ -155,7 +160,7 @@ int decode_setup(pkv::DecodeArgs& a, bool* empty, const char* what, void* out, i
               PKV_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", what);
   const int G = current_num_sms();
   PKV_REQUIRE(G > 0, PKV_ERR_LAUNCH, "%s: no CUDA device", what);
-  const size_t need = decode_workspace_bytes(B, H, H_kv, head_dim, G);
+  const size_t need = decode_workspace_bytes(B, H * q_len, H_kv, head_dim, G);
   PKV_REQUIRE(workspace && workspace_bytes >= need && (((uintptr_t)workspace) & 255) == 0,
               PKV_ERR_WORKSPACE, "%s: workspace needs %zu bytes, 256-aligned", what, need);
   a = DecodeArgs{};
@@ -173,7 +178,9 @@ int decode_setup(pkv::DecodeArgs& a, bool* empty, const char* what, void* out, i
   a.Hkv = H_kv;
   a.n_rep = n_rep;
   a.max_blocks = max_blocks_per_seq;
-  a.window = window;
+  a.q_len = q_len;
+  a.row_window = window;
+  a.window = window > 0 ? window + q_len - 1 : 0;
   a.out_f32 = out_dtype == PKV_F32;
   a.num_ctas = G;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -207,6 +214,34 @@ int pkv_paged_attention_decode(void* out, int32_t out_dtype, float* lse, const v
                          "pkv_paged_attention_decode (attention)");
   if (rc != PKV_OK) return rc;
   return launch_status(launch_decode_merge(a, s), "pkv_paged_attention_decode (merge)");
+}
+
+size_t pkv_decode_spec_workspace_size(int32_t B, int32_t q_len, int32_t H, int32_t H_kv,
+                                      int32_t head_dim) {
+  if (B < 0 || q_len < 1 || H <= 0 || H_kv <= 0 || H % H_kv || head_dim <= 0) return 0;
+  return decode_workspace_bytes(B, H * q_len, H_kv, head_dim, current_num_sms());
+}
+
+int pkv_paged_attention_decode_spec(void* out, int32_t out_dtype, float* lse, const void* q,
+                                    const void* k_cache, const void* v_cache,
+                                    const int32_t* block_table, int32_t max_blocks_per_seq,
+                                    const int32_t* seq_lens, int32_t B, int32_t q_len, int32_t H,
+                                    int32_t H_kv, int32_t head_dim, int32_t block_size,
+                                    int64_t num_blocks, float scale, int32_t window,
+                                    void* workspace, size_t workspace_bytes, int* dev_status,
+                                    void* stream) {
+  DecodeArgs a;
+  bool empty;
+  const int rc0 = decode_setup(a, &empty, "pkv_paged_attention_decode_spec", out, out_dtype, lse,
+                               q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, B,
+                               H, H_kv, head_dim, block_size, num_blocks, scale, window, workspace,
+                               workspace_bytes, dev_status, q_len);
+  if (rc0 != PKV_OK || empty) return rc0;
+  clear_error();
+  cudaStream_t s = (cudaStream_t)stream;
+  int rc = launch_status(launch_decode_spec(a, s), "pkv_paged_attention_decode_spec (attention)");
+  if (rc != PKV_OK) return rc;
+  return launch_status(launch_decode_merge(a, s), "pkv_paged_attention_decode_spec (merge)");
 }
 
 int pkv_kv_cache_write_fp8(void* k_cache, void* v_cache, float* k_scale, float* v_scale,

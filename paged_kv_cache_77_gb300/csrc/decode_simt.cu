@@ -237,16 +237,17 @@ __global__ void __launch_bounds__(simt::THREADS, 1) decode_simt_kernel(DecodeArg
 
 // --------------------------------------------------------------------------
 // LSE merge of split pieces: lse = log sum_i exp(lse_i), o = sum_i exp(lse_i - lse) o_i.
-// One CTA per (b, kv head) with one warp per query head of the group; lane = 4
-// consecutive output elements. Segments finished inside one attention CTA are
-// skipped; empty sequences get o = 0, lse = -inf.
+// Grid (b * Hkv + kv head, block of 16 query rows); one warp per query row of the
+// group (q_len * n_rep rows, ordered token then head); lane = 4 consecutive output
+// elements. Segments finished inside one attention CTA are skipped; empty
+// sequences get o = 0, lse = -inf.
 // --------------------------------------------------------------------------
 __global__ void __launch_bounds__(512) decode_merge_kernel(DecodeArgs a) {
   constexpr int D = 128;
   const int seg = blockIdx.x;  // b * Hkv + g
   const int b = seg / a.Hkv, g = seg % a.Hkv;
-  const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_rep = a.n_rep;
+  const int h = blockIdx.y * 16 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int n_rep = a.n_rep * a.q_len;  // rows per (b, kv head)
   if (h >= n_rep) return;
   const int bs = 128;
   const int cap = a.max_blocks * bs;
@@ -264,7 +265,8 @@ __global__ void __launch_bounds__(512) decode_merge_kernel(DecodeArgs a) {
   const int64_t T = tot * a.Hkv, G = a.num_ctas;
   const int n = live_blocks(clamp_len(__ldg(a.seq_lens + b), cap), bs, a.window).n;
   const int64_t base = before * a.Hkv + (int64_t)g * n;
-  const int64_t row = (int64_t)b * a.H + (int64_t)g * n_rep + h;
+  const int64_t row =
+      ((int64_t)b * a.q_len + h / a.n_rep) * a.H + (int64_t)g * a.n_rep + h % a.n_rep;
   auto put = [&](float4 v) {
     if (a.out_f32) {
       reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + row * D)[lane] = v;
@@ -306,6 +308,7 @@ __global__ void __launch_bounds__(512) decode_merge_kernel(DecodeArgs a) {
   if (a.lse && lane == 0) a.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * kLn2 : -INFINITY;
 }
 
+// H here counts every query row of a sequence (q_len * heads).
 size_t decode_workspace_bytes(int B, int H, int Hkv, int D, int G) {
   const int64_t slots = (int64_t)B * Hkv + G;
   const int64_t n_rep = H / Hkv;
@@ -316,7 +319,7 @@ size_t decode_workspace_bytes(int B, int H, int Hkv, int D, int G) {
 
 void decode_workspace_carve(DecodeArgs& a, void* ws) {
   const int64_t slots = (int64_t)a.B * a.Hkv + a.num_ctas;
-  const size_t o_bytes = (size_t)(slots * a.n_rep * 128 * 4 + 255) / 256 * 256;
+  const size_t o_bytes = (size_t)(slots * a.n_rep * a.q_len * 128 * 4 + 255) / 256 * 256;
   a.ws_o = reinterpret_cast<float*>(ws);
   a.ws_lse = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + o_bytes);
 }
@@ -344,7 +347,9 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream) {
   if (a.B * a.Hkv == 0) return cudaSuccess;
-  decode_merge_kernel<<<a.B * a.Hkv, 32 * a.n_rep, 0, stream>>>(a);
+  const int rows = a.n_rep * a.q_len;
+  const dim3 grid(a.B * a.Hkv, (rows + 15) / 16);
+  decode_merge_kernel<<<grid, 32 * (rows < 16 ? rows : 16), 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,481 @@
+// Paged decode attention for GQA head groups on the tcgen05 tensor cores.
+//
+// Same result as the CUDA-core kernel: for each (b, h), softmax(scale * q . K^T) V
+// over the visible positions of sequence b read through block_table ("KV Cache 笔记",
+// decode incremental form; GQA mapping h -> h / n_rep). The n_rep query heads of a
+// kv head share every K/V tile, so each tile is a small dense contraction:
+//
+//   S^T [128 tokens x N] = K_tile [128 x 128 d] . Q_g^T        (M = 128)
+//   O^T [128 d x N]      = V_tile^T [128 d x 128 tokens] . P^T (M = 128)
+//
+// ("swap AB": the token / d axis takes the M = 128 side of the MMA). Both products
+// run as tcgen05.mma kind::f16 (bf16 in, fp32 accumulate in tensor memory).
+//
+// The same kernel runs speculative (multi-token) decode: with q_len = QL new rows
+// per sequence (standalone guide, appendix C: a multi-token decode step takes the
+// bottom-right causal mask of prefill), the QL * n_rep query rows of a kv head are
+// the N columns, ordered (token, head). Query token i sits at position
+// len - QL + i and sees keys p <= len - QL + i (and, with a window W, p > that
+// position - W). The rows are padded to N = 16 or 32; each block of 16 columns has
+// its own four softmax warps.
+//
+// Work split: the balanced (b, kv head, block) tile list of device_common.cuh, one
+// persistent CTA per SM. Warp roles:
+//   warp 0      TMA producer: Q of each piece (box {64 d, n_rep heads, QL tokens}),
+//               K and V halves of each tile (box {64 d, 1 head, 128 tokens}),
+//               128-byte swizzle, 3-deep ring;
+//   warp 1      MMA issuer; S^T of tile j+1 is issued before O^T of tile j so
+//               that the softmax of tile j+1 overlaps the value product of j;
+//   warps 2..   softmax, four warps per 16 columns: thread = token lane of S^T.
+//               Block max per column by warp shuffles plus a shared-memory
+//               exchange; exp2 in fp32 with q . k pre-scaled by scale * log2 e;
+//               P^T written as bf16 in the swizzled K-major layout of the second
+//               product's B operand; then thread = d lane of O^T, accumulating O
+//               in registers with the online-softmax rescale.
+// All waits are bounded (tc_ptx.cuh); a timeout sets PKV_DEV_TIMEOUT and every
+// role winds down.
+//
+// Roofline: HBM. Algorithmic bytes per tile = 2 * 128 tokens * 128 d * 2 bytes.
+#pragma once
+
+#include <cuda.h>
+
+#include "device_common.cuh"
+#include "launch.h"
+#include "tc_ptx.cuh"
+
+namespace pkv {
+namespace tcd {
+
+constexpr int D = 128;
+constexpr int BS = 128;
+constexpr int NST = 3;
+constexpr int HALF = 16384;          // [128 rows x 128 bytes], one 64-wide d half
+constexpr int TILE = 2 * HALF;       // one K (or V) tile of one kv head
+
+enum {
+  B_KFULL = 0,
+  B_VFULL = B_KFULL + NST,
+  B_KVEMPTY = B_VFULL + NST,
+  B_QFULL = B_KVEMPTY + NST,
+  B_QEMPTY = B_QFULL + 2,
+  B_SFULL = B_QEMPTY + 2,
+  B_SEMPTY = B_SFULL + 2,
+  B_PFULL = B_SEMPTY + 2,
+  B_PEMPTY = B_PFULL + 2,
+  B_OFULL = B_PEMPTY + 2,
+  B_OEMPTY = B_OFULL + 2,
+  B_COUNT = B_OEMPTY + 2
+};
+
+// One kernel instance: NR = QL * n_rep query rows per (b, kv head), padded to the
+// MMA N; NCH blocks of 16 columns, each with four softmax warps.
+template <int NREP, int QL>
+struct Shape {
+  static constexpr int NR = NREP * QL;
+  static constexpr int N = NR <= 16 ? 16 : 32;
+  static constexpr int NCH = N / 16;
+  static constexpr int CW = NCH == 1 ? NR : 16;  // columns a softmax thread carries
+  static constexpr int NTHREADS = 64 + 128 * NCH;
+  static constexpr int QBUF = N * 256;           // N rows x 128 d, two 64-wide halves
+  static constexpr int PBUF = N * 256;           // N rows x 128 tokens, two halves
+  // Shared-memory layout (offsets from a 1024-aligned base).
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + NST * TILE;
+  static constexpr int OFF_Q = OFF_V + NST * TILE;
+  static constexpr int OFF_P = OFF_Q + 2 * QBUF;
+  static constexpr int OFF_BAR = OFF_P + 2 * PBUF;
+  static constexpr int OFF_RED = OFF_BAR + B_COUNT * 8;   // float [2][4][N]
+  static constexpr int OFF_LRED = OFF_RED + 2 * 4 * N * 4;  // float [4][N]
+  static constexpr int OFF_MISC = OFF_LRED + 4 * N * 4;     // tmem addr, abort, total, snaps
+  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;   // + alignment slack
+  // TMEM columns: S^T buffers at 0 and N, O^T buffers at 2N and 3N.
+  static constexpr uint32_t TMEM_COLS = 4 * N;
+  static_assert(NR <= 32, "at most 32 query rows per kv head");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+// Byte offset of (row, k) inside a K-major 128-byte-swizzled half [rows x 64].
+__device__ __forceinline__ uint32_t sw128(int row, int k) {
+  return (uint32_t)(row * 128 + ((((k >> 3) ^ row) & 7) << 4) + (k & 7) * 2);
+}
+
+}  // namespace tcd
+
+template <int NREP, int QL>
+__global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
+    decode_tc_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q) {
+  using namespace tcd;
+  using namespace tc;
+  using L = Shape<NREP, QL>;
+  constexpr int NR = L::NR, N = L::N, NCH = L::NCH, CW = L::CW;
+  constexpr int QBUF = L::QBUF, PBUF = L::PBUF;
+  constexpr int OFF_K = L::OFF_K, OFF_V = L::OFF_V, OFF_Q = L::OFF_Q, OFF_P = L::OFF_P;
+  constexpr int OFF_BAR = L::OFF_BAR, OFF_MISC = L::OFF_MISC;
+  constexpr uint32_t TMEM_COLS = L::TMEM_COLS;
+  constexpr int NSOFT = 128 * NCH;  // softmax threads
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(base);
+  auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
+  auto s_col = [](int b) { return (uint32_t)(b * N); };
+  auto o_col = [](int b) { return (uint32_t)(2 * N + b * N); };
+  float* red = reinterpret_cast<float*>(base + L::OFF_RED);
+  float* lred = reinterpret_cast<float*>(base + L::OFF_LRED);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(base + OFF_MISC);
+  volatile uint32_t* abort_flag = misc + 1;
+  long long* total_s = reinterpret_cast<long long*>(misc + 2);
+  volatile uint32_t* abort_snap = misc + 4;  // [NCH][2]: flag as seen before each softmax barrier
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cap = a.max_blocks * BS;
+
+  if (tid == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(bar(B_KFULL + i), 1);
+      mbar_init(bar(B_VFULL + i), 1);
+      mbar_init(bar(B_KVEMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_QFULL + i), 1);
+      mbar_init(bar(B_QEMPTY + i), 1);
+      mbar_init(bar(B_SFULL + i), 1);
+      mbar_init(bar(B_SEMPTY + i), NSOFT);
+      mbar_init(bar(B_PFULL + i), NSOFT);
+      mbar_init(bar(B_PEMPTY + i), 1);
+      mbar_init(bar(B_OFULL + i), 1);
+      mbar_init(bar(B_OEMPTY + i), NSOFT);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    const int64_t tot = total_live_blocks(a.seq_lens, a.B, BS, a.window, cap, a.dev_status);
+    if (lane == 0) *total_s = tot * a.Hkv;
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_q);
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(sbase + OFF_MISC, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const int64_t T = *total_s, G = gridDim.x;
+  const int64_t t0 = cta_tile_start(blockIdx.x, T, G), t1 = cta_tile_start(blockIdx.x + 1, T, G);
+  const int ntiles = (int)(t1 - t0);
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    flag_status(a.dev_status, PKV_DEV_TIMEOUT);
+  };
+
+  if (ntiles > 0 && warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    TileCursor c;
+    cursor_seek(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap, t0, t1);
+    int piece = 0;
+    const int rows_oob = (int)(a.num_blocks * BS);  // first row past the cache: zero fill
+    for (int j = 0; j < ntiles && !*abort_flag; ++j) {
+      if (j == 0 || c.j == 0) {
+        const int qb = piece & 1;
+        if (!mbar_wait(bar(B_QEMPTY + qb), ((piece >> 1) & 1) ^ 1)) { fail(); break; }
+        mbar_expect_tx(bar(B_QFULL + qb), NR * 256);
+        const uint32_t qs = sbase + OFF_Q + qb * QBUF;
+        tma_load_3d(qs, &tm_q, bar(B_QFULL + qb), 0, c.g * NREP, c.b * QL);
+        tma_load_3d(qs + QBUF / 2, &tm_q, bar(B_QFULL + qb), 64, c.g * NREP, c.b * QL);
+        ++piece;
+      }
+      const int st = j % NST;
+      if (!mbar_wait(bar(B_KVEMPTY + st), ((j / NST) & 1) ^ 1)) { fail(); break; }
+      const int blk = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.jlo + c.j);
+      const bool ok = blk >= 0 && (int64_t)blk < a.num_blocks;
+      if (!ok) flag_status(a.dev_status, PKV_DEV_BAD_BLOCK);
+      const int row = ok ? blk * BS : rows_oob;
+      const uint32_t ks = sbase + OFF_K + st * TILE, vs = sbase + OFF_V + st * TILE;
+      mbar_expect_tx(bar(B_KFULL + st), TILE);
+      tma_load_3d(ks, &tm_k, bar(B_KFULL + st), 0, c.g, row);
+      tma_load_3d(ks + HALF, &tm_k, bar(B_KFULL + st), 64, c.g, row);
+      mbar_expect_tx(bar(B_VFULL + st), TILE);
+      tma_load_3d(vs, &tm_v, bar(B_VFULL + st), 0, c.g, row);
+      tma_load_3d(vs + HALF, &tm_v, bar(B_VFULL + st), 64, c.g, row);
+      cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
+    }
+  } else if (ntiles > 0 && warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t ID_S = idesc_bf16(128, N, 0, 0);  // K (K-major) x Q^T (K-major)
+    constexpr uint32_t ID_O = idesc_bf16(128, N, 1, 0);  // V^T (MN-major) x P^T (K-major)
+    TileCursor c;
+    cursor_seek(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap, t0, t1);
+    int piece = -1;
+    bool ok = true;
+    auto issue_s = [&](int j) -> bool {
+      const bool first = (j == 0) || (c.j == 0);
+      const bool last = (j + 1 == ntiles) || (c.j + 1 == c.n);
+      if (first) ++piece;
+      const int qb = piece & 1, st = j % NST, sb = j & 1;
+      if (first && !mbar_wait(bar(B_QFULL + qb), (piece >> 1) & 1)) return false;
+      if (!mbar_wait(bar(B_KFULL + st), (j / NST) & 1)) return false;
+      if (!mbar_wait(bar(B_SEMPTY + sb), ((j >> 1) & 1) ^ 1)) return false;
+      tc_fence_after();
+      // Base descriptors once per tile; each K step only adds a constant offset.
+      const uint64_t kd = smem_desc(sbase + OFF_K + st * TILE, 16, 1024, kSwizzle128);
+      const uint64_t qd = smem_desc(sbase + OFF_Q + qb * QBUF, 16, 1024, kSwizzle128);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss(tmem + s_col(sb), desc_add(kd, (kk >> 2) * HALF + (kk & 3) * 32),
+               desc_add(qd, (kk >> 2) * (QBUF / 2) + (kk & 3) * 32), ID_S, kk > 0);
+      mma_commit(bar(B_SFULL + sb));
+      if (last) mma_commit(bar(B_QEMPTY + qb));
+      cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
+      return true;
+    };
+    auto issue_o = [&](int j) -> bool {
+      const int st = j % NST, ob = j & 1;
+      if (!mbar_wait(bar(B_VFULL + st), (j / NST) & 1)) return false;
+      if (!mbar_wait(bar(B_PFULL + ob), (j >> 1) & 1)) return false;
+      if (!mbar_wait(bar(B_OEMPTY + ob), ((j >> 1) & 1) ^ 1)) return false;
+      tc_fence_after();
+      const uint64_t vd = smem_desc(sbase + OFF_V + st * TILE, HALF, 1024, kSwizzle128);
+      const uint64_t pd = smem_desc(sbase + OFF_P + ob * PBUF, 16, 1024, kSwizzle128);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss(tmem + o_col(ob), desc_add(vd, kk * 2048),
+               desc_add(pd, (kk >> 2) * (PBUF / 2) + (kk & 3) * 32), ID_O, kk > 0);
+      mma_commit(bar(B_OFULL + ob));
+      mma_commit(bar(B_PEMPTY + ob));
+      mma_commit(bar(B_KVEMPTY + st));
+      return true;
+    };
+    ok = issue_s(0);
+    for (int j = 0; ok && j < ntiles && !*abort_flag; ++j) {
+      if (j + 1 < ntiles && !issue_s(j + 1)) { ok = false; break; }
+      if (!issue_o(j)) { ok = false; break; }
+    }
+    if (!ok) fail();
+  } else if (ntiles > 0 && warp >= 2) {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int chunk = (warp - 2) >> 2;            // block of 16 columns
+    const int qbase = chunk * 16;                 // first column of the block
+    const int quarter = warp & 3;                 // TMEM lane quarter this warp may access
+    const int r = quarter * 32 + lane;            // token row of S^T, d row of O^T
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int bar_id = 1 + chunk;                 // named barrier of the block's 128 threads
+    float* cred = red + qbase;                    // [2][4][N] from this block's first column
+    float* clred = lred + qbase;                  // [4][N]
+    volatile uint32_t* snap = abort_snap + 2 * chunk;
+    TileCursor c;
+    cursor_seek(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap, t0, t1);
+    // o_reg holds the output of the tiles folded so far, scaled to the running max
+    // of the newest tile whose scores are done: acc_o(j - 1) runs after tile j's
+    // rescale factors are known and applies them together with O(j - 1).
+    float m_run[CW], l_part[CW], o_reg[CW];
+    // State of the piece being accumulated.
+    int pb = 0, pg = 0;
+    int64_t p_first = t0, p_segbase = 0;
+    bool p_whole = false;
+    bool aborted = false;
+    float ones[CW];
+#pragma unroll
+    for (int i = 0; i < CW; ++i) ones[i] = 1.f;
+
+    auto acc_o = [&](int jj, const float (&mult)[CW]) {
+      const int ob = jj & 1;
+      if (!mbar_wait(bar(B_OFULL + ob), (jj >> 1) & 1)) fail();
+      __syncwarp();
+      tc_fence_after();
+      uint32_t v[16];
+      tmem_ld16(tmem + lane_off + o_col(ob) + qbase, v);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(B_OEMPTY + ob));
+#pragma unroll
+      for (int i = 0; i < CW; ++i) o_reg[i] = (o_reg[i] + __uint_as_float(v[i])) * mult[i];
+    };
+    auto finalize = [&]() {
+#pragma unroll
+      for (int i = 0; i < CW; ++i) {
+        float l = l_part[i];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) clred[quarter * N + i] = l;
+      }
+      named_bar_sync(bar_id, 128);
+      const int64_t slot = (p_first == p_segbase) ? (int64_t)pb * a.Hkv + pg
+                                                  : (int64_t)a.B * a.Hkv + blockIdx.x;
+#pragma unroll
+      for (int i = 0; i < CW; ++i) {
+        const int h = qbase + i;  // column: query token h / NREP, head h % NREP
+        if (NCH > 1 && h >= NR) continue;
+        const float l = clred[i] + clred[N + i] + clred[2 * N + i] + clred[3 * N + i];
+        const float ov = l > 0.f ? o_reg[i] / l : 0.f;
+        const float lse2 = l > 0.f ? m_run[i] + log2f(l) : -INFINITY;
+        if (p_whole) {
+          const int64_t row = ((int64_t)pb * QL + h / NREP) * a.H + (int64_t)pg * NREP + h % NREP;
+          if (a.out_f32)
+            reinterpret_cast<float*>(a.out)[row * D + r] = ov;
+          else
+            reinterpret_cast<__nv_bfloat16*>(a.out)[row * D + r] = __float2bfloat16_rn(ov);
+          if (a.lse && r == 0) a.lse[row] = lse2 * kLn2;
+        } else {
+          a.ws_o[(slot * NR + h) * D + r] = ov;
+          if (r == 0) a.ws_lse[slot * NR + h] = lse2;
+        }
+      }
+      named_bar_sync(bar_id, 128);  // lred reused by the next piece
+    };
+
+    for (int j = 0; j < ntiles; ++j) {
+      const bool first = (j == 0) || (c.j == 0);
+      if (first) {
+        if (j > 0) {
+          acc_o(j - 1, ones);
+          finalize();
+        }
+#pragma unroll
+        for (int i = 0; i < CW; ++i) {
+          m_run[i] = -INFINITY;
+          l_part[i] = 0.f;
+          o_reg[i] = 0.f;
+        }
+        pb = c.b;
+        pg = c.g;
+        p_first = c.t;
+        p_segbase = c.seg_base;
+        p_whole = (c.t == c.seg_base) && (c.t + c.n <= t1);
+      }
+      // ---- scores of tile j
+      const int sb = j & 1;
+      if (!mbar_wait(bar(B_SFULL + sb), (j >> 1) & 1)) fail();
+      __syncwarp();
+      tc_fence_after();
+      uint32_t sv[16];
+      tmem_ld16(tmem + lane_off + s_col(sb) + qbase, sv);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(B_SEMPTY + sb));
+
+      // Visible columns of this token: query tokens [qlo, qhi], i.e. columns
+      // [qlo * NREP, (qhi + 1) * NREP) of the piece. dpos = position - (len - QL):
+      // token i sees it iff dpos <= i, and with a window iff i <= dpos + W - 1.
+      const int blk = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.jlo + c.j);
+      const bool blk_ok = blk >= 0 && (int64_t)blk < a.num_blocks;
+      const int dpos = (c.jlo + c.j) * BS + r - (c.len - QL);
+      const int qlo = dpos > 0 ? dpos : 0;
+      int qhi = QL - 1;
+      if (a.row_window > 0 && dpos + a.row_window - 1 < qhi) qhi = dpos + a.row_window - 1;
+      const bool any = blk_ok && qlo <= qhi;
+      const int ilo = any ? qlo * NREP - qbase : 0;
+      const int ihi = any ? (qhi + 1) * NREP - qbase : 0;
+      float x[CW];
+#pragma unroll
+      for (int i = 0; i < CW; ++i) {
+        x[i] = (i >= ilo && i < ihi) ? __uint_as_float(sv[i]) * a.scale_log2 : -INFINITY;
+        float m = x[i];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) cred[(sb * 4 + quarter) * N + i] = m;
+      }
+      // One thread snapshots the abort flag before the barrier so that every
+      // thread of the block takes the same decision after it.
+      if (r == 0) snap[sb] = *abort_flag;
+      named_bar_sync(bar_id, 128);
+      if (snap[sb]) {
+        aborted = true;
+        break;
+      }
+      float alpha[CW];
+#pragma unroll
+      for (int i = 0; i < CW; ++i) {
+        const float* rr = cred + sb * 4 * N + i;
+        const float mb = fmaxf(fmaxf(rr[0], rr[N]), fmaxf(rr[2 * N], rr[3 * N]));
+        const float mn = fmaxf(m_run[i], mb);
+        alpha[i] = (mn == -INFINITY) ? 1.f : exp2f(m_run[i] - mn);
+        // P enters the value product as bf16; the normaliser sums the same rounded
+        // weights, so the output is an exact convex combination of V rows.
+        const float p = __bfloat162float(__float2bfloat16_rn(
+            (x[i] == -INFINITY) ? 0.f : exp2f(x[i] - mn)));
+        l_part[i] = l_part[i] * alpha[i] + p;
+        m_run[i] = mn;
+        x[i] = p;
+      }
+      // A position no query row sees may hold any bytes (an unwritten tail slot):
+      // once the tile has landed, zero its V row so that its weight 0 cannot meet a
+      // NaN in the value product (made visible to the MMA by the proxy fence before
+      // PFULL). Positions some row sees hold written, finite rows.
+      if (!any && chunk == 0) {
+        const int st = j % NST;
+        if (!mbar_wait(bar(B_VFULL + st), (j / NST) & 1)) fail();
+        uint8_t* vrow = base + OFF_V + st * TILE + r * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          *reinterpret_cast<uint4*>(vrow + q * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vrow + HALF + q * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      // ---- P^T (bf16) into the B operand of the value product
+      if (!mbar_wait(bar(B_PEMPTY + sb), ((j >> 1) & 1) ^ 1)) fail();
+      // Column qbase + i sits in 8-row atom (qbase + i) / 8 = qbase / 8 + i / 8.
+      uint8_t* ps = base + OFF_P + sb * PBUF + (r >> 6) * (PBUF / 2) + qbase * 128;
+      const int k = r & 63;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float p = i < CW ? x[i < CW ? i : 0] : 0.f;
+        *reinterpret_cast<__nv_bfloat16*>(ps + (i >> 3) * 1024 + sw128(i & 7, k)) = __float2bfloat16_rn(p);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(B_PFULL + sb));
+      // ---- fold the previous tile's O^T into the registers
+      if (!first) acc_o(j - 1, alpha);
+      cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
+    }
+    if (!aborted) {
+      acc_o(ntiles - 1, ones);
+      finalize();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// bf16 tensor map with a 128-byte swizzle and 256-byte L2 promotion (decode_tc.cu).
+bool make_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
+                    const uint64_t* strides, const uint32_t* box);
+
+template <int NREP, int QL>
+static cudaError_t launch_tc_n(const DecodeArgs& a, cudaStream_t stream) {
+  using namespace tcd;
+  using L = Shape<NREP, QL>;
+  CUtensorMap tk, tv, tq;
+  const uint64_t rows = (uint64_t)a.num_blocks * BS;
+  const uint64_t kdims[3] = {D, (uint64_t)a.Hkv, rows};
+  const uint64_t kstr[2] = {D * 2, (uint64_t)a.Hkv * D * 2};
+  const uint32_t kbox[3] = {64, 1, BS};
+  // q [B * QL, H, D]: one box is the n_rep heads of a kv head for the QL tokens.
+  const uint64_t qdims[3] = {D, (uint64_t)a.H, (uint64_t)a.B * QL};
+  const uint64_t qstr[2] = {D * 2, (uint64_t)a.H * D * 2};
+  const uint32_t qbox[3] = {64, NREP, QL};
+  if (!make_tmap_bf16(&tk, a.k_cache, 3, kdims, kstr, kbox) ||
+      !make_tmap_bf16(&tv, a.v_cache, 3, kdims, kstr, kbox) ||
+      !make_tmap_bf16(&tq, a.q, 3, qdims, qstr, qbox))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NREP, QL>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  decode_tc_kernel<NREP, QL><<<a.num_ctas, L::NTHREADS, L::SMEM_BYTES, stream>>>(a, tk, tv, tq);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -26,18 +26,21 @@ cudaError_t launch_mla_rmsnorm_rope_write(void* cache_nope, void* cache_rope, vo
 
 // Arguments of the split-KV decode kernels and their LSE merge.
 struct DecodeArgs {
-  const uint16_t* q;          // [B, H, D] bf16
+  const uint16_t* q;          // [B, q_len, H, D] bf16
   const uint8_t* k_cache;     // [nb, bs, Hkv, D] bf16
   const uint8_t* v_cache;
   const int32_t* block_table; // [B, max_blocks]
   const int32_t* seq_lens;    // [B]
-  void* out;                  // [B, H, D] bf16 or f32
-  float* lse;                 // [B, H] or null
-  float* ws_o;                // [(B*Hkv + G) * n_rep * D] partial outputs
-  float* ws_lse;              // [(B*Hkv + G) * n_rep] partial log2-sum-exp
+  void* out;                  // [B, q_len, H, D] bf16 or f32
+  float* lse;                 // [B, q_len, H] or null
+  float* ws_o;                // [(B*Hkv + G) * q_len * n_rep * D] partial outputs
+  float* ws_lse;              // [(B*Hkv + G) * q_len * n_rep] partial log2-sum-exp
   int* dev_status;
   int64_t num_blocks;
-  int B, H, Hkv, n_rep, max_blocks, window, out_f32;
+  int B, H, Hkv, n_rep, max_blocks, out_f32;
+  int q_len;                  // new query rows per sequence (1 = plain decode)
+  int row_window;             // window of one query row (0 = full attention)
+  int window;                 // live-block span: row_window + q_len - 1 (0 = all)
   int num_ctas;               // G: CTAs of the attention kernel (one per SM)
   float scale_log2;           // scale * log2(e)
   const float* k_scale;       // FP8 cache only: [nb, Hkv, bs] per-row scales
@@ -52,6 +55,8 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream);
 // tcgen05 split-KV decode for head groups (n_rep 1..16), same partials as above.
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream);
+// The same kernel for q_len 1..4 query rows per sequence (q_len * n_rep <= 32).
+cudaError_t launch_decode_spec(const DecodeArgs& a, cudaStream_t stream);
 // tcgen05 split-KV decode over an FP8 (E4M3) cache with per-row scales; same
 // partials and merge as above.
 cudaError_t launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream);

@@ -34,7 +34,7 @@ class Workload:
     """One synthetic workload (a batch of sequences over one attention layer)."""
 
     name: str
-    kind: str  # "decode" | "mla_decode" | "prefill"
+    kind: str  # "decode" | "spec_decode" | "mla_decode" | "prefill"
     batch: int
     num_heads: int
     num_kv_heads: int
@@ -47,7 +47,7 @@ class Workload:
     max_seq_len: int = 0  # arange layout only: tokens per sequence slice
     len_lo: int = 1  # total-length draw bounds (decode) or prior-context bounds (prefill)
     len_hi: int = 1
-    q_lo: int = 1  # prefill: new-token count bounds
+    q_lo: int = 1  # prefill: new-token count bounds; spec_decode: q_lo = q_hi = q_len
     q_hi: int = 1
     forced_q1: int = 0  # prefill: leading sequences forced to q_len 1
     seed: int = 0
@@ -84,6 +84,12 @@ def _wl():
             name="mla", kind="mla_decode", batch=128, num_heads=128, num_kv_heads=1,
             head_dim=512, rope_dim=64, scale=inv(192), len_lo=1, len_hi=8192, seed=1003,
             notes="seq_len ~ U[1,8192]; scale 1/sqrt(128+64)"),
+        # Speculative (MTP) decode on the GQA long-context shape: 4 new rows per
+        # sequence (the verified token plus 3 drafts), bottom-right causal.
+        "spec_decode": Workload(
+            name="spec_decode", kind="spec_decode", batch=64, num_heads=64, num_kv_heads=8,
+            head_dim=128, scale=inv(128), len_lo=4, len_hi=32768, q_lo=4, q_hi=4, seed=1005,
+            notes="seq_len ~ U[4,32768] incl. the 4 new rows"),
         # Mixed chunked prefill + decode batch, causal (bottom-right aligned).
         "mixed_prefill": Workload(
             name="mixed_prefill", kind="prefill", batch=16, num_heads=32, num_kv_heads=8,
@@ -122,6 +128,9 @@ def draw(wl: Workload) -> Draw:
         qlen[: wl.forced_q1] = 1
         seq_lens = prior + qlen
         num_new = qlen
+    elif wl.kind == "spec_decode":
+        seq_lens = rng.integers(wl.len_lo, wl.len_hi, size=B, endpoint=True)
+        num_new = np.minimum(seq_lens, wl.q_hi)
     elif wl.layout == "arange":
         kv_len = rng.integers(wl.len_lo, wl.len_hi, size=B, endpoint=True)
         seq_lens = kv_len + 1
@@ -172,8 +181,10 @@ def values(wl: Workload, d: Draw, device="cpu", poison_null: bool = False) -> di
         out["cache_rope"] = _randn_bf16((d.num_blocks, bs, 1, wl.rope_dim), g, device)
         caches = ("cache_nope", "cache_rope")
     else:
-        qrows = T if wl.kind == "prefill" else B
-        out["q"] = _randn_bf16((qrows, H, dh), g, device)
+        if wl.kind == "spec_decode":
+            out["q"] = _randn_bf16((B, wl.q_hi, H, dh), g, device)
+        else:
+            out["q"] = _randn_bf16((T if wl.kind == "prefill" else B, H, dh), g, device)
         out["k_new"] = _randn_bf16((T, Hkv, dh), g, device)
         out["v_new"] = _randn_bf16((T, Hkv, dh), g, device)
         out["k_cache"] = _randn_bf16((d.num_blocks, bs, Hkv, dh), g, device)

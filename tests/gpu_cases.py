@@ -22,10 +22,12 @@ def tables(wl: synth.Workload, d: synth.Draw):
         table = api.build_block_table_arange(wl.batch, d.max_blocks_per_seq)
         ref_table = bp.block_table_arange(wl.batch, d.max_blocks_per_seq)
     else:
+        # Speculative decode keeps blocks live from the first new row's window start.
+        win = wl.window + wl.q_hi - 1 if wl.kind == "spec_decode" and wl.window > 0 else wl.window
         table = api.BlockPool(d.num_blocks, d.pool_order).build_block_table(
-            d.seq_lens, wl.block_size, wl.window, d.max_blocks_per_seq)
+            d.seq_lens, wl.block_size, win, d.max_blocks_per_seq)
         ref_table = bp.prepare_block_tables(bp.BlockPool(d.num_blocks, d.pool_order), d.seq_lens,
-                                            wl.block_size, wl.window, d.max_blocks_per_seq)
+                                            wl.block_size, win, d.max_blocks_per_seq)
     assert np.array_equal(table, ref_table)
     slots = api.build_slot_mapping(table, d.start_pos, d.num_new, wl.block_size)
     assert np.array_equal(slots, bp.slot_mapping(ref_table, d.start_pos, d.num_new, wl.block_size))

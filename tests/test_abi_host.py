@@ -137,3 +137,20 @@ def test_device_calls_reject_bad_arguments_before_launch():
     # v_cache without v.
     rc = lib.pkv_kv_cache_write(p, p, p, None, p, 1, 1, 128, 1, 8, 8, None, None)
     assert rc == -1
+
+
+def test_spec_decode_rejects_unsupported_shapes_before_launch():
+    lib = load()
+    args = lambda q_len, H, Hkv: (None, 1, None, None, None, None, None, 16, None, 2, q_len, H, Hkv,
+                                  128, 128, 10, 0.1, 0, None, 0, None, None)
+    # q_len outside 1..4.
+    assert lib.pkv_paged_attention_decode_spec(*args(5, 8, 2)) == -2
+    assert b"q_len" in lib.pkv_last_error()
+    assert lib.pkv_paged_attention_decode_spec(*args(0, 8, 2)) == -2
+    # More than 32 query rows per kv head: 3 tokens x 16 heads.
+    assert lib.pkv_paged_attention_decode_spec(*args(3, 32, 2)) == -2
+    assert b"32" in lib.pkv_last_error()
+    # The workspace grows with q_len: [B*Hkv + G] slots x q_len * n_rep rows.
+    one = lib.pkv_decode_spec_workspace_size(4, 1, 64, 8, 128)
+    four = lib.pkv_decode_spec_workspace_size(4, 4, 64, 8, 128)
+    assert one == lib.pkv_decode_workspace_size(4, 64, 8, 128) and four > 3 * one
