@@ -27,11 +27,12 @@
 //   warp 1      MMA issuer; S^T of tile j+1 is issued before O^T of tile j so
 //               that the softmax of tile j+1 overlaps the value product of j;
 //   warps 2..   softmax, four warps per 16 columns: thread = token lane of S^T.
-//               Block max per column by warp shuffles plus a shared-memory
+//               Block max per column by one warp redux plus a shared-memory
 //               exchange; exp2 in fp32 with q . k pre-scaled by scale * log2 e;
-//               P^T written as bf16 in the swizzled K-major layout of the second
-//               product's B operand; then thread = d lane of O^T, accumulating O
-//               in registers with the online-softmax rescale.
+//               P^T written as bf16 in the MN-major layout of the second
+//               product's B operand (a thread's 16 columns are two 16-byte
+//               stores); then thread = d lane of O^T, accumulating O in
+//               registers with the online-softmax rescale.
 // All waits are bounded (tc_ptx.cuh); a timeout sets PKV_DEV_TIMEOUT and every
 // role winds down.
 //
@@ -78,14 +79,14 @@ struct Shape {
   static constexpr int CW = NCH == 1 ? NR : 16;  // columns a softmax thread carries
   static constexpr int NTHREADS = 64 + 128 * NCH;
   static constexpr int QBUF = N * 256;           // N rows x 128 d, two 64-wide halves
-  static constexpr int PBUF = N * 256;           // N rows x 128 tokens, two halves
+  static constexpr int PBUF = N * 256;           // 128 tokens x N columns, MN-major
   // Shared-memory layout (offsets from a 1024-aligned base).
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NST * TILE;
   static constexpr int OFF_Q = OFF_V + NST * TILE;
   static constexpr int OFF_P = OFF_Q + 2 * QBUF;
   static constexpr int OFF_BAR = OFF_P + 2 * PBUF;
-  static constexpr int OFF_RED = OFF_BAR + B_COUNT * 8;   // float [2][4][N]
+  static constexpr int OFF_RED = (OFF_BAR + B_COUNT * 8 + 15) & ~15;  // float [2][4][N]
   static constexpr int OFF_LRED = OFF_RED + 2 * 4 * N * 4;  // float [4][N]
   static constexpr int OFF_MISC = OFF_LRED + 4 * N * 4;     // tmem addr, abort, total, snaps
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;   // + alignment slack
@@ -94,11 +95,6 @@ struct Shape {
   static_assert(NR <= 32, "at most 32 query rows per kv head");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
-
-// Byte offset of (row, k) inside a K-major 128-byte-swizzled half [rows x 64].
-__device__ __forceinline__ uint32_t sw128(int row, int k) {
-  return (uint32_t)(row * 128 + ((((k >> 3) ^ row) & 7) << 4) + (k & 7) * 2);
-}
 
 }  // namespace tcd
 
@@ -211,7 +207,7 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
   } else if (ntiles > 0 && warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t ID_S = idesc_bf16(128, N, 0, 0);  // K (K-major) x Q^T (K-major)
-    constexpr uint32_t ID_O = idesc_bf16(128, N, 1, 0);  // V^T (MN-major) x P^T (K-major)
+    constexpr uint32_t ID_O = idesc_bf16(128, N, 1, 1);  // V^T (MN-major) x P^T (MN-major)
     TileCursor c;
     cursor_seek(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap, t0, t1);
     int piece = -1;
@@ -244,11 +240,15 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
       if (!mbar_wait(bar(B_OEMPTY + ob), ((j >> 1) & 1) ^ 1)) return false;
       tc_fence_after();
       const uint64_t vd = smem_desc(sbase + OFF_V + st * TILE, HALF, 1024, kSwizzle128);
-      const uint64_t pd = smem_desc(sbase + OFF_P + ob * PBUF, 16, 1024, kSwizzle128);
+      // P^T, MN-major without swizzle: 8 columns x 8 tokens per 128-byte core matrix.
+      // In this layout the descriptor's stride field (SBO) steps along MN (column
+      // groups, 128 bytes apart) and the leading field (LBO) along K (8-token
+      // groups, N * 16 bytes apart), the reverse of the swizzled MN-major forms.
+      const uint64_t pd = smem_desc(sbase + OFF_P + ob * PBUF, N * 16, 128, 0);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ss(tmem + o_col(ob), desc_add(vd, kk * 2048),
-               desc_add(pd, (kk >> 2) * (PBUF / 2) + (kk & 3) * 32), ID_O, kk > 0);
+        mma_ss(tmem + o_col(ob), desc_add(vd, kk * 2048), desc_add(pd, kk * 2 * N * 16), ID_O,
+               kk > 0);
       mma_commit(bar(B_OFULL + ob));
       mma_commit(bar(B_PEMPTY + ob));
       mma_commit(bar(B_KVEMPTY + st));
@@ -376,12 +376,23 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
       const int ihi = any ? (qhi + 1) * NREP - qbase : 0;
       float x[CW];
 #pragma unroll
-      for (int i = 0; i < CW; ++i) {
+      for (int i = 0; i < CW; ++i)
         x[i] = (i >= ilo && i < ihi) ? __uint_as_float(sv[i]) * a.scale_log2 : -INFINITY;
-        float m = x[i];
+      {
+        float wm[CW];
 #pragma unroll
-        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) cred[(sb * 4 + quarter) * N + i] = m;
+        for (int i = 0; i < CW; ++i) wm[i] = warp_max(x[i]);
+        float* dst = cred + (sb * 4 + quarter) * N;
+        if (lane == 0) {
+          if constexpr (CW % 4 == 0) {
+#pragma unroll
+            for (int i = 0; i < CW; i += 4)
+              *reinterpret_cast<float4*>(dst + i) = make_float4(wm[i], wm[i + 1], wm[i + 2], wm[i + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < CW; ++i) dst[i] = wm[i];
+          }
+        }
       }
       // One thread snapshots the abort flag before the barrier so that every
       // thread of the block takes the same decision after it.
@@ -391,20 +402,51 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
         aborted = true;
         break;
       }
+      float mb[CW];
+      {
+        const float* src = cred + sb * 4 * N;
+        if constexpr (CW % 4 == 0) {
+#pragma unroll
+          for (int i = 0; i < CW; i += 4) {
+            float4 q0 = *reinterpret_cast<const float4*>(src + i);
+            const float4 q1 = *reinterpret_cast<const float4*>(src + N + i);
+            const float4 q2 = *reinterpret_cast<const float4*>(src + 2 * N + i);
+            const float4 q3 = *reinterpret_cast<const float4*>(src + 3 * N + i);
+            mb[i] = fmaxf(fmaxf(q0.x, q1.x), fmaxf(q2.x, q3.x));
+            mb[i + 1] = fmaxf(fmaxf(q0.y, q1.y), fmaxf(q2.y, q3.y));
+            mb[i + 2] = fmaxf(fmaxf(q0.z, q1.z), fmaxf(q2.z, q3.z));
+            mb[i + 3] = fmaxf(fmaxf(q0.w, q1.w), fmaxf(q2.w, q3.w));
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < CW; ++i)
+            mb[i] = fmaxf(fmaxf(src[i], src[N + i]), fmaxf(src[2 * N + i], src[3 * N + i]));
+        }
+      }
       float alpha[CW];
+      // P enters the value product as bf16 (pairs of columns packed with one
+      // round-to-nearest-even conversion); the normaliser sums the same rounded
+      // weights, so the output is an exact convex combination of V rows.
+      uint32_t pk[8];
 #pragma unroll
       for (int i = 0; i < CW; ++i) {
-        const float* rr = cred + sb * 4 * N + i;
-        const float mb = fmaxf(fmaxf(rr[0], rr[N]), fmaxf(rr[2 * N], rr[3 * N]));
-        const float mn = fmaxf(m_run[i], mb);
+        const float mn = fmaxf(m_run[i], mb[i]);
         alpha[i] = (mn == -INFINITY) ? 1.f : exp2f(m_run[i] - mn);
-        // P enters the value product as bf16; the normaliser sums the same rounded
-        // weights, so the output is an exact convex combination of V rows.
-        const float p = __bfloat162float(__float2bfloat16_rn(
-            (x[i] == -INFINITY) ? 0.f : exp2f(x[i] - mn)));
-        l_part[i] = l_part[i] * alpha[i] + p;
+        x[i] = (x[i] == -INFINITY) ? 0.f : exp2f(x[i] - mn);
         m_run[i] = mn;
-        x[i] = p;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float lo = 2 * j < CW ? x[2 * j < CW ? 2 * j : 0] : 0.f;
+        const float hi = 2 * j + 1 < CW ? x[2 * j + 1 < CW ? 2 * j + 1 : 0] : 0.f;
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
+        pk[j] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+#pragma unroll
+      for (int i = 0; i < CW; ++i) {
+        const float p = (i & 1) ? __uint_as_float(pk[i >> 1] & 0xffff0000u)
+                                : __uint_as_float(pk[i >> 1] << 16);
+        l_part[i] = l_part[i] * alpha[i] + p;
       }
       // A position no query row sees may hold any bytes (an unwritten tail slot):
       // once the tile has landed, zero its V row so that its weight 0 cannot meet a
@@ -420,16 +462,13 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
           *reinterpret_cast<uint4*>(vrow + HALF + q * 16) = make_uint4(0, 0, 0, 0);
         }
       }
-      // ---- P^T (bf16) into the B operand of the value product
+      // ---- P^T (bf16) into the B operand of the value product: token r's columns
+      // qbase..qbase+7 and qbase+8..qbase+15 are one 16-byte row each of two core
+      // matrices (8-token group r / 8, row r % 8).
       if (!mbar_wait(bar(B_PEMPTY + sb), ((j >> 1) & 1) ^ 1)) fail();
-      // Column qbase + i sits in 8-row atom (qbase + i) / 8 = qbase / 8 + i / 8.
-      uint8_t* ps = base + OFF_P + sb * PBUF + (r >> 6) * (PBUF / 2) + qbase * 128;
-      const int k = r & 63;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float p = i < CW ? x[i < CW ? i : 0] : 0.f;
-        *reinterpret_cast<__nv_bfloat16*>(ps + (i >> 3) * 1024 + sw128(i & 7, k)) = __float2bfloat16_rn(p);
-      }
+      uint8_t* ps = base + OFF_P + sb * PBUF + (r >> 3) * (N * 16) + (r & 7) * 16 + qbase * 16;
+      *reinterpret_cast<uint4*>(ps) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      *reinterpret_cast<uint4*>(ps + 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       fence_proxy_async_smem();
       mbar_arrive(bar(B_PFULL + sb));
       // ---- fold the previous tile's O^T into the registers

@@ -39,6 +39,14 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   return r;
 }
 
+// Maximum of v over the 32 lanes of a full warp (one redux instruction; NaN inputs
+// are ignored like fmaxf does).
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;\n" : "=f"(r) : "f"(v));
+  return r;
+}
+
 __device__ __forceinline__ void flag_status(int* dev_status, int bits) {
   if (dev_status) atomicOr(dev_status, bits);
 }
