@@ -160,6 +160,17 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
     tmem_alloc(sbase + OFF_MISC, TMEM_COLS);
     tmem_relinquish();
   }
+  if constexpr (NR < N) {
+    // Query rows NR..N-1 of both Q buffers are never loaded: zero them once, so the
+    // padding columns of S^T are 0 instead of whatever the memory held.
+    constexpr int PAD = (N - NR) * 128;  // bytes per 64-wide half
+    for (int o = tid * 16; o < 4 * PAD; o += L::NTHREADS * 16) {
+      const int half = o / PAD;  // buffer * 2 + d half
+      *reinterpret_cast<uint4*>(base + OFF_Q + half * (QBUF / 2) + NR * 128 + o % PAD) =
+          make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -271,10 +282,20 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
     float* cred = red + qbase;                    // [2][4][N] from this block's first column
     float* clred = lred + qbase;                  // [4][N]
     volatile uint32_t* snap = abort_snap + 2 * chunk;
+    // Columns of the block past the last query row (NR not a multiple of 16) see a
+    // zero query row: their scores are 0 or masked, and nothing reads them.
+    const int nreal = NR - qbase < CW ? NR - qbase : CW;
     TileCursor c;
     cursor_seek(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap, t0, t1);
-    // o_reg holds the output of the tiles folded so far, scaled to the running max
-    // of the newest tile whose scores are done: acc_o(j - 1) runs after tile j's
+    // Online softmax with a lazily moved reference: m_run (log2 units) changes only
+    // when a block's max exceeds it by more than kLazy, so most tiles skip the
+    // rescale; weights stay below 2^kLazy, well inside bf16 and fp32. The result is
+    // the same softmax (o = sum p v / sum p for any reference). m_run starts at a
+    // large finite negative value, so no -inf arithmetic is needed anywhere.
+    constexpr float kLazy = 8.f;
+    constexpr float kMinit = -1e30f;
+    // o_reg holds the output of the tiles folded so far, scaled to the reference of
+    // the newest tile whose scores are done: acc_o(j - 1) runs after tile j's
     // rescale factors are known and applies them together with O(j - 1).
     float m_run[CW], l_part[CW], o_reg[CW];
     // State of the piece being accumulated.
@@ -282,11 +303,8 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
     int64_t p_first = t0, p_segbase = 0;
     bool p_whole = false;
     bool aborted = false;
-    float ones[CW];
-#pragma unroll
-    for (int i = 0; i < CW; ++i) ones[i] = 1.f;
 
-    auto acc_o = [&](int jj, const float (&mult)[CW]) {
+    auto acc_o = [&](int jj, bool resc, const float (&alpha)[CW]) {
       const int ob = jj & 1;
       if (!mbar_wait(bar(B_OFULL + ob), (jj >> 1) & 1)) fail();
       __syncwarp();
@@ -296,8 +314,13 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bar(B_OEMPTY + ob));
+      if (resc) {
 #pragma unroll
-      for (int i = 0; i < CW; ++i) o_reg[i] = (o_reg[i] + __uint_as_float(v[i])) * mult[i];
+        for (int i = 0; i < CW; ++i) o_reg[i] = (o_reg[i] + __uint_as_float(v[i])) * alpha[i];
+      } else {
+#pragma unroll
+        for (int i = 0; i < CW; ++i) o_reg[i] += __uint_as_float(v[i]);
+      }
     };
     auto finalize = [&]() {
 #pragma unroll
@@ -332,16 +355,18 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
       named_bar_sync(bar_id, 128);  // lred reused by the next piece
     };
 
+    float alpha[CW];
+    bool resc = false;
     for (int j = 0; j < ntiles; ++j) {
       const bool first = (j == 0) || (c.j == 0);
       if (first) {
         if (j > 0) {
-          acc_o(j - 1, ones);
+          acc_o(j - 1, false, alpha);
           finalize();
         }
 #pragma unroll
         for (int i = 0; i < CW; ++i) {
-          m_run[i] = -INFINITY;
+          m_run[i] = kMinit;
           l_part[i] = 0.f;
           o_reg[i] = 0.f;
         }
@@ -351,7 +376,7 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
         p_segbase = c.seg_base;
         p_whole = (c.t == c.seg_base) && (c.t + c.n <= t1);
       }
-      // ---- scores of tile j
+      // ---- scores of tile j (raw q . k; the scale is applied inside exp2)
       const int sb = j & 1;
       if (!mbar_wait(bar(B_SFULL + sb), (j >> 1) & 1)) fail();
       __syncwarp();
@@ -375,9 +400,14 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
       const int ilo = any ? qlo * NREP - qbase : 0;
       const int ihi = any ? (qhi + 1) * NREP - qbase : 0;
       float x[CW];
+      if (__all_sync(0xffffffffu, any && ilo <= 0 && ihi >= nreal)) {
+        // Every real column of the block sees every token of the warp.
 #pragma unroll
-      for (int i = 0; i < CW; ++i)
-        x[i] = (i >= ilo && i < ihi) ? __uint_as_float(sv[i]) * a.scale_log2 : -INFINITY;
+        for (int i = 0; i < CW; ++i) x[i] = __uint_as_float(sv[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < CW; ++i) x[i] = (i >= ilo && i < ihi) ? __uint_as_float(sv[i]) : -INFINITY;
+      }
       {
         float wm[CW];
 #pragma unroll
@@ -402,13 +432,15 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
         aborted = true;
         break;
       }
+      // Block max per column (raw units; scale > 0), then the reference test. Every
+      // thread of the block reads the same maxima, so `resc` is uniform.
       float mb[CW];
       {
         const float* src = cred + sb * 4 * N;
         if constexpr (CW % 4 == 0) {
 #pragma unroll
           for (int i = 0; i < CW; i += 4) {
-            float4 q0 = *reinterpret_cast<const float4*>(src + i);
+            const float4 q0 = *reinterpret_cast<const float4*>(src + i);
             const float4 q1 = *reinterpret_cast<const float4*>(src + N + i);
             const float4 q2 = *reinterpret_cast<const float4*>(src + 2 * N + i);
             const float4 q3 = *reinterpret_cast<const float4*>(src + 3 * N + i);
@@ -423,30 +455,42 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
             mb[i] = fmaxf(fmaxf(src[i], src[N + i]), fmaxf(src[2 * N + i], src[3 * N + i]));
         }
       }
-      float alpha[CW];
+      const float cs = a.scale_log2;
+      resc = false;
+#pragma unroll
+      for (int i = 0; i < CW; ++i) resc |= mb[i] * cs > m_run[i] + kLazy;
+      if (resc) {
+#pragma unroll
+        for (int i = 0; i < CW; ++i) {
+          const float mn = fmaxf(m_run[i], mb[i] * cs);
+          alpha[i] = exp2f(m_run[i] - mn);
+          m_run[i] = mn;
+        }
+      }
       // P enters the value product as bf16 (pairs of columns packed with one
       // round-to-nearest-even conversion); the normaliser sums the same rounded
-      // weights, so the output is an exact convex combination of V rows.
+      // weights, so the output is an exact convex combination of V rows. A masked
+      // score is -inf and gives weight exp2(-inf) = 0.
+#pragma unroll
+      for (int i = 0; i < CW; ++i) x[i] = exp2f(fmaf(x[i], cs, -m_run[i]));
       uint32_t pk[8];
 #pragma unroll
-      for (int i = 0; i < CW; ++i) {
-        const float mn = fmaxf(m_run[i], mb[i]);
-        alpha[i] = (mn == -INFINITY) ? 1.f : exp2f(m_run[i] - mn);
-        x[i] = (x[i] == -INFINITY) ? 0.f : exp2f(x[i] - mn);
-        m_run[i] = mn;
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float lo = 2 * j < CW ? x[2 * j < CW ? 2 * j : 0] : 0.f;
-        const float hi = 2 * j + 1 < CW ? x[2 * j + 1 < CW ? 2 * j + 1 : 0] : 0.f;
+      for (int jj = 0; jj < 8; ++jj) {
+        const float lo = 2 * jj < CW ? x[2 * jj < CW ? 2 * jj : 0] : 0.f;
+        const float hi = 2 * jj + 1 < CW ? x[2 * jj + 1 < CW ? 2 * jj + 1 : 0] : 0.f;
         __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
-        pk[j] = *reinterpret_cast<uint32_t*>(&h2);
+        pk[jj] = *reinterpret_cast<uint32_t*>(&h2);
       }
+      if (resc) {
 #pragma unroll
-      for (int i = 0; i < CW; ++i) {
-        const float p = (i & 1) ? __uint_as_float(pk[i >> 1] & 0xffff0000u)
-                                : __uint_as_float(pk[i >> 1] << 16);
-        l_part[i] = l_part[i] * alpha[i] + p;
+        for (int i = 0; i < CW; ++i)
+          l_part[i] = l_part[i] * alpha[i] + ((i & 1) ? __uint_as_float(pk[i >> 1] & 0xffff0000u)
+                                                      : __uint_as_float(pk[i >> 1] << 16));
+      } else {
+#pragma unroll
+        for (int i = 0; i < CW; ++i)
+          l_part[i] += (i & 1) ? __uint_as_float(pk[i >> 1] & 0xffff0000u)
+                               : __uint_as_float(pk[i >> 1] << 16);
       }
       // A position no query row sees may hold any bytes (an unwritten tail slot):
       // once the tile has landed, zero its V row so that its weight 0 cannot meet a
@@ -471,12 +515,12 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
       *reinterpret_cast<uint4*>(ps + 128) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       fence_proxy_async_smem();
       mbar_arrive(bar(B_PFULL + sb));
-      // ---- fold the previous tile's O^T into the registers
-      if (!first) acc_o(j - 1, alpha);
+      // ---- fold the previous tile's O^T into the registers, with this tile's rescale
+      if (!first) acc_o(j - 1, resc, alpha);
       cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
     }
     if (!aborted) {
-      acc_o(ntiles - 1, ones);
+      acc_o(ntiles - 1, false, alpha);
       finalize();
     }
   }
