@@ -74,7 +74,7 @@ constexpr int CTILE = BS * D;          // 16 KB of codes: [128 tokens x 128 byte
 constexpr int HALF = 16384;            // f16 [128 rows x 64], one d half, swizzled
 constexpr int VOPB = 2 * HALF;         // one V' tile
 constexpr int QBUF = 4096;             // 16 rows x 128 d (16-bit), two 2 KB halves
-constexpr int PBUF = 4096;             // 16 heads x 128 tokens (16-bit), two halves
+constexpr int PBUF = 4096;             // 128 tokens x 16 heads (16-bit), MN-major
 constexpr int SCB = 1024;              // 128 K scales + 128 V scales
 
 constexpr int OFF_KST = 0;
@@ -120,10 +120,6 @@ __device__ __forceinline__ uint32_t k_col(int b) { return 64 + b * 64; }
 // Byte offset of 16-byte chunk `c` of row `row` in a 128-byte-swizzled [rows x 128 B] tile.
 __device__ __forceinline__ uint32_t sw_chunk(int row, int c) {
   return (uint32_t)(row * 128 + (((c ^ row) & 7) << 4));
-}
-// Byte offset of (row, k) inside a K-major 128-byte-swizzled 16-bit half [rows x 64].
-__device__ __forceinline__ uint32_t sw128(int row, int k) {
-  return (uint32_t)(row * 128 + ((((k >> 3) ^ row) & 7) << 4) + (k & 7) * 2);
 }
 
 #ifndef PKV_F8_CVT
@@ -279,7 +275,7 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
     // P' buffer of tile j-2, which the softmax has folded (resp. released) before it
     // arrives PFULL(j). So no separate "empty" barriers are needed.
     constexpr uint32_t ID_S = idesc_f16(128, N, 0, 0);  // K' (TMEM) x Q'^T (K-major smem)
-    constexpr uint32_t ID_O = idesc_f16(128, N, 1, 0);  // V'^T (MN-major) x P'^T (K-major)
+    constexpr uint32_t ID_O = idesc_f16(128, N, 1, 1);  // V'^T (MN-major) x P'^T (MN-major)
     TileCursor c;
     cursor_seek(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap, t0, t1);
     int piece = -1;
@@ -308,11 +304,14 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       if (!mbar_wait(bar(B_PFULL + ob), (j >> 1) & 1)) return false;
       tc_fence_after();
       const uint64_t vd = smem_desc(sbase + OFF_VOP + vb * VOPB, HALF, 1024, kSwizzle128);
-      const uint64_t pd = smem_desc(sbase + OFF_P + ob * PBUF, 16, 1024, kSwizzle128);
+      // P'^T, MN-major without swizzle: 8 heads x 8 tokens per 128-byte core matrix;
+      // the stride field (SBO) steps along MN (head groups, 128 bytes apart), the
+      // leading field (LBO) along K (8-token groups, 256 bytes apart).
+      const uint64_t pd = smem_desc(sbase + OFF_P + ob * PBUF, N * 16, 128, 0);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         mma_ss(tmem + o_col(ob), desc_add(vd, kk * 2048),
-               desc_add(pd, (kk >> 2) * (PBUF / 2) + (kk & 3) * 32), ID_O, kk > 0);
+               desc_add(pd, kk * 2 * N * 16), ID_O, kk > 0);
       mma_commit(bar(B_OFULL + ob));
       return true;
     };
@@ -414,7 +413,15 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
     float* qm = reinterpret_cast<float*>(base + OFF_QM);
     TileCursor c;
     cursor_seek(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap, t0, t1);
-    float m_run[HG], l_part[HG], o_reg[HG], alpha_prev[HG], qmul[HG];
+    // Online softmax with a lazily moved reference (log2 units): m_run changes only
+    // when a block max exceeds it by more than kLazy, so most tiles skip the
+    // rescale; it starts at a large finite negative value, so no -inf arithmetic is
+    // needed. o_reg is kept in the reference of the newest tile whose scores are
+    // done: acc_o(j - 1) runs after tile j's rescale factors are known.
+    constexpr float kLazy = 8.f;
+    constexpr float kMinit = -1e30f;
+    float m_run[HG], l_part[HG], o_reg[HG], alpha[HG], qmul[HG];
+    bool resc = false;
     float f_prev = 1.f;
     int pb = 0, pg = 0, piece = -1;
     int64_t p_first = t0, p_segbase = 0;
@@ -462,7 +469,7 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       mbar_arrive(bar(B_QOPF + qb));
       return ok;
     };
-    auto acc_o = [&](int jj) {
+    auto acc_o = [&](int jj, bool rs) {
       const int ob = jj & 1;
       if (!mbar_wait(bar(B_OFULL + ob), (jj >> 1) & 1)) fail();
       __syncwarp();
@@ -471,9 +478,15 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       tmem_ld16(tmem + lane_off + o_col(ob), v);
       tmem_wait_ld();
       tc_fence_before();  // ordered before the next PFULL arrive, which frees O^T(jj)
+      if (rs) {
 #pragma unroll
-      for (int h = 0; h < HG; ++h)
-        o_reg[h] = o_reg[h] * alpha_prev[h] + f_prev * __uint_as_float(grp ? v[(HG + h) & 15] : v[h]);
+        for (int h = 0; h < HG; ++h)
+          o_reg[h] = (o_reg[h] + f_prev * __uint_as_float(grp ? v[(HG + h) & 15] : v[h])) * alpha[h];
+      } else {
+#pragma unroll
+        for (int h = 0; h < HG; ++h)
+          o_reg[h] += f_prev * __uint_as_float(grp ? v[(HG + h) & 15] : v[h]);
+      }
     };
     auto finalize = [&]() {
 #pragma unroll
@@ -518,15 +531,14 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
         ++piece;
         if (!convert_q()) fail();
         if (j > 0) {
-          acc_o(j - 1);
+          acc_o(j - 1, false);
           finalize();
         }
 #pragma unroll
         for (int h = 0; h < HG; ++h) {
-          m_run[h] = -INFINITY;
+          m_run[h] = kMinit;
           l_part[h] = 0.f;
           o_reg[h] = 0.f;
-          alpha_prev[h] = 1.f;
         }
         f_prev = 1.f;
         pb = c.b;
@@ -560,15 +572,11 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
         // Column h0 + h, chosen between two compile-time indices (no local memory).
         const uint32_t sx = grp ? svr[(HG + h) & 15] : svr[h];
         x[h] = (valid && has_heads) ? __uint_as_float(sx) * (smul * qmul[h]) : -INFINITY;
-        float m = x[h];
-#pragma unroll
-        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float m = warp_max(x[h]);
         if (lane == 0 && has_heads) red[(sb * 4 + quarter) * 16 + h0 + h] = m;
       }
       if (grp == 0) {
-        float fv = valid ? sv : 0.f;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) fv = fmaxf(fv, __shfl_xor_sync(0xffffffffu, fv, o));
+        const float fv = warp_max(valid ? sv : 0.f);
         if (lane == 0) fred[sb * 4 + quarter] = fv;
       }
       if (ts == 0) abort_snap[sb] = *abort_flag;
@@ -580,41 +588,63 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       float f = fmaxf(fmaxf(fred[sb * 4], fred[sb * 4 + 1]), fmaxf(fred[sb * 4 + 2], fred[sb * 4 + 3]));
       f = f > 0.f ? f : 1.f;
       const float vmul = valid ? __fdividef(sv, f) : 0.f;
-      float alpha[HG];
+      // Block max per head and the reference test; both groups read the same
+      // maxima for their own heads, so `resc` is uniform within a group.
+      float mb[HG];
+      resc = false;
 #pragma unroll
       for (int h = 0; h < HG; ++h) {
         const float* rr = red + sb * 64 + h0 + h;
-        const float mb = has_heads ? fmaxf(fmaxf(rr[0], rr[16]), fmaxf(rr[32], rr[48])) : -INFINITY;
-        const float mn = fmaxf(m_run[h], mb);
-        alpha[h] = (mn == -INFINITY) ? 1.f : exp2f(m_run[h] - mn);
-        const float p = (x[h] == -INFINITY) ? 0.f : exp2f(x[h] - mn);
-        l_part[h] = l_part[h] * alpha[h] + p;
-        m_run[h] = mn;
+        mb[h] = has_heads ? fmaxf(fmaxf(rr[0], rr[16]), fmaxf(rr[32], rr[48])) : -INFINITY;
+        resc |= mb[h] > m_run[h] + kLazy;
+      }
+      if (resc) {
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+          const float mn = fmaxf(m_run[h], mb[h]);
+          alpha[h] = exp2f(m_run[h] - mn);
+          m_run[h] = mn;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < HG; ++h) {
+        const float p = exp2f(x[h] - m_run[h]);  // a masked score is -inf: weight 0
+        l_part[h] = resc ? l_part[h] * alpha[h] + p : l_part[h] + p;
         x[h] = p * vmul;  // P' = p * v_scale / f
       }
       // ---- P'^T (f16) of the group's heads into the B operand of the value product
-      // (O(j-2), its last reader, is complete: acc_o(j-2) waited for it). Columns of
-      // heads >= NREP only feed O^T columns that are never read.
-      uint8_t* ps = base + OFF_P + sb * PBUF + (r >> 6) * (PBUF / 2);
-      const int k = r & 63;
+      // (O(j-2), its last reader, is complete: acc_o(j-2) waited for it): heads
+      // h0..h0+HG-1 of token r are HG contiguous halves of the 16-byte row r % 8 of
+      // core matrix (r / 8, h0 / 8). Columns of heads >= NREP are never written and
+      // only feed O^T columns that are never read.
+      if (has_heads) {
+        uint8_t* ps = base + OFF_P + sb * PBUF + (r >> 3) * (N * 16) + (r & 7) * 16 +
+                      (h0 >> 3) * 128 + (h0 & 7) * 2;
+        if constexpr (HG == 1) {
+          *reinterpret_cast<__half*>(ps) = __float2half_rn(x[0]);
+        } else {
+          uint32_t pk[HG / 2];
 #pragma unroll
-      for (int hh = 0; hh < HG; ++hh) {
-        const int h = h0 + hh;
-        if (h < NREP) *reinterpret_cast<__half*>(ps + (h >> 3) * 1024 + sw128(h & 7, k)) = __float2half_rn(x[hh]);
+          for (int i = 0; i < HG / 2; ++i) {
+            const __half2 h2 = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+            pk[i] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          if constexpr (HG == 2) *reinterpret_cast<uint32_t*>(ps) = pk[0];
+          if constexpr (HG == 4) *reinterpret_cast<uint2*>(ps) = make_uint2(pk[0], pk[1]);
+          if constexpr (HG == 8) *reinterpret_cast<uint4*>(ps) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(B_PFULL + sb));
       // Tile j's values are all computed; advance and start the next block-id load.
       cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
       if (j + 1 < ntiles) blk_next = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.jlo + c.j);
-      // ---- fold the previous tile's O^T into the registers
-      if (!first) acc_o(j - 1);
-#pragma unroll
-      for (int h = 0; h < HG; ++h) alpha_prev[h] = alpha[h];
+      // ---- fold the previous tile's O^T into the registers, with this tile's rescale
+      if (!first) acc_o(j - 1, resc);
       f_prev = f * kWidenScale;  // O^T of this tile carries V' = value * code factor / f
     }
     if (!aborted) {
-      acc_o(ntiles - 1);
+      acc_o(ntiles - 1, false);
       finalize();
     }
   }
