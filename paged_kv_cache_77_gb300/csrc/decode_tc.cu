@@ -45,6 +45,19 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const uint64_t* d
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
+// bf16 map with a 64-byte swizzle (boxes whose rows are 64 bytes, 32 elements).
+bool make_tmap_bf16_sw64(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
+                         const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr),
+                  (const cuuint64_t*)dims, (const cuuint64_t*)strides, (const cuuint32_t*)box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
   switch (a.n_rep) {
     case 1: return launch_tc_n<1, 1>(a, stream);

@@ -1,4 +1,4 @@
-// Absorbed MLA paged decode on the tcgen05 tensor cores.
+// Absorbed MLA paged decode on the tcgen05 tensor cores, one CTA pair per tile range.
 //
 // One latent KV head serves all query heads. key = value = cache_nope (kv_lora_rank
 // 512) and a separate 64-wide rope key adds to the scores ("KVCache 优化技能" 模式三;
@@ -6,31 +6,39 @@
 //
 //   s_j = scale * (q_nope . nope_j + q_rope . rope_j),   o = softmax(s) . nope
 //
-// Tiles are 64 tokens of one sequence, streamed by TMA through a 2-deep ring (72 KB
-// a stage). Per tile, with the 128 query heads on the M = 128 side of the MMA:
+// The two CTAs of a cluster walk the same tiles of 64 tokens. CTA `half` owns the
+// latent columns [256 half, 256 half + 256) and rope columns [32 half, 32 half + 32):
 //
-//   S [128 heads x 64] = [Q_nope | Q_rope] [128 x 576] . [nope | rope]_tile^T
-//   O_half [128 x 256] += P [128 x 64] . nope_tile[:, half]      (P read from TMEM)
+//   S_half [128 heads x 64] = Q[:, own columns] . tile[:, own columns]^T   (K = 288)
+//   S = S_0 + S_1          (partial scores swapped through distributed shared memory)
+//   O_half [128 x 256]    += P [128 x 64] . nope_tile[:, own latent columns]
 //
-// 64-token tiles halve the MMA issues per token of 32-token tiles (an N=64 MMA costs
-// about what an N=32 one does) and the handoffs per token; shared memory and tensor
-// memory are then full, so S has a single buffer (the next score product waits only
-// until the softmax has read S into registers).
+// The score product is split along its reduction axis, so no product is computed
+// twice, and each CTA streams only its 36 KB of a tile (four 64-column latent chunks
+// in a 128-byte swizzle, its 32 rope columns in a 64-byte swizzle) through a 4-deep
+// TMA ring; the pair reads every byte of the cache once.
 //
-// O for all 512 latent columns (128 x 512 fp32) would fill the whole 512-column
-// tensor memory, so the 512 columns are split across two CTAs ("halves"); each CTA
-// computes the full S of its tiles (1.5x the minimum tensor work) and half of O.
-// CTA i and CTA i + G/2 walk the same tile range, so the second read of a tile
-// usually hits L2. To leave shared memory for the ring, the A operand Q is split:
-// columns 0..319 stay in shared memory, columns 320..511 and the rope part are
-// written by the softmax warps into tensor memory and read from there by the MMA.
+// The partial score tile crosses to the peer as fp32 st.async stores that count their
+// bytes on the peer's mbarrier (the receiver opens each phase with expect_tx, so the
+// sender needs no fence). Both CTAs add the same two numbers, hold bit-identical S,
+// take identical softmax decisions and write identical P. The exchange is double-
+// buffered and software-pipelined: tile j+1's partial is sent while tile j's softmax
+// runs.
 //
-// Softmax: thread = head row of S (all 64 scores of a tile in one thread, no
-// shuffles); exp2 in fp32 with the scale folded into log2 units; P rounded to bf16
-// and stored into TMEM as the A operand of the value product; the normaliser sums
-// the rounded weights. The running max is only raised when a tile's max exceeds it
-// by more than 8 (log2 units): P stays below 2^8 and O in TMEM is rescaled only then
-// (warp-uniform), which is rare after the first tile.
+// Warps: 0 TMA producer, 1 MMA issuer (polls and issues whichever product is ready),
+// 2..9 softmax, two per TMEM lane quarter, each with 32 of a tile's 64 score columns
+// and 128 of the 256 O columns; the two warps of a quarter agree on the row max
+// through shared memory.
+//
+// Tensor memory (512 columns): S 0..63, P 64..127 (two buffers of 64 bf16 packed in
+// pairs, the A operand of the value product), this CTA's 256 Q latent columns
+// 128..255 (the A operand of 16 score K-steps), O half 256..511. The rope part of Q
+// stays in shared memory (two K-steps from shared memory).
+//
+// Softmax: thread = head row; exp2 in fp32 with the scale folded into log2 units; P
+// rounded to bf16; the normaliser sums the rounded weights. The reference max is
+// raised only when a tile's max exceeds it by more than 8 (log2 units), so P stays
+// below 2^8 and O in TMEM is rescaled only then.
 //
 // Roofline: HBM and tensor both matter. Algorithmic bytes per token = 1152 (nope +
 // rope row); algorithmic flops per token = 128 * (2*576 + 2*512).
@@ -44,6 +52,8 @@ namespace pkv {
 
 bool make_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
                     const uint64_t* strides, const uint32_t* box);
+bool make_tmap_bf16_sw64(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
+                         const uint64_t* strides, const uint32_t* box);
 
 namespace mla {
 
@@ -52,19 +62,21 @@ constexpr int DR = 64;           // rope width
 constexpr int TT = 64;           // tokens per tile (MMA N of the score product)
 constexpr int BS = 128;          // block size
 constexpr int M = 128;           // query heads per MMA (rows)
-constexpr int DH = 256;          // latent columns per CTA half
-constexpr int NCH = 9;           // 64-wide chunks of [nope | rope]
-constexpr int QSM = 5;           // Q chunks 0-4 (nope 0..319) live in shared memory,
-                                 // chunks 5-8 (nope 320..511 and rope) in tensor memory
-constexpr int QCH = M * 128;     // one Q chunk: 128 rows x 128 bytes
-constexpr int KCH = TT * 128;    // one K chunk: TT rows x 128 bytes
-constexpr int NST = 2;           // K stages (72 KB each)
-constexpr int NSB = 1;           // S buffers in tensor memory
-constexpr int NTHREADS = 192;
+constexpr int DH = 256;          // latent columns per CTA
+constexpr int NLC = 4;           // 64-wide latent chunks per CTA
+constexpr int DRH = DR / 2;      // rope columns per CTA
+constexpr int QRB = M * DRH * 2; // this CTA's rope part of Q: 128 rows x 64 bytes
+constexpr int KCH = TT * 128;    // one latent chunk of a tile: TT rows x 128 bytes
+constexpr int KRB = TT * DRH * 2;  // this CTA's rope part of a tile: TT rows x 64 bytes
+constexpr int STAGE = NLC * KCH + KRB;  // 4 latent chunks + 32 rope columns (36 KB)
+constexpr int NST = 4;           // K stages
+constexpr int XBUF = TT * M * 4; // one partial score tile, fp32 (32 KB)
+constexpr int NTHREADS = 320;  // TMA warp, MMA warp, 8 softmax warps
 
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + QSM * QCH;           // 81920
-constexpr int OFF_BAR = OFF_K + NST * NCH * KCH;   // 229376
+constexpr int OFF_K = 0;
+constexpr int OFF_QR = OFF_K + NST * STAGE;        // rope part of Q (64-byte swizzle)
+constexpr int OFF_X = OFF_QR + QRB;                // two partial-score buffers
+constexpr int OFF_BAR = OFF_X + 2 * XBUF;
 enum {
   B_KFULL = 0,
   B_KEMPTY = B_KFULL + NST,
@@ -72,25 +84,29 @@ enum {
   B_QEMPTY = B_QFULL + 1,
   B_QTFULL = B_QEMPTY + 1,
   B_SFULL = B_QTFULL + 1,
-  B_SEMPTY = B_SFULL + NSB,
-  B_PFULL = B_SEMPTY + NSB,
+  B_SEMPTY = B_SFULL + 1,
+  B_PFULL = B_SEMPTY + 1,
   B_PEMPTY = B_PFULL + 2,
   B_ODONE = B_PEMPTY + 2,
   B_OFREE = B_ODONE + 2,
-  B_COUNT = B_OFREE + 1
+  B_XFULL = B_OFREE + 1,   // peer's partial scores arrived (transaction bytes)
+  B_COUNT = B_XFULL + 2
 };
-constexpr int OFF_MISC = OFF_BAR + B_COUNT * 8;
+// Exchange between the two softmax warps of a lane quarter: float [2][256] sums, then
+// float2 [2][256] (row max, abort flag).
+constexpr int OFF_RED = OFF_BAR + B_COUNT * 8;
+constexpr int OFF_MISC = OFF_RED + 2 * 256 * 4 + 2 * 256 * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
+static_assert(STAGE % 1024 == 0 && OFF_QR % 1024 == 0 && OFF_X % 1024 == 0, "alignment");
+static_assert((NLC * KCH) % 512 == 0, "a 64-byte-swizzled box starts on a 512-byte boundary");
 
-// TMEM columns: S 0..63 (one buffer, TT fp32 columns), P 64..127 (two buffers of TT
-// bf16 packed in pairs), Q chunks 5-8 128..255 (32 columns each), O half 256..511.
 constexpr uint32_t TMEM_COLS = 512;
-__device__ __forceinline__ uint32_t s_col(int b) { return b * TT; }
-__device__ __forceinline__ uint32_t p_col(int b) { return NSB * TT + b * (TT / 2); }
-constexpr uint32_t Q_COL = NSB * TT + TT;
+constexpr uint32_t S_COL = 0;
+__device__ __forceinline__ uint32_t p_col(int b) { return TT + b * (TT / 2); }
+constexpr uint32_t Q_COL = 2 * TT;
 constexpr uint32_t O_COL = 256;
-static_assert(Q_COL + (NCH - QSM) * 32 <= O_COL, "tensor memory");
+static_assert(Q_COL + NLC * 32 <= O_COL, "tensor memory");
 
 }  // namespace mla
 
@@ -104,14 +120,16 @@ struct MlaArgs {
   float* lse;           // [B, H] or null
   float* ws_o;          // [(B + Gh) * 2 * 128 * 256]
   float* ws_lse;        // [(B + Gh) * 2 * 128]
+  long long* ws_bnd;    // [Gh][4]: first sequence of pair i's range (-1: empty range),
+                        // that sequence's first tile, its tile count, total tiles
   int* dev_status;
   int64_t num_blocks;
   int B, H, max_blocks, out_f32;
-  int g_half;           // CTAs per latent half
+  int g_half;           // CTA pairs (clusters)
   float scale_log2;
 };
 
-__global__ void __launch_bounds__(mla::NTHREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
     mla_tc_kernel(const __grid_constant__ MlaArgs a, const __grid_constant__ CUtensorMap tm_qn,
                   const __grid_constant__ CUtensorMap tm_qr, const __grid_constant__ CUtensorMap tm_cn,
                   const __grid_constant__ CUtensorMap tm_cr) {
@@ -126,8 +144,8 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
   long long* total_s = reinterpret_cast<long long*>(misc + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int half = blockIdx.x / a.g_half;
-  const int ci = blockIdx.x % a.g_half;
+  const int half = (int)cluster_ctarank();
+  const int ci = blockIdx.x >> 1;  // pair index
   const int cap = a.max_blocks * BS;
 
   if (tid == 0) {
@@ -137,17 +155,16 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
     }
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QEMPTY), 1);
-    mbar_init(bar(B_QTFULL), 128);
-    for (int i = 0; i < NSB; ++i) {
-      mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_SEMPTY + i), 128);
-    }
+    mbar_init(bar(B_QTFULL), 256);
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_SEMPTY), 256);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_PFULL + i), 128);
+      mbar_init(bar(B_PFULL + i), 256);
       mbar_init(bar(B_PEMPTY + i), 1);
       mbar_init(bar(B_ODONE + i), 1);
+      mbar_init(bar(B_XFULL + i), 1);
     }
-    mbar_init(bar(B_OFREE), 128);
+    mbar_init(bar(B_OFREE), 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -168,25 +185,34 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  // Both CTAs' barriers are initialised before either arrives on the other's.
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = misc[0];
   const int64_t T = *total_s, G = a.g_half;
   const int64_t t0 = cta_tile_start(ci, T, G), t1 = cta_tile_start(ci + 1, T, G);
-  const int ntiles = (half < 2) ? (int)(t1 - t0) : 0;
+  const int ntiles = (int)(t1 - t0);
   auto fail = [&]() {
     *abort_flag = 1;
     flag_status(a.dev_status, PKV_DEV_TIMEOUT);
   };
+  if (ntiles == 0 && half == 0 && tid == 0) a.ws_bnd[4 * ci] = -1;
 
   if (ntiles > 0 && warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     TileCursor c;
     cursor_seek(c, a.seq_lens, a.B, 1, TT, 0, cap, t0, t1);
+    if (half == 0) {
+      long long* e = a.ws_bnd + 4 * ci;
+      e[0] = c.b;
+      e[1] = c.seg_base;
+      e[2] = c.n;
+      e[3] = T;
+    }
     int piece = 0;
     const int rows_oob = (int)(a.num_blocks * BS);
-    // L2 prefetch runs kPrefetch tiles ahead of the loads (second cursor `pc`): a
-    // stage frees only when O(j-2) completes, and the load then finds its tile in L2.
+    // L2 prefetch runs kPrefetch tiles ahead of the loads (second cursor `pc`), so
+    // that a load issued when its stage frees finds the tile in L2.
     constexpr int kPrefetch = 2;
     TileCursor pc = c;
     auto prefetch_next = [&](int jp) {
@@ -195,8 +221,8 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
       const int pblk = __ldg(a.block_table + (int64_t)pc.b * a.max_blocks + ptok / BS);
       if (pblk >= 0 && (int64_t)pblk < a.num_blocks) {
         const int prow = pblk * BS + (ptok % BS);
-        for (int ch = 0; ch < 8; ++ch) tma_prefetch_2d(&tm_cn, ch * 64, prow);
-        tma_prefetch_2d(&tm_cr, 0, prow);
+        for (int ch = 0; ch < NLC; ++ch) tma_prefetch_2d(&tm_cn, (NLC * half + ch) * 64, prow);
+        tma_prefetch_2d(&tm_cr, DRH * half, prow);
       }
       cursor_next(pc, a.seq_lens, a.B, 1, TT, 0, cap);
     };
@@ -204,11 +230,9 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
     for (int j = 0; j < ntiles && !*abort_flag; ++j) {
       prefetch_next(j + kPrefetch);
       if (j == 0 || c.j == 0) {
-        if (!mbar_wait(bar(B_QEMPTY), (piece & 1) ^ 1)) { fail(); break; }
-        mbar_expect_tx(bar(B_QFULL), QSM * QCH);
-        const int qrow = c.b * a.H;
-        for (int ch = 0; ch < QSM; ++ch)
-          tma_load_2d(sbase + OFF_Q + ch * QCH, &tm_qn, bar(B_QFULL), ch * 64, qrow);
+        if (!mbar_wait_sleepy(bar(B_QEMPTY), (piece & 1) ^ 1)) { fail(); break; }
+        mbar_expect_tx(bar(B_QFULL), QRB);
+        tma_load_2d(sbase + OFF_QR, &tm_qr, bar(B_QFULL), DRH * half, c.b * a.H);
         ++piece;
       }
       const int st = j % NST;
@@ -216,12 +240,13 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
       const int blk = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + tok0 / BS);
       const bool ok = blk >= 0 && (int64_t)blk < a.num_blocks;
       const int row = ok ? blk * BS + (tok0 % BS) : rows_oob;
-      if (!mbar_wait(bar(B_KEMPTY + st), ((j / NST) & 1) ^ 1)) { fail(); break; }
+      if (!mbar_wait_sleepy(bar(B_KEMPTY + st), ((j / NST) & 1) ^ 1)) { fail(); break; }
       if (!ok) flag_status(a.dev_status, PKV_DEV_BAD_BLOCK);
-      const uint32_t ks = sbase + OFF_K + st * NCH * KCH;
-      mbar_expect_tx(bar(B_KFULL + st), NCH * KCH);
-      for (int ch = 0; ch < 8; ++ch) tma_load_2d(ks + ch * KCH, &tm_cn, bar(B_KFULL + st), ch * 64, row);
-      tma_load_2d(ks + 8 * KCH, &tm_cr, bar(B_KFULL + st), 0, row);
+      const uint32_t ks = sbase + OFF_K + st * STAGE;
+      mbar_expect_tx(bar(B_KFULL + st), STAGE);
+      for (int ch = 0; ch < NLC; ++ch)
+        tma_load_2d(ks + ch * KCH, &tm_cn, bar(B_KFULL + st), (NLC * half + ch) * 64, row);
+      tma_load_2d(ks + NLC * KCH, &tm_cr, bar(B_KFULL + st), DRH * half, row);
       cursor_next(c, a.seq_lens, a.B, 1, TT, 0, cap);
     }
   } else if (ntiles > 0 && warp == 1 && lane == 0) {
@@ -231,69 +256,62 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
     TileCursor c;
     cursor_seek(c, a.seq_lens, a.B, 1, TT, 0, cap, t0, t1);
     int piece_s = -1;
-    // Dynamic issue order: the thread polls (non-blocking) and issues whichever
-    // product is ready. With two K stages the load of tile j+2 can only start when
-    // O(j) has completed, so O(j) must not wait behind a score product that is itself
-    // waiting for its tile; a fixed order exposed the whole TMA latency every tile.
-    // Phases cannot alias: S(js) needs the softmax to have read S(js-1), and its K
-    // stage is refilled only after O(js-2), so js <= jo + 2 while O(jo) is pending.
-    bool first_of[4] = {false, false, false, false};  // by tile index mod 4
+    // Dynamic issue order: poll (non-blocking) and issue whichever product is ready,
+    // so that O(j) never waits behind a score product that waits for its tile.
+    // Phases cannot alias: S(js) needs the softmax to have read S(js-1), and the K
+    // stage of js is refilled only after O(js-NST).
+    uint32_t first_bits = 0;  // bit (j mod 4): tile j opens a piece
     int piece_o = -1;
     auto ready_s = [&](int j) -> bool {
       const bool first = (j == 0) || (c.j == 0);
-      const int st = j % NST, sb = j % NSB;
+      const int st = j % NST;
       if (first && (!mbar_try(bar(B_QFULL), (piece_s + 1) & 1) ||
                     !mbar_try(bar(B_QTFULL), (piece_s + 1) & 1)))
         return false;
-      return mbar_try(bar(B_KFULL + st), (j / NST) & 1) &&
-             mbar_try(bar(B_SEMPTY + sb), ((j / NSB) & 1) ^ 1);
+      return mbar_try(bar(B_KFULL + st), (j / NST) & 1) && mbar_try(bar(B_SEMPTY), (j & 1) ^ 1);
     };
     auto issue_s = [&](int j) {
       const bool first = (j == 0) || (c.j == 0);
       const bool last = (j + 1 == ntiles) || (c.j + 1 == c.n);
-      const int st = j % NST, sb = j % NSB;
-      first_of[j & 3] = first;
+      const int st = j % NST;
+      first_bits = (first_bits & ~(1u << (j & 3))) | ((uint32_t)first << (j & 3));
       if (first) ++piece_s;
       tc_fence_after();
-      // Base descriptors once per tile; each K step only adds a constant offset.
-      const uint64_t kd = smem_desc(sbase + OFF_K + st * NCH * KCH, 16, 1024, kSwizzle128);
-      const uint64_t qd = smem_desc(sbase + OFF_Q, 16, 1024, kSwizzle128);
-      const uint32_t sd = tmem + s_col(sb), qt = tmem + Q_COL;
+      const uint64_t kd = smem_desc(sbase + OFF_K + st * STAGE, 16, 1024, kSwizzle128);
+      // Rope parts: rows of 64 bytes, 64-byte swizzle, 8-row groups 512 bytes apart.
+      const uint64_t qd = smem_desc(sbase + OFF_QR, 16, 512, kSwizzle64);
+      const uint64_t krd = smem_desc(sbase + OFF_K + st * STAGE + NLC * KCH, 16, 512, kSwizzle64);
+      const uint32_t sd = tmem + S_COL, qt = tmem + Q_COL;
 #pragma unroll
-      for (int ch = 0; ch < QSM; ++ch) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss(sd, desc_add(qd, ch * QCH + kk * 32), desc_add(kd, ch * KCH + kk * 32), ID_S,
-                 (ch | kk) != 0);
-      }
-#pragma unroll
-      for (int ch = QSM; ch < NCH; ++ch) {
+      for (int ch = 0; ch < NLC; ++ch) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ts(sd, qt + (ch - QSM) * 32 + kk * 8, desc_add(kd, ch * KCH + kk * 32), ID_S, 1);
+          mma_ts(sd, qt + ch * 32 + kk * 8, desc_add(kd, ch * KCH + kk * 32), ID_S, (ch | kk) != 0);
       }
-      mma_commit(bar(B_SFULL + sb));
+      // This CTA's 32 rope columns: two K-steps of 16 (32 bytes) within the 64-byte rows.
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) mma_ss(sd, desc_add(qd, kk * 32), desc_add(krd, kk * 32), ID_S, 1);
+      mma_commit(bar(B_SFULL));
       if (last) mma_commit(bar(B_QEMPTY));
       cursor_next(c, a.seq_lens, a.B, 1, TT, 0, cap);
     };
     auto ready_o = [&](int j) -> bool {
-      const int sb = j & 1;  // P buffer
-      if (!mbar_try(bar(B_PFULL + sb), (j >> 1) & 1)) return false;
-      return !first_of[j & 3] || mbar_try(bar(B_OFREE), ((piece_o + 1) & 1) ^ 1);
+      const int pb = j & 1;
+      if (!mbar_try(bar(B_PFULL + pb), (j >> 1) & 1)) return false;
+      return !((first_bits >> (j & 3)) & 1u) || mbar_try(bar(B_OFREE), ((piece_o + 1) & 1) ^ 1);
     };
     auto issue_o = [&](int j) {
-      const int st = j % NST, sb = j & 1;
-      const bool first = first_of[j & 3];
+      const int st = j % NST, pb = j & 1;
+      const bool first = (first_bits >> (j & 3)) & 1u;
       if (first) ++piece_o;
       tc_fence_after();
-      const uint64_t vd = smem_desc(sbase + OFF_K + st * NCH * KCH + (4 * half) * KCH, KCH, 1024,
-                                    kSwizzle128);
+      const uint64_t vd = smem_desc(sbase + OFF_K + st * STAGE, KCH, 1024, kSwizzle128);
 #pragma unroll
       for (int kk = 0; kk < TT / 16; ++kk)
-        mma_ts(tmem + O_COL, tmem + p_col(sb) + kk * 8, desc_add(vd, kk * 2048), ID_O,
+        mma_ts(tmem + O_COL, tmem + p_col(pb) + kk * 8, desc_add(vd, kk * 2048), ID_O,
                !(first && kk == 0));
-      mma_commit(bar(B_ODONE + sb));
-      mma_commit(bar(B_PEMPTY + sb));
+      mma_commit(bar(B_ODONE + pb));
+      mma_commit(bar(B_PEMPTY + pb));
       mma_commit(bar(B_KEMPTY + st));
     };
     int js = 0, jo = 0;
@@ -312,46 +330,49 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
       } else if (*abort_flag || clock64() - idle_since > kWaitCycles) {
         fail();
         break;
+      } else {
+        __nanosleep(32);  // leave the sub-partition's issue slots to the softmax warps
       }
     }
   } else if (ntiles > 0 && warp >= 2) {
     // ------------------------------------------------------------ softmax / epilogue
+    // Eight warps, two per TMEM lane quarter: warp w takes head row r of its quarter
+    // and score columns [32 hc, 32 hc + 32) of each tile, O columns [128 hc, +128).
     const int quarter = warp & 3;
+    const int hc = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;  // head row
+    const int st_id = hc * 128 + r;     // 0..255
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t peer = (uint32_t)(half ^ 1);
+    // Partial-score buffers: [TT/4 token groups][128 heads][4 tokens] fp32, so a warp's
+    // 16-byte accesses cover 512 contiguous bytes. This thread's groups are 8 hc + g.
+    const uint32_t x_peer = mapa_shared(sbase + OFF_X + (uint32_t)(8 * hc * M + r) * 16, peer);
+    const uint32_t xbar_peer = mapa_shared(bar(B_XFULL), peer);
+    float* red = reinterpret_cast<float*>(base + OFF_RED);
+    const int qbar = 1 + quarter;                            // named barrier of the two warps
     TileCursor c;
     cursor_seek(c, a.seq_lens, a.B, 1, TT, 0, cap, t0, t1);
-    float m_ref = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY, l = 0.f;  // l: normaliser over this warp's columns
     bool aborted = false;
     int piece_sm = 0;
-    // Q columns 256..511 and the rope part of head row r into tensor memory (the A
-    // operand of chunks 4-8 of the score product), once the previous piece's score
-    // products no longer read them.
+    // This CTA's 256 latent columns of Q for head row r into tensor memory (the A
+    // operand of the score product), once the previous piece's score products no
+    // longer read them. Column half hc writes chunks 2 hc and 2 hc + 1.
     auto load_q_tmem = [&](int b) {
       if (!mbar_wait(bar(B_QEMPTY), (piece_sm & 1) ^ 1)) fail();
       __syncwarp();
       tc_fence_after();
       const bool have = r < a.H;
       const int64_t qrow = (int64_t)b * a.H + r;
-      for (int ch = 0; ch < NCH - QSM; ++ch) {
-        const int gch = QSM + ch;  // chunk of [nope | rope]: 0-7 nope, 8 rope
-        const uint4* src = (gch < 8)
-            ? reinterpret_cast<const uint4*>(a.q_nope + qrow * DC + gch * 64)
-            : reinterpret_cast<const uint4*>(a.q_rope + qrow * DR);
-        uint32_t w[32];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 v = have ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
-          w[4 * k] = v.x;
-          w[4 * k + 1] = v.y;
-          w[4 * k + 2] = v.z;
-          w[4 * k + 3] = v.w;
-        }
+      for (int ch = 2 * hc; ch < 2 * hc + 2; ++ch) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.q_nope + qrow * DC + half * DH + ch * 64);
         uint32_t lo[16], hi[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          lo[k] = w[k];
-          hi[k] = w[16 + k];
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = have ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+          const uint4 w = have ? __ldg(src + 4 + k) : make_uint4(0, 0, 0, 0);
+          lo[4 * k] = v.x; lo[4 * k + 1] = v.y; lo[4 * k + 2] = v.z; lo[4 * k + 3] = v.w;
+          hi[4 * k] = w.x; hi[4 * k + 1] = w.y; hi[4 * k + 2] = w.z; hi[4 * k + 3] = w.w;
         }
         tmem_st16(tmem + lane_off + Q_COL + ch * 32, lo);
         tmem_st16(tmem + lane_off + Q_COL + ch * 32 + 16, hi);
@@ -361,19 +382,43 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
       mbar_arrive(bar(B_QTFULL));
       ++piece_sm;
     };
-    int pb = 0, plast = 0;
+    int pb = 0;
     int64_t p_first = t0, p_segbase = 0;
     bool p_whole = false;
+    int red_par = 0;  // alternates per exchange through `red`
+
+    // Sum of a per-row value over the two warps of the quarter.
+    auto pair_sum = [&](float v) {
+      float* slot = red + red_par * 256;
+      slot[st_id] = v;
+      named_bar_sync(qbar, 64);
+      const float o = slot[(hc ^ 1) * 128 + r];
+      red_par ^= 1;
+      return v + o;
+    };
+    // Row max over the two warps, together with their views of the abort flag, so
+    // that both warps of a quarter leave the loop at the same tile (they meet at a
+    // named barrier in every exchange).
+    auto pair_max_abort = [&](float v, bool& stop) {
+      float2* slot = reinterpret_cast<float2*>(red + 512) + red_par * 256;
+      slot[st_id] = make_float2(v, *abort_flag ? 1.f : 0.f);
+      named_bar_sync(qbar, 64);
+      const float2 o = slot[(hc ^ 1) * 128 + r];
+      red_par ^= 1;
+      stop = __any_sync(0xffffffffu, slot[st_id].y != 0.f || o.y != 0.f);
+      return fmaxf(v, o.x);
+    };
 
     auto finalize = [&](int jl) {
+      const float lt = pair_sum(l);
       if (!mbar_wait(bar(B_ODONE + (jl & 1)), (jl >> 1) & 1)) fail();
       __syncwarp();
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const float lse2 = l > 0.f ? m_ref + log2f(l) : -INFINITY;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float lse2 = lt > 0.f ? m_ref + log2f(lt) : -INFINITY;
       const bool store = r < a.H;
       const int64_t slot = (p_first == p_segbase) ? (int64_t)pb : (int64_t)a.B + ci;
-      for (int c0 = 0; c0 < DH; c0 += 32) {
+      for (int c0 = 128 * hc; c0 < 128 * hc + 128; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_off + O_COL + c0, v);
         tmem_wait_ld();
@@ -408,7 +453,7 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
                                __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
         }
       }
-      if (store) {
+      if (store && hc == 0) {
         if (p_whole) {
           if (a.lse && half == 0) a.lse[(int64_t)pb * a.H + r] = lse2 * kLn2;
         } else {
@@ -417,43 +462,84 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
       }
       tc_fence_before();
       mbar_arrive(bar(B_OFREE));
-      (void)plast;
     };
 
-    for (int j = 0; j < ntiles; ++j) {
-      const bool first = (j == 0) || (c.j == 0);
-      if (first) {
-        if (j > 0) finalize(j - 1);
-        load_q_tmem(c.b);
-        m_ref = -INFINITY;
-        l = 0.f;
-        pb = c.b;
-        p_first = c.t;
-        p_segbase = c.seg_base;
-        p_whole = (c.t == c.seg_base) && (c.t + c.n <= t1);
-      }
-      const int ssb = j % NSB, sb = j & 1;  // S buffer, P buffer
-      if (!mbar_wait(bar(B_SFULL + ssb), (j / NSB) & 1)) fail();
+    // The exchange is software-pipelined: while tile j's softmax runs, this CTA's
+    // partial scores of tile j+1 are already on their way to the peer. They travel as
+    // st.async stores that count their bytes on the peer's XFULL barrier, whose phase
+    // the peer opens (expect_tx) itself, so the sender needs no fence. Two buffers are
+    // enough: tile j+1 is sent only after this thread has consumed the peer's tile j
+    // (its values feed the max below), and the peer sends tile j+2 into the buffer of
+    // tile j only once this CTA's tile j+1 has reached it.
+    uint32_t sv[TT / 2];  // this warp's 32 partial scores of the tile in flight
+    // Read S of tile jn from tensor memory and send it into the peer's buffer.
+    auto fetch_send = [&](int jn) {
+      if (!mbar_wait(bar(B_SFULL), jn & 1)) fail();
       __syncwarp();
       tc_fence_after();
-      uint32_t sv[TT];
-#pragma unroll
-      for (int c0 = 0; c0 < TT; c0 += 32)
-        tmem_ld32(tmem + lane_off + s_col(ssb) + c0, *reinterpret_cast<uint32_t(*)[32]>(&sv[c0]));
+      tmem_ld32(tmem + lane_off + S_COL + 32 * hc, sv);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bar(B_SEMPTY + ssb));
+      mbar_arrive(bar(B_SEMPTY));
+      const uint32_t xo = (uint32_t)(jn & 1) * XBUF, xbar = xbar_peer + 8u * (jn & 1);
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        st_async_v4(x_peer + xo + g * (M * 16), sv[4 * g], sv[4 * g + 1], sv[4 * g + 2], sv[4 * g + 3], xbar);
+    };
+    auto lookup_block = [&](const TileCursor& cc) {
+      return __ldg(a.block_table + (int64_t)cc.b * a.max_blocks + (cc.j * TT) / BS);
+    };
+    auto begin_piece = [&]() {
+      m_ref = -INFINITY;
+      l = 0.f;
+      pb = c.b;
+      p_first = c.t;
+      p_segbase = c.seg_base;
+      p_whole = (c.t == c.seg_base) && (c.t + c.n <= t1);
+    };
+    const bool opener = (hc == 0 && quarter == 2 && lane == 0);  // opens each XFULL phase
 
-      const int tok0 = c.j * TT;
-      const int blk = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + tok0 / BS);
+    load_q_tmem(c.b);
+    begin_piece();
+    int blk = lookup_block(c);
+    fetch_send(0);
+    for (int j = 0; j < ntiles; ++j) {
+      const bool first = (j == 0) || (c.j == 0);
+      const bool more = j + 1 < ntiles;
+      const bool next_first = more && (c.j + 1 == c.n);  // tile j+1 opens a new piece
+      const int xb = j & 1;
+      // Block id of tile j+1, loaded a whole tile before it is used.
+      TileCursor cn = c;
+      cursor_next(cn, a.seq_lens, a.B, 1, TT, 0, cap);
+      const int blk_next = more ? lookup_block(cn) : 0;
+      // Peer's partial scores of tile j, added to this CTA's.
+      if (opener) mbar_expect_tx(bar(B_XFULL + xb), XBUF);
+      if (!mbar_wait_cluster(bar(B_XFULL + xb), (j >> 1) & 1)) fail();
+      const float4* xin = reinterpret_cast<const float4*>(base + OFF_X + xb * XBUF + (8 * hc * M + r) * 16);
+      const int tok0 = c.j * TT + 32 * hc;  // first token of this warp's columns
       const bool blk_ok = blk >= 0 && (int64_t)blk < a.num_blocks;
-      const int nvalid = blk_ok ? min(TT, c.len - tok0) : 0;
-      float x[TT];
+      const int nvalid = blk_ok ? min(32, c.len - tok0) : 0;  // may be <= 0
+      const int nvalid_tile = blk_ok ? min(TT, c.len - c.j * TT) : 0;
+      float x[32];
       float mt = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < TT; ++i) {
-        x[i] = i < nvalid ? __uint_as_float(sv[i]) * a.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, x[i]);
+      for (int g = 0; g < 8; ++g) {
+        const float4 pv = xin[g * M];
+        const float s4[4] = {__uint_as_float(sv[4 * g]) + pv.x, __uint_as_float(sv[4 * g + 1]) + pv.y,
+                             __uint_as_float(sv[4 * g + 2]) + pv.z, __uint_as_float(sv[4 * g + 3]) + pv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 4 * g + e;
+          x[i] = i < nvalid ? s4[e] * a.scale_log2 : -INFINITY;
+          mt = fmaxf(mt, x[i]);
+        }
+      }
+      if (more && !next_first) fetch_send(j + 1);
+      bool stop = false;
+      mt = pair_max_abort(mt, stop);
+      if (stop) {
+        aborted = true;
+        break;
       }
       // Raise the reference max only when this tile exceeds it by more than 8.
       const bool need = mt > m_ref + 8.f;
@@ -465,21 +551,15 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
           if (!mbar_wait(bar(B_ODONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) fail();
           __syncwarp();
           tc_fence_after();
-          for (int c0 = 0; c0 < DH; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_off + O_COL + c0, v);
+          // 16 columns at a time: x and the next tile's scores are live here.
+#pragma unroll 1
+          for (int c0 = 128 * hc; c0 < 128 * hc + 128; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(tmem + lane_off + O_COL + c0, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * (need ? alpha : 1.f));
-            // 32 columns as two 16-column stores
-            uint32_t lo[16], hi[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              lo[k] = v[k];
-              hi[k] = v[16 + k];
-            }
-            tmem_st16(tmem + lane_off + O_COL + c0, lo);
-            tmem_st16(tmem + lane_off + O_COL + c0 + 16, hi);
+            for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * (need ? alpha : 1.f));
+            tmem_st16(tmem + lane_off + O_COL + c0, v);
           }
           tmem_wait_st();
         }
@@ -488,10 +568,10 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
           m_ref = m_new;
         }
       }
-      uint32_t pk[TT / 2];
+      uint32_t pk[16];
       float psum = 0.f;
 #pragma unroll
-      for (int i = 0; i < TT; i += 2) {
+      for (int i = 0; i < 32; i += 2) {
         const float p0 = x[i] == -INFINITY ? 0.f : exp2f(x[i] - m_ref);
         const float p1 = x[i + 1] == -INFINITY ? 0.f : exp2f(x[i + 1] - m_ref);
         __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
@@ -501,33 +581,38 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
       }
       l += psum;
       // Tokens past the sequence's end (the tile's tail) hold any bytes: the score
-      // product is done with this tile (SFULL), so zero those rows of the nope chunks
-      // this CTA's value product reads, so that a weight 0 cannot meet a NaN there.
-      if (nvalid < TT) {
-        uint8_t* kt = base + OFF_K + (j % NST) * NCH * KCH + (4 * half) * KCH;
+      // product is done with this tile (SFULL), so zero those rows of the latent
+      // chunks this CTA's value product reads, so that a weight 0 cannot meet a NaN.
+      if (nvalid_tile < TT) {
+        uint8_t* kt = base + OFF_K + (j % NST) * STAGE;
 #pragma unroll
-        for (int k = 0; k < TT / 4; ++k) {
-          const int pidx = r + 128 * k;           // TT rows x 4 chunks x 8 pieces of 16 B
+        for (int k = 0; k < TT / 8; ++k) {
+          const int pidx = st_id + 256 * k;       // TT rows x 4 chunks x 8 pieces of 16 B
           const int row = pidx >> 5, ch = (pidx >> 3) & 3, q = pidx & 7;
-          if (row >= nvalid)
+          if (row >= nvalid_tile)
             *reinterpret_cast<uint4*>(kt + ch * KCH + row * 128 + q * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
       }
-      if (!mbar_wait(bar(B_PEMPTY + sb), ((j >> 1) & 1) ^ 1)) fail();
+      if (!mbar_wait(bar(B_PEMPTY + xb), ((j >> 1) & 1) ^ 1)) fail();
       __syncwarp();
       tc_fence_after();
-#pragma unroll
-      for (int c0 = 0; c0 < TT / 2; c0 += 16)
-        tmem_st16(tmem + lane_off + p_col(sb) + c0, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c0]));
+      tmem_st16(tmem + lane_off + p_col(xb) + 16 * hc, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(B_PFULL + sb));
-      cursor_next(c, a.seq_lens, a.B, 1, TT, 0, cap);
-      // Warp-uniform exit: the tcgen05 loads and stores above are warp-collective.
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
-        aborted = true;
-        break;
+      mbar_arrive(bar(B_PFULL + xb));
+      c = cn;
+      blk = blk_next;
+      if (more) {
+        if (next_first) {
+          // The score product of a new piece needs that piece's Q in tensor memory
+          // (free once this piece's last score product is done): write it first, so
+          // that S(j+1) runs while this piece's O is read out and stored.
+          load_q_tmem(c.b);
+          fetch_send(j + 1);
+          finalize(j);
+          begin_piece();
+        }
       }
     }
     if (!aborted) finalize(ntiles - 1);
@@ -539,35 +624,28 @@ __global__ void __launch_bounds__(mla::NTHREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
+  // Neither CTA leaves while the other may still write into its shared memory.
+  cluster_sync();
 }
 
 // LSE merge of split MLA pieces: lse = log2 sum_i 2^lse_i, o = sum_i 2^(lse_i - lse) o_i.
-// Grid (sequence, latent half, head group of 8); warp = one query head, lane = 8
-// consecutive latent columns of the half. Segments finished inside one attention
-// CTA are skipped; empty sequences get o = 0, lse = -inf.
+// Only a sequence whose tiles straddle a boundary between two pairs' tile ranges was
+// split. The attention kernel records, per pair, the sequence its range starts in;
+// block (k, g) takes pair i = k + 1 and merges that sequence if pair i's range starts
+// at the sequence's first cut. Warp = one (head, latent half) row of row
+// group g, lane = 8 consecutive latent columns. Block (k, g) also writes o = 0,
+// lse = -inf into row group g of the empty sequences b = k (mod gridDim.x).
 __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
   using namespace mla;
-  const int b = blockIdx.x, half = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.z * 8 + warp;
-  if (h >= a.H) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.y * 8 + warp;  // (head, half) row, 256 per sequence
+  const int h = row >> 1, half = row & 1;
   const int cap = a.max_blocks * BS;
-  int64_t tot = 0, before = 0;
-  for (int bb = lane; bb < a.B; bb += 32) {
-    const int n = live_blocks(clamp_len(__ldg(a.seq_lens + bb), cap), TT, 0).n;
-    tot += n;
-    if (bb < b) before += n;
-  }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    before += __shfl_xor_sync(0xffffffffu, before, o);
-  }
-  const int64_t T = tot, G = a.g_half, base = before;
-  const int n = live_blocks(clamp_len(__ldg(a.seq_lens + b), cap), TT, 0).n;
-  const int64_t out_off = ((int64_t)b * a.H + h) * DC + half * DH + lane * 8;
-  auto put = [&](const float (&v)[8]) {
+  const int64_t G = a.g_half;
+  auto put = [&](int b, const float (&v)[8]) {
+    const int64_t off = ((int64_t)b * a.H + h) * DC + half * DH + lane * 8;
     if (a.out_f32) {
-      float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + out_off);
+      float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off);
       o[0] = make_float4(v[0], v[1], v[2], v[3]);
       o[1] = make_float4(v[4], v[5], v[6], v[7]);
     } else {
@@ -577,29 +655,38 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
         __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
         w[e] = *reinterpret_cast<uint32_t*>(&h2);
       }
-      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + out_off) =
-          make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + off) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   };
-  if (n == 0) {
+  if (h >= a.H) return;
+  for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
+    if (clamp_len(__ldg(a.seq_lens + b), cap) > 0) continue;
     const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    put(z);
+    put(b, z);
     if (a.lse && half == 0 && lane == 0) a.lse[(int64_t)b * a.H + h] = -INFINITY;
-    return;
   }
+  const int64_t i = (int64_t)blockIdx.x + 1;  // boundary between pairs i-1 and i
+  if (i >= G) return;
+  const long long* e = a.ws_bnd + 4 * i;
+  const long long b = e[0];
+  if (b < 0) return;
+  const int64_t base = e[1], n = e[2], T = e[3];
+  const int64_t t = cta_tile_start(i, T, G);
   const int64_t i0 = cta_of_tile(base, T, G), i1 = cta_of_tile(base + n - 1, T, G);
-  if (i0 == i1) return;
-  auto slot_of = [&](int64_t i) { return (i == i0) ? (int64_t)b : (int64_t)a.B + i; };
+  // The sequence's first cut is at tile start(i0 + 1); pairs with empty ranges share
+  // that start with the one non-empty pair that holds it, which merges.
+  if (t == base || cta_tile_start(i0 + 1, T, G) != t) return;
+  auto slot_of = [&](int64_t k) { return (k == i0) ? (int64_t)b : (int64_t)a.B + k; };
   float mx = -INFINITY;
-  for (int64_t i = i0; i <= i1; ++i) {
-    if (i > i0 && cta_tile_start(i + 1, T, G) == cta_tile_start(i, T, G)) continue;
-    mx = fmaxf(mx, a.ws_lse[(slot_of(i) * 2 + half) * M + h]);
+  for (int64_t k = i0; k <= i1; ++k) {
+    if (k > i0 && cta_tile_start(k + 1, T, G) == cta_tile_start(k, T, G)) continue;
+    mx = fmaxf(mx, a.ws_lse[(slot_of(k) * 2 + half) * M + h]);
   }
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   float wsum = 0.f;
-  for (int64_t i = i0; i <= i1; ++i) {
-    if (i > i0 && cta_tile_start(i + 1, T, G) == cta_tile_start(i, T, G)) continue;
-    const int64_t slot = slot_of(i);
+  for (int64_t k = i0; k <= i1; ++k) {
+    if (k > i0 && cta_tile_start(k + 1, T, G) == cta_tile_start(k, T, G)) continue;
+    const int64_t slot = slot_of(k);
     const float l2 = a.ws_lse[(slot * 2 + half) * M + h];
     const float w = (l2 == -INFINITY) ? 0.f : exp2f(l2 - mx);
     const float4* src = reinterpret_cast<const float4*>(a.ws_o + ((slot * 2 + half) * M + h) * DH + lane * 8);
@@ -610,8 +697,8 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] *= inv;
-  put(acc);
+  for (int q = 0; q < 8; ++q) acc[q] *= inv;
+  put((int)b, acc);
   if (a.lse && half == 0 && lane == 0)
     a.lse[(int64_t)b * a.H + h] = wsum > 0.f ? (mx + log2f(wsum)) * kLn2 : -INFINITY;
 }
@@ -620,7 +707,30 @@ size_t mla_workspace_bytes(int B, int g_half) {
   const int64_t slots = (int64_t)B + g_half;
   const size_t o_bytes = (size_t)(slots * 2 * mla::M * mla::DH * 4 + 255) / 256 * 256;
   const size_t l_bytes = (size_t)(slots * 2 * mla::M * 4 + 255) / 256 * 256;
-  return o_bytes + l_bytes;
+  const size_t b_bytes = (size_t)(g_half * 4 * 8 + 255) / 256 * 256;
+  return o_bytes + l_bytes + b_bytes;
+}
+
+// CTA pairs that can be resident at once on the current device (at most num_sms / 2):
+// a pair needs two SMs of one GPC, and a pair that had to wait for a second wave
+// would double the kernel's time.
+static int mla_resident_pairs(int num_sms) {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
+  if (cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms, 1, 1);
+  cfg.blockDim = dim3(mla::NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = mla::SMEM_BYTES;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, (const void*)mla_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    n = num_sms / 2;
+  }
+  n = n < num_sms / 2 ? n : num_sms / 2;
+  cached[dev] = n;
+  return n;
 }
 
 cudaError_t launch_mla_decode(const void* q_nope, const void* q_rope, const void* cache_nope,
@@ -629,6 +739,8 @@ cudaError_t launch_mla_decode(const void* q_nope, const void* q_rope, const void
                               int H, int64_t num_blocks, float scale, void* ws, int* dev_status,
                               int num_sms, cudaStream_t stream) {
   using namespace mla;
+  cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   MlaArgs a{};
   a.q_nope = (const uint16_t*)q_nope;
   a.q_rope = (const uint16_t*)q_rope;
@@ -642,12 +754,14 @@ cudaError_t launch_mla_decode(const void* q_nope, const void* q_rope, const void
   a.H = H;
   a.max_blocks = max_blocks;
   a.out_f32 = out_f32;
-  a.g_half = num_sms / 2;
+  a.g_half = mla_resident_pairs(num_sms);
   a.scale_log2 = scale * 1.4426950408889634f;
   const int64_t slots = (int64_t)B + a.g_half;
   const size_t o_bytes = (size_t)(slots * 2 * M * DH * 4 + 255) / 256 * 256;
   a.ws_o = reinterpret_cast<float*>(ws);
+  const size_t l_bytes = (size_t)(slots * 2 * M * 4 + 255) / 256 * 256;
   a.ws_lse = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + o_bytes);
+  a.ws_bnd = reinterpret_cast<long long*>(reinterpret_cast<uint8_t*>(ws) + o_bytes + l_bytes);
 
   CUtensorMap tqn, tqr, tcn, tcr;
   const uint64_t rows_q = (uint64_t)B * H, rows_c = (uint64_t)num_blocks * BS;
@@ -656,16 +770,16 @@ cudaError_t launch_mla_decode(const void* q_nope, const void* q_rope, const void
   const uint64_t dcn[2] = {DC, rows_c}, scn[1] = {DC * 2};
   const uint64_t dcr[2] = {DR, rows_c}, scr[1] = {DR * 2};
   const uint32_t qbox[2] = {64, M}, cbox[2] = {64, TT};
-  if (!make_tmap_bf16(&tqn, q_nope, 2, dqn, sqn, qbox) || !make_tmap_bf16(&tqr, q_rope, 2, dqr, sqr, qbox) ||
+  const uint32_t qrbox[2] = {DRH, M}, crbox[2] = {DRH, TT};
+  if (!make_tmap_bf16(&tqn, q_nope, 2, dqn, sqn, qbox) ||
+      !make_tmap_bf16_sw64(&tqr, q_rope, 2, dqr, sqr, qrbox) ||
       !make_tmap_bf16(&tcn, cache_nope, 2, dcn, scn, cbox) ||
-      !make_tmap_bf16(&tcr, cache_rope, 2, dcr, scr, cbox))
+      !make_tmap_bf16_sw64(&tcr, cache_rope, 2, dcr, scr, crbox))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (e != cudaSuccess) return e;
   mla_tc_kernel<<<2 * a.g_half, NTHREADS, SMEM_BYTES, stream>>>(a, tqn, tqr, tcn, tcr);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (B > 0) mla_merge_kernel<<<dim3(B, 2, (H + 7) / 8), 256, 0, stream>>>(a);
+  if (B > 0) mla_merge_kernel<<<dim3(a.g_half > 1 ? a.g_half - 1 : 1, 32), 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
