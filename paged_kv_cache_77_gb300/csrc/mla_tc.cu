@@ -211,24 +211,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
     }
     int piece = 0;
     const int rows_oob = (int)(a.num_blocks * BS);
-    // L2 prefetch runs kPrefetch tiles ahead of the loads (second cursor `pc`), so
-    // that a load issued when its stage frees finds the tile in L2.
-    constexpr int kPrefetch = 2;
-    TileCursor pc = c;
-    auto prefetch_next = [&](int jp) {
-      if (jp >= ntiles) return;
-      const int ptok = pc.j * TT;
-      const int pblk = __ldg(a.block_table + (int64_t)pc.b * a.max_blocks + ptok / BS);
-      if (pblk >= 0 && (int64_t)pblk < a.num_blocks) {
-        const int prow = pblk * BS + (ptok % BS);
-        for (int ch = 0; ch < NLC; ++ch) tma_prefetch_2d(&tm_cn, (NLC * half + ch) * 64, prow);
-        tma_prefetch_2d(&tm_cr, DRH * half, prow);
-      }
-      cursor_next(pc, a.seq_lens, a.B, 1, TT, 0, cap);
-    };
-    for (int jp = 0; jp < kPrefetch; ++jp) prefetch_next(jp);
     for (int j = 0; j < ntiles && !*abort_flag; ++j) {
-      prefetch_next(j + kPrefetch);
       if (j == 0 || c.j == 0) {
         if (!mbar_wait_sleepy(bar(B_QEMPTY), (piece & 1) ^ 1)) { fail(); break; }
         mbar_expect_tx(bar(B_QFULL), QRB);
@@ -632,17 +615,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
 // Only a sequence whose tiles straddle a boundary between two pairs' tile ranges was
 // split. The attention kernel records, per pair, the sequence its range starts in;
 // block (k, g) takes pair i = k + 1 and merges that sequence if pair i's range starts
-// at the sequence's first cut. Warp = one (head, latent half) row of row
-// group g, lane = 8 consecutive latent columns. Block (k, g) also writes o = 0,
-// lse = -inf into row group g of the empty sequences b = k (mod gridDim.x).
+// at the sequence's first cut. Warp = two (head, latent half) rows of row group g,
+// lane = 8 consecutive latent columns; the loads of two pieces are issued before any
+// is used. Block (k, g) also writes o = 0, lse = -inf into row group g of the empty
+// sequences b = k (mod gridDim.x).
 __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
   using namespace mla;
+  constexpr int kRows = 2, kMaxPieces = 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.y * 8 + warp;  // (head, half) row, 256 per sequence
-  const int h = row >> 1, half = row & 1;
   const int cap = a.max_blocks * BS;
   const int64_t G = a.g_half;
-  auto put = [&](int b, const float (&v)[8]) {
+  auto put = [&](int b, int h, int half, const float (&v)[8]) {
     const int64_t off = ((int64_t)b * a.H + h) * DC + half * DH + lane * 8;
     if (a.out_f32) {
       float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off);
@@ -658,15 +641,19 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
       *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + off) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   };
-  if (h >= a.H) return;
+  const int row0 = (blockIdx.y * 8 + warp) * kRows;  // first (head, half) row of this warp
   for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
     if (clamp_len(__ldg(a.seq_lens + b), cap) > 0) continue;
     const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    put(b, z);
-    if (a.lse && half == 0 && lane == 0) a.lse[(int64_t)b * a.H + h] = -INFINITY;
+    for (int q = 0; q < kRows; ++q) {
+      const int h = (row0 + q) >> 1, half = (row0 + q) & 1;
+      if (h >= a.H) continue;
+      put(b, h, half, z);
+      if (a.lse && half == 0 && lane == 0) a.lse[(int64_t)b * a.H + h] = -INFINITY;
+    }
   }
-  const int64_t i = (int64_t)blockIdx.x + 1;  // boundary between pairs i-1 and i
-  if (i >= G) return;
+  const int64_t i = (int64_t)blockIdx.x + 1;  // pair whose range start may cut a sequence
+  if (i >= G || row0 >= 2 * a.H) return;
   const long long* e = a.ws_bnd + 4 * i;
   const long long b = e[0];
   if (b < 0) return;
@@ -676,31 +663,74 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
   // The sequence's first cut is at tile start(i0 + 1); pairs with empty ranges share
   // that start with the one non-empty pair that holds it, which merges.
   if (t == base || cta_tile_start(i0 + 1, T, G) != t) return;
-  auto slot_of = [&](int64_t k) { return (k == i0) ? (int64_t)b : (int64_t)a.B + k; };
-  float mx = -INFINITY;
-  for (int64_t k = i0; k <= i1; ++k) {
-    if (k > i0 && cta_tile_start(k + 1, T, G) == cta_tile_start(k, T, G)) continue;
-    mx = fmaxf(mx, a.ws_lse[(slot_of(k) * 2 + half) * M + h]);
-  }
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  float wsum = 0.f;
-  for (int64_t k = i0; k <= i1; ++k) {
-    if (k > i0 && cta_tile_start(k + 1, T, G) == cta_tile_start(k, T, G)) continue;
-    const int64_t slot = slot_of(k);
-    const float l2 = a.ws_lse[(slot * 2 + half) * M + h];
-    const float w = (l2 == -INFINITY) ? 0.f : exp2f(l2 - mx);
-    const float4* src = reinterpret_cast<const float4*>(a.ws_o + ((slot * 2 + half) * M + h) * DH + lane * 8);
-    const float4 x0 = src[0], x1 = src[1];
-    acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
-    acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
-    wsum += w;
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  int64_t slots[kMaxPieces];
+  float mx[kRows], wsum[kRows], acc[kRows][8];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) acc[q] *= inv;
-  put((int)b, acc);
-  if (a.lse && half == 0 && lane == 0)
-    a.lse[(int64_t)b * a.H + h] = wsum > 0.f ? (mx + log2f(wsum)) * kLn2 : -INFINITY;
+  for (int q = 0; q < kRows; ++q) {
+    mx[q] = -INFINITY;
+    wsum[q] = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[q][c] = 0.f;
+  }
+  int64_t k = i0;
+  bool first_pass = true;
+  while (k <= i1) {
+    // Next batch of up to kMaxPieces pieces (pairs with empty ranges hold none).
+    int np = 0;
+    for (; k <= i1 && np < kMaxPieces; ++k) {
+      if (k > i0 && cta_tile_start(k + 1, T, G) == cta_tile_start(k, T, G)) continue;
+      slots[np++] = (k == i0) ? (int64_t)b : (int64_t)a.B + k;
+    }
+    float l2[kMaxPieces][kRows];
+    float4 x[kMaxPieces][kRows][2];
+#pragma unroll
+    for (int p = 0; p < kMaxPieces; ++p) {
+#pragma unroll
+      for (int q = 0; q < kRows; ++q) {
+        const int hr = (row0 + q) >> 1, half = (row0 + q) & 1;
+        const bool ok = p < np && hr < a.H;
+        const int64_t r = ok ? (slots[p] * 2 + half) * M + hr : 0;
+        l2[p][q] = ok ? a.ws_lse[r] : -INFINITY;
+        const float4* src = reinterpret_cast<const float4*>(a.ws_o + r * DH + lane * 8);
+        x[p][q][0] = ok ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[p][q][1] = ok ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    // Online combination across batches (rescale what was accumulated so far).
+#pragma unroll
+    for (int q = 0; q < kRows; ++q) {
+      float m = mx[q];
+#pragma unroll
+      for (int p = 0; p < kMaxPieces; ++p) m = fmaxf(m, l2[p][q]);
+      const float sc = (first_pass || mx[q] == -INFINITY) ? 0.f : exp2f(mx[q] - m);
+      wsum[q] *= sc;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[q][c] *= sc;
+      mx[q] = m;
+#pragma unroll
+      for (int p = 0; p < kMaxPieces; ++p) {
+        const float w = (l2[p][q] == -INFINITY) ? 0.f : exp2f(l2[p][q] - m);
+        wsum[q] += w;
+        acc[q][0] += w * x[p][q][0].x; acc[q][1] += w * x[p][q][0].y;
+        acc[q][2] += w * x[p][q][0].z; acc[q][3] += w * x[p][q][0].w;
+        acc[q][4] += w * x[p][q][1].x; acc[q][5] += w * x[p][q][1].y;
+        acc[q][6] += w * x[p][q][1].z; acc[q][7] += w * x[p][q][1].w;
+      }
+    }
+    first_pass = false;
+  }
+#pragma unroll
+  for (int q = 0; q < kRows; ++q) {
+    const int h = (row0 + q) >> 1, half = (row0 + q) & 1;
+    if (h >= a.H) continue;
+    const float inv = wsum[q] > 0.f ? 1.f / wsum[q] : 0.f;
+    float v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) v[c] = acc[q][c] * inv;
+    put((int)b, h, half, v);
+    if (a.lse && half == 0 && lane == 0)
+      a.lse[(int64_t)b * a.H + h] = wsum[q] > 0.f ? (mx[q] + log2f(wsum[q])) * kLn2 : -INFINITY;
+  }
 }
 
 size_t mla_workspace_bytes(int B, int g_half) {
@@ -779,7 +809,7 @@ cudaError_t launch_mla_decode(const void* q_nope, const void* q_rope, const void
   mla_tc_kernel<<<2 * a.g_half, NTHREADS, SMEM_BYTES, stream>>>(a, tqn, tqr, tcn, tcr);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (B > 0) mla_merge_kernel<<<dim3(a.g_half > 1 ? a.g_half - 1 : 1, 32), 256, 0, stream>>>(a);
+  if (B > 0) mla_merge_kernel<<<dim3(a.g_half > 1 ? a.g_half - 1 : 1, 16), 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
