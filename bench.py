@@ -581,7 +581,7 @@ def run_mla(args, dev):
                      "kernel": f"mla_paged_decode (attention + merge), {dec_ms * 1e3:.1f} us per call",
                      "peak_kind": peak_kind},
         "tensor": {"achieved_tflops": tfl, "peak_tflops": tf, "frac": tfl / tf,
-                   "note": "algorithmic flops; the kernel executes S twice (two latent halves)"},
+                   "note": "algorithmic flops; each score product is split along K across a CTA pair, none is computed twice"},
         "gpu_launches": 3 * args.steps, "clocks": clocks}), flush=True)
 
 
