@@ -4,7 +4,8 @@ One step = the whole decode hot path over one batch: the slot_mapping write of t
 new K/V rows (kv_cache_write) followed by paged decode attention (split-KV
 attention + LSE merge). Inputs are synthetic (synth/), resident in HBM; the KV
 cache of the default workload (4.3 GB) is far larger than the 129 MB L2, so no L2
-flush is needed between steps.
+flush is needed between steps. Caches under 4x L2 (the tiny MHA workload) are
+flushed from L2 before every timed step, outside the timed events.
 
 Prints one JSON line (rank 0). Usage:
   python bench.py [--gpus N --steps K --warmup W] [--workload gqa_long|swa|mha_tiny]
@@ -216,6 +217,10 @@ def cpu_baseline_child(args):
 
 
 # ---------------------------------------------------------------- our arm
+# Caches below this size are L2-flushed between timed steps (4x the 129 MB L2).
+L2_FLUSH_BELOW = 4 * 129e6
+
+
 def traffic_from_profiles(kernel_key: str):
     """DRAM bytes per launch recorded from an ncu capture, if the kernel source is unchanged."""
     import hashlib
@@ -312,27 +317,44 @@ def run_ours(args):
     ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # A cache smaller than 4x the 129 MB L2 would stay L2-resident from step to step:
+    # then L2 is flushed before every step (a 512 MB write, outside the timed events)
+    # and each step is timed by its own events.
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if nbytes["kv"] < L2_FLUSH_BELOW else None
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(i & 0xff)
+        ev_step[i][0].record(stream)
         api.kv_cache_write(v["k_cache"], v["v_cache"], v["k_new"], v["v_new"], slots)
         ev_dec[i][0].record(stream)
         attend(v["q"])
         ev_dec[i][1].record(stream)
+        ev_step[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    ms_total = t_start.elapsed_time(t_end)
+    if flush is None:
+        ms_total = t_start.elapsed_time(t_end)
+    else:
+        ms_total = sum(a.elapsed_time(b) for a, b in ev_step)
     if world > 1:
         tt = torch.tensor([ms_total], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms_total = float(tt.item())
     ms_step = ms_total / args.steps
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_dec)
+    l2_note = ("inputs larger than L2 (KV cache %.2f GB vs 129 MB L2)" % (nbytes["kv"] / 1e9)
+               if flush is None else
+               "L2 flushed before every timed step (512 MB write, not timed); KV cache %.3f GB"
+               % (nbytes["kv"] / 1e9))
 
     # ---- end to end through the public API with host buffers
     pin = {k: v[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")}
@@ -345,6 +367,10 @@ def run_ours(args):
     d2h = out_host.numel() * out_host.element_size()
 
     def e2e_step():
+        if flush is not None:
+            flush.fill_(1)
+            torch.cuda.current_stream().synchronize()
+        t = time.perf_counter()
         sm = api.build_slot_mapping(table_np, d.start_pos, d.num_new, wl.block_size)
         sm_pin = torch.from_numpy(sm)
         dq.copy_(pin["q"], non_blocking=True)
@@ -356,16 +382,14 @@ def run_ours(args):
         attend(dq)
         out_host.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
+        return time.perf_counter() - t
 
     for _ in range(max(3, args.warmup)):
         e2e_step()
     e2e_steps = max(10, args.steps // 4)
     if world > 1:
         dist.barrier()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_s = sum(e2e_step() for _ in range(e2e_steps)) / e2e_steps
     if world > 1:
         tt = torch.tensor([e2e_s], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -387,7 +411,7 @@ def run_ours(args):
                    "step": "kv_cache_write + paged_attention_decode%s (attention + LSE merge)"
                            % ("_spec" if spec else ""),
                    "step_bytes": nbytes["step"],
-                   "l2": "inputs larger than L2 (KV cache %.2f GB vs 129 MB L2)" % (nbytes["kv"] / 1e9),
+                   "l2": l2_note,
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic_from_profiles(f"decode:{wl.name}"),
@@ -657,7 +681,9 @@ def run_prefill(args, dev):
                                f"prior U[{wl.len_lo},{wl.len_hi}], q U[{wl.q_lo},{wl.q_hi}], "
                                f"{wl.forced_q1} decode rows",
                    "step": "kv_cache_write of the new rows + paged_attention_prefill",
-                   "write_bytes": write_bytes, "flops": flops},
+                   "write_bytes": write_bytes, "flops": flops,
+                   "l2": "inputs larger than L2 (KV cache read %.2f GB, q %.2f GB; tensor-bound)"
+                         % (int(d.seq_lens.sum()) * row * 2 / 1e9, T * wl.num_heads * wl.head_dim * 2 / 1e9)},
         "roofline": {"bound": "tensor", "achieved": tfl, "peak": tf, "unit": "TFLOP/s",
                      "frac": tfl / tf, "traffic": traffic_from_profiles("prefill:mixed_prefill"),
                      "kernel": f"paged_attention_prefill (attention + merge), {pf_ms * 1e3:.1f} us",
