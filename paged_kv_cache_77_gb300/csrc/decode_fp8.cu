@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
   using namespace f8d;
   using namespace tc;
   extern __shared__ uint8_t smem_raw[];
+  pdl_launch_dependents();  // the merge may launch now; it waits for this grid
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(base);
   auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };

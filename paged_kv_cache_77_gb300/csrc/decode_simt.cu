@@ -48,6 +48,7 @@ struct SimtSmem {
 
 template <int NREP>
 __global__ void __launch_bounds__(simt::THREADS, 1) decode_simt_kernel(DecodeArgs a) {
+  pdl_launch_dependents();  // the merge may launch now; it waits for this grid
   using namespace simt;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   auto& S = *reinterpret_cast<SimtSmem<NREP>*>(smem_raw);
@@ -276,13 +277,14 @@ __global__ void __launch_bounds__(512) decode_merge_kernel(DecodeArgs a) {
           make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
     }
   };
+  const int64_t i0 = n ? cta_of_tile(base, T, G) : 0, i1 = n ? cta_of_tile(base + n - 1, T, G) : 0;
+  if (n > 0 && i0 == i1) return;  // finished by the attention kernel
+  pdl_wait_primary();
   if (n == 0) {
     put(make_float4(0.f, 0.f, 0.f, 0.f));
     if (a.lse && lane == 0) a.lse[row] = -INFINITY;
     return;
   }
-  const int64_t i0 = cta_of_tile(base, T, G), i1 = cta_of_tile(base + n - 1, T, G);
-  if (i0 == i1) return;  // finished by the attention kernel
   auto slot_of = [&](int64_t i) { return (i == i0) ? (int64_t)seg : (int64_t)a.B * a.Hkv + i; };
   float mx = -INFINITY;
   for (int64_t i = i0; i <= i1; ++i) {
@@ -349,8 +351,7 @@ cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t stream) {
   if (a.B * a.Hkv == 0) return cudaSuccess;
   const int rows = a.n_rep * a.q_len;
   const dim3 grid(a.B * a.Hkv, (rows + 15) / 16);
-  decode_merge_kernel<<<grid, 32 * (rows < 16 ? rows : 16), 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(decode_merge_kernel, grid, dim3(32 * (rows < 16 ? rows : 16)), 0, stream, a);
 }
 
 }  // namespace pkv

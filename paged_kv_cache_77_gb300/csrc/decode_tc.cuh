@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
   using namespace tcd;
   using namespace tc;
   using L = Shape<NREP, QL>;
+  pdl_launch_dependents();  // the merge may launch now; it waits for this grid
   constexpr int NR = L::NR, N = L::N, NCH = L::NCH, CW = L::CW;
   constexpr int QBUF = L::QBUF, PBUF = L::PBUF;
   constexpr int OFF_K = L::OFF_K, OFF_V = L::OFF_V, OFF_Q = L::OFF_Q, OFF_P = L::OFF_P;

@@ -47,6 +47,33 @@ __device__ __forceinline__ float warp_max(float v) {
   return r;
 }
 
+// Programmatic dependent launch. An attention kernel lets the merge kernel that
+// follows it on the stream be launched at once; the merge runs its prologue (which
+// reads only the call's inputs), then waits for the attention kernel to complete and
+// its writes to be visible before it reads the workspace or writes any output.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
+// Launch of a kernel that may start while the previous kernel on the stream is still
+// running (it must call pdl_wait_primary() before depending on that kernel).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 __device__ __forceinline__ void flag_status(int* dev_status, int bits) {
   if (dev_status) atomicOr(dev_status, bits);
 }

@@ -135,6 +135,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
                   const __grid_constant__ CUtensorMap tm_cr) {
   using namespace mla;
   using namespace tc;
+  pdl_launch_dependents();  // the merge may launch now; it waits for this grid
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(base);
@@ -642,6 +643,7 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
     }
   };
   const int row0 = (blockIdx.y * 8 + warp) * kRows;  // first (head, half) row of this warp
+  pdl_wait_primary();
   for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
     if (clamp_len(__ldg(a.seq_lens + b), cap) > 0) continue;
     const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -809,8 +811,8 @@ cudaError_t launch_mla_decode(const void* q_nope, const void* q_rope, const void
   mla_tc_kernel<<<2 * a.g_half, NTHREADS, SMEM_BYTES, stream>>>(a, tqn, tqr, tcn, tcr);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (B > 0) mla_merge_kernel<<<dim3(a.g_half > 1 ? a.g_half - 1 : 1, 16), 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  if (B > 0) return launch_dependent(mla_merge_kernel, dim3(a.g_half > 1 ? a.g_half - 1 : 1, 16), dim3(256), 0, stream, a);
+  return cudaSuccess;
 }
 
 }  // namespace pkv

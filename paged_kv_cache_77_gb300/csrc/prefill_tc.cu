@@ -282,6 +282,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using namespace pf;
   using namespace tc;
+  pdl_launch_dependents();  // the merge may launch now; it waits for this grid
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(base);
@@ -691,6 +692,7 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(PrefillArgs a, int G
   while (first_after < V && empty(first_after)) ++first_after;
   if (first_after != k) return;
   const int64_t i1 = pf_vcta_of_tile(seg_end - 1, W, G);
+  pdl_wait_primary();
   for (int rr = warp; rr < M; rr += 8) {
     const int tok = c.qt * a.qt_tokens + rr / a.n_rep;
     if (tok >= c.s.qlen) continue;
@@ -781,8 +783,7 @@ cudaError_t launch_prefill(const void* q, const int32_t* cu_q, const void* k_cac
   prefill_tc_kernel<<<num_sms, NTHREADS, SMEM_BYTES, stream>>>(a, tq, tk, tv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  prefill_merge_kernel<<<kRounds * num_sms, 256, 0, stream>>>(a, num_sms);
-  return cudaGetLastError();
+  return launch_dependent(prefill_merge_kernel, dim3(kRounds * num_sms), dim3(256), 0, stream, a, num_sms);
 }
 
 }  // namespace pkv
