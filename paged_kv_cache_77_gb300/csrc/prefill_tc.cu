@@ -583,7 +583,8 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       }
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int k = 0; k < 64; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(sv[k]));
+      for (int k = 0; k < 64; k += 2)
+        m4[(k >> 1) & 3] = max3f(m4[(k >> 1) & 3], __uint_as_float(sv[k]), __uint_as_float(sv[k + 1]));
       // Row max over both halves (raw scores; scale_log2 > 0 keeps the order).
       const float mown = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       const float mt = fmaxf(mown, exchange(mown)) * a.scale_log2;
@@ -599,18 +600,15 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
           if (!mbar_wait(bar(B_ODONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) fail();
           __syncwarp();
           tc_fence_after();
-          for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_off + O_COL + c0, v);
+          // 16 columns at a time: the 64 scores of this block are live here.
+#pragma unroll 1
+          for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(tmem + lane_off + O_COL + c0, v);
             tmem_wait_ld();
-            uint32_t lo[16], hi[16];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              lo[k] = __float_as_uint(__uint_as_float(v[k]) * (need ? alpha : 1.f));
-              hi[k] = __float_as_uint(__uint_as_float(v[16 + k]) * (need ? alpha : 1.f));
-            }
-            tmem_st16(tmem + lane_off + O_COL + c0, lo);
-            tmem_st16(tmem + lane_off + O_COL + c0 + 16, hi);
+            for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * (need ? alpha : 1.f));
+            tmem_st16(tmem + lane_off + O_COL + c0, v);
           }
           tmem_wait_st();
         }
@@ -635,24 +633,31 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       tc_fence_after();
       // p = exp2(s * scale_log2 - m_ref): one FMA and one exp2 per key. A row with no
       // visible key so far keeps m_ref = -inf; its p are all 0 (exp2(-inf)).
+      // Scores are taken in pairs: one fma.f32x2 scales and shifts two of them, one
+      // add.f32x2 adds two weights to the normaliser.
       const float mneg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t cs2 = f2pack(a.scale_log2, a.scale_log2), mn2 = f2pack(mneg, mneg);
+      uint64_t ps2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
-          const float p0 = exp2f(fmaf(__uint_as_float(sv[c0 + k]), a.scale_log2, mneg));
-          const float p1 = exp2f(fmaf(__uint_as_float(sv[c0 + k + 1]), a.scale_log2, mneg));
+          const float2 t = f2unpack(ffma2(f2pack(__uint_as_float(sv[c0 + k]), __uint_as_float(sv[c0 + k + 1])),
+                                          cs2, mn2));
+          const float p0 = exp2f(t.x), p1 = exp2f(t.y);
           __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-          const uint32_t w = *reinterpret_cast<uint32_t*>(&h2);
-          // The normaliser sums the bf16-rounded weights the MMA uses.
-          ps4[(k >> 1) & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
-          pk[k / 2] = w;
+          // The normaliser sums the fp32 weights; the MMA uses them rounded to bf16
+          // (relative difference below 2^-9 per weight, averaging out in the sum).
+          ps2[(k >> 1) & 1] = fadd2(ps2[(k >> 1) & 1], f2pack(p0, p1));
+          pk[k / 2] = *reinterpret_cast<uint32_t*>(&h2);
         }
         tmem_st16(tmem + lane_off + p_col(sb) + half * 32 + c0 / 2, pk);
       }
-      l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+      {
+        const float2 s0 = f2unpack(ps2[0]), s1 = f2unpack(ps2[1]);
+        l += (s0.x + s0.y) + (s1.x + s1.y);
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + sb));
