@@ -88,14 +88,29 @@ class DecodeCase:
         assert int(self.status.item()) == 0
 
 
+def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 numbers (8 significant bits) at |x|."""
+    ax = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
+    return np.ldexp(1.0, np.floor(np.log2(ax)).astype(np.int64) - 8)
+
+
 def compare(out: torch.Tensor, lse: torch.Tensor | None, o_ref: np.ndarray, lse_ref: np.ndarray,
             rows, what: str):
-    """Max / mean abs error on the selected leading-index rows."""
+    """Max / mean abs error on the selected leading-index rows.
+
+    A bf16 output is the kernel's fp32 result rounded to nearest even, so each element
+    may differ from the exact value by the 1e-2 bound plus half a bf16 ulp (0.0156 at
+    |o| in [4, 8)); fp32 outputs are held to the bound itself.
+    """
     got = out.float().cpu().numpy()[rows]
     exp = o_ref[rows]
     assert np.isfinite(got).all(), f"{what}: non-finite output"
     err = np.abs(got - exp)
-    assert err.max() <= MAX_ABS_TOL, f"{what}: max abs err {err.max():.3e}"
+    if out.dtype == torch.bfloat16:
+        excess = err - bf16_half_ulp(np.abs(exp) + MAX_ABS_TOL)
+        assert excess.max() <= MAX_ABS_TOL, f"{what}: max abs err beyond bf16 rounding {excess.max():.3e}"
+    else:
+        assert err.max() <= MAX_ABS_TOL, f"{what}: max abs err {err.max():.3e}"
     assert err.mean() <= MEAN_ABS_TOL, f"{what}: mean abs err {err.mean():.3e}"
     if lse is not None:
         lg = lse.cpu().numpy()[rows]
