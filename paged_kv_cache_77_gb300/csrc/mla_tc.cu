@@ -504,20 +504,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       const bool blk_ok = blk >= 0 && (int64_t)blk < a.num_blocks;
       const int nvalid = blk_ok ? min(32, c.len - tok0) : 0;  // may be <= 0
       const int nvalid_tile = blk_ok ? min(TT, c.len - c.j * TT) : 0;
-      float x[32];
-      float mt = -INFINITY;
+      // Raw scores of this warp's 32 columns (the two partial sums added in pairs);
+      // masked columns become -inf. The max is taken on raw scores (scale > 0).
+      uint64_t x2[16];
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
         const float4 pv = xin[g * M];
-        const float s4[4] = {__uint_as_float(sv[4 * g]) + pv.x, __uint_as_float(sv[4 * g + 1]) + pv.y,
-                             __uint_as_float(sv[4 * g + 2]) + pv.z, __uint_as_float(sv[4 * g + 3]) + pv.w};
+        x2[2 * g] = fadd2(f2pack(__uint_as_float(sv[4 * g]), __uint_as_float(sv[4 * g + 1])), f2pack(pv.x, pv.y));
+        x2[2 * g + 1] = fadd2(f2pack(__uint_as_float(sv[4 * g + 2]), __uint_as_float(sv[4 * g + 3])), f2pack(pv.z, pv.w));
+      }
+      if (!__all_sync(0xffffffffu, nvalid >= 32)) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = 4 * g + e;
-          x[i] = i < nvalid ? s4[e] * a.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[i]);
+        for (int q = 0; q < 16; ++q) {
+          const float2 t = f2unpack(x2[q]);
+          x2[q] = f2pack(2 * q < nvalid ? t.x : -INFINITY, 2 * q + 1 < nvalid ? t.y : -INFINITY);
         }
       }
+      float m2[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const float2 t = f2unpack(x2[q]);
+        m2[q & 1] = max3f(m2[q & 1], t.x, t.y);
+      }
+      float mt = fmaxf(m2[0], m2[1]) * a.scale_log2;
       if (more && !next_first) fetch_send(j + 1);
       bool stop = false;
       mt = pair_max_abort(mt, stop);
@@ -552,18 +561,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
           m_ref = m_new;
         }
       }
+      // p = exp2(s * scale_log2 - m_ref): one fma.f32x2 per two scores; a masked
+      // score (-inf) gives 0, and a row that has seen no visible key (m_ref = -inf)
+      // keeps all weights 0. The normaliser sums the fp32 weights (the value product
+      // uses them rounded to bf16; the difference averages out).
+      const float mneg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      const uint64_t cs2 = f2pack(a.scale_log2, a.scale_log2), mn2 = f2pack(mneg, mneg);
       uint32_t pk[16];
-      float psum = 0.f;
+      uint64_t ps2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const float p0 = x[i] == -INFINITY ? 0.f : exp2f(x[i] - m_ref);
-        const float p1 = x[i + 1] == -INFINITY ? 0.f : exp2f(x[i + 1] - m_ref);
+      for (int q = 0; q < 16; ++q) {
+        const float2 t = f2unpack(ffma2(x2[q], cs2, mn2));
+        const float p0 = exp2f(t.x), p1 = exp2f(t.y);
         __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-        const float2 back = __bfloat1622float2(h2);
-        psum += back.x + back.y;
-        pk[i / 2] = *reinterpret_cast<uint32_t*>(&h2);
+        ps2[q & 1] = fadd2(ps2[q & 1], f2pack(p0, p1));
+        pk[q] = *reinterpret_cast<uint32_t*>(&h2);
       }
-      l += psum;
+      {
+        const float2 s0 = f2unpack(ps2[0]), s1 = f2unpack(ps2[1]);
+        l += (s0.x + s0.y) + (s1.x + s1.y);
+      }
       // Tokens past the sequence's end (the tile's tail) hold any bytes: the score
       // product is done with this tile (SFULL), so zero those rows of the latent
       // chunks this CTA's value product reads, so that a weight 0 cannot meet a NaN.
