@@ -87,8 +87,11 @@ enum {
   B_SEMPTY = B_SFULL + 1,
   B_PFULL = B_SEMPTY + 1,
   B_PEMPTY = B_PFULL + 2,
-  B_ODONE = B_PEMPTY + 2,
-  B_OFREE = B_ODONE + 2,
+  // One commit after each value product O(j) completes phase j/2 of barrier j%2:
+  // "P buffer free" and "O holds block j" are the same event, so one barrier pair
+  // serves both.
+  B_ODONE = B_PEMPTY,
+  B_OFREE = B_PEMPTY + 2,
   B_XFULL = B_OFREE + 1,   // peer's partial scores arrived (transaction bytes)
   B_COUNT = B_XFULL + 2
 };
@@ -162,7 +165,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_PFULL + i), 256);
       mbar_init(bar(B_PEMPTY + i), 1);
-      mbar_init(bar(B_ODONE + i), 1);
       mbar_init(bar(B_XFULL + i), 1);
     }
     mbar_init(bar(B_OFREE), 256);
@@ -294,7 +296,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       for (int kk = 0; kk < TT / 16; ++kk)
         mma_ts(tmem + O_COL, tmem + p_col(pb) + kk * 8, desc_add(vd, kk * 2048), ID_O,
                !(first && kk == 0));
-      mma_commit(bar(B_ODONE + pb));
       mma_commit(bar(B_PEMPTY + pb));
       mma_commit(bar(B_KEMPTY + st));
     };

@@ -44,24 +44,33 @@ namespace pf {
 constexpr int D = 128;
 constexpr int BS = 128;
 constexpr int M = 128;
+#ifndef PKV_PF_NQ
+#define PKV_PF_NQ 1
+#endif
 #ifndef PKV_PF_NK
-#define PKV_PF_NK 2
+#define PKV_PF_NK 3
 #endif
 #ifndef PKV_PF_SAHEAD
 #define PKV_PF_SAHEAD 1
 #endif
+// Shared memory holds 7 tiles of 32 KB. A unit's Q is needed only at its start, while
+// K and V loads take ~3.9k cycles under this traffic (measured), so one Q buffer and
+// a deeper K/V ring beat two Q buffers: the next unit's Q load waits for the last
+// score product of the previous unit, once per ~40 blocks.
+constexpr int NQ = PKV_PF_NQ;    // Q buffers
 constexpr int NK = PKV_PF_NK;    // K ring: a K tile is released once its score product is done
-constexpr int NV = 5 - NK;       // V ring: a V tile is released after its value product
+constexpr int NV = 7 - NQ - NK;  // V ring: a V tile is released after its value product
 constexpr int kSAhead = PKV_PF_SAHEAD;  // score products issued ahead of the value product
 // S(j + kSAhead) reuses the S buffer of block j + kSAhead - 2, so more than two ahead
 // would wait on a softmax that itself waits on the value product not yet issued.
-static_assert(NK >= 2 && NV >= 2 && kSAhead >= 1 && kSAhead <= 2, "prefill ring / lookahead");
+static_assert(NQ >= 1 && NQ <= 2 && NK >= 2 && NV >= 2 && kSAhead >= 1 && kSAhead <= 2,
+              "prefill ring / lookahead");
 constexpr int NTHREADS = 384;    // warp 0 Q/K loads, 1 MMAs, 2 V loads, 4-11 softmax
 constexpr int NSM = 256;         // softmax threads: two warps per TMEM lane quarter
 constexpr int HALF = 16384;      // [128 rows x 128 bytes]
 constexpr int TILE = 2 * HALF;   // K or V tile, or a Q tile
-constexpr int OFF_Q = 0;                          // 2 Q buffers
-constexpr int OFF_K = OFF_Q + 2 * TILE;           // NK K tiles
+constexpr int OFF_Q = 0;                          // NQ Q buffers
+constexpr int OFF_K = OFF_Q + NQ * TILE;          // NK K tiles
 constexpr int OFF_V = OFF_K + NK * TILE;          // NV V tiles
 constexpr int OFF_BAR = OFF_V + NV * TILE;        // 229376
 enum {
@@ -75,8 +84,11 @@ enum {
   B_SEMPTY = B_SFULL + 2,
   B_PFULL = B_SEMPTY + 2,
   B_PEMPTY = B_PFULL + 2,
-  B_ODONE = B_PEMPTY + 2,
-  B_OFREE = B_ODONE + 2,
+  // One commit after each value product O(j) completes phase j/2 of barrier j%2:
+  // "P buffer free" and "O holds block j" are the same event, so one barrier pair
+  // serves both.
+  B_ODONE = B_PEMPTY,
+  B_OFREE = B_PEMPTY + 2,
   B_COUNT = B_OFREE + 1
 };
 constexpr int OFF_XCH = OFF_BAR + B_COUNT * 8;      // float [2 halves][128 rows]
@@ -308,7 +320,6 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       mbar_init(bar(B_SEMPTY + i), NSM);
       mbar_init(bar(B_PFULL + i), NSM);
       mbar_init(bar(B_PEMPTY + i), 1);
-      mbar_init(bar(B_ODONE + i), 1);
     }
     mbar_init(bar(B_OFREE), NSM);
     *abort_flag = 0;
@@ -347,8 +358,8 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
     const int rows_oob = (int)(a.num_blocks * BS);
     for (int j = 0; j < ntiles && !*abort_flag; ++j) {
       if (j == 0 || c.j == 0 || c.range_start) {
-        const int qb = piece & 1;
-        if (!mbar_wait(bar(B_QEMPTY + qb), ((piece >> 1) & 1) ^ 1)) { fail(); break; }
+        const int qb = piece % NQ;
+        if (!mbar_wait(bar(B_QEMPTY + qb), ((piece / NQ) & 1) ^ 1)) { fail(); break; }
         mbar_expect_tx(bar(B_QFULL + qb), TILE);
         const int tok = c.s.q0 + c.qt * a.qt_tokens;
         const uint32_t qs = sbase + OFF_Q + qb * TILE;
@@ -404,8 +415,8 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       const int st = j % NK, sb = j & 1;
       firsts = (firsts & ~(1u << (j & 3))) | ((first ? 1u : 0u) << (j & 3));
       if (first) ++piece_s;
-      const int qb = piece_s & 1;
-      if (first && !mbar_wait(bar(B_QFULL + qb), (piece_s >> 1) & 1)) return false;
+      const int qb = piece_s % NQ;
+      if (first && !mbar_wait(bar(B_QFULL + qb), (piece_s / NQ) & 1)) return false;
       if (!mbar_wait(bar(B_KFULL + st), (j / NK) & 1)) return false;
       if (!mbar_wait(bar(B_SEMPTY + sb), ((j >> 1) & 1) ^ 1)) return false;
       tc_fence_after();
@@ -437,7 +448,6 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         mma_ts(tmem + O_COL, pt + kk * 8, desc_add(vd, kk * 2048), ID_O, !(first && kk == 0));
-      mma_commit(bar(B_ODONE + sb));
       mma_commit(bar(B_PEMPTY + sb));
       mma_commit(bar(B_VEMPTY + st));
       return true;
