@@ -95,6 +95,7 @@ constexpr int OFF_XCH = OFF_BAR + B_COUNT * 8;      // float [2 halves][128 rows
 constexpr int OFF_AFL = OFF_XCH + 2 * 128 * 4;      // int [2 halves][4 quarters] abort votes
 constexpr int OFF_MISC = OFF_AFL + 2 * 4 * 4;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory");
 constexpr uint32_t TMEM_COLS = 512;
 __device__ __forceinline__ uint32_t s_col(int b) { return b * 128; }
 __device__ __forceinline__ uint32_t p_col(int b) { return 256 + b * 64; }
