@@ -63,7 +63,7 @@ constexpr int NV = 7 - NQ - NK;  // V ring: a V tile is released after its value
 constexpr int kSAhead = PKV_PF_SAHEAD;  // score products issued ahead of the value product
 // S(j + kSAhead) reuses the S buffer of block j + kSAhead - 2, so more than two ahead
 // would wait on a softmax that itself waits on the value product not yet issued.
-static_assert(NQ >= 1 && NQ <= 2 && NK >= 2 && NV >= 2 && kSAhead >= 1 && kSAhead <= 2,
+static_assert(NQ >= 1 && NQ <= 2 && NK >= 2 && NV >= 2 && kSAhead == 1,
               "prefill ring / lookahead");
 constexpr int NTHREADS = 384;    // warp 0 Q/K loads, 1 MMAs, 2 V loads, 4-11 softmax
 constexpr int NSM = 256;         // softmax threads: two warps per TMEM lane quarter
@@ -88,8 +88,8 @@ enum {
   // "P buffer free" and "O holds block j" are the same event, so one barrier pair
   // serves both.
   B_ODONE = B_PEMPTY,
-  B_OFREE = B_PEMPTY + 2,
-  B_COUNT = B_OFREE + 1
+  B_OFREE = B_PEMPTY + 2,  // per O buffer
+  B_COUNT = B_OFREE + 2
 };
 constexpr int OFF_XCH = OFF_BAR + B_COUNT * 8;      // float [2 halves][128 rows]
 constexpr int OFF_AFL = OFF_XCH + 2 * 128 * 4;      // int [2 halves][4 quarters] abort votes
@@ -97,9 +97,14 @@ constexpr int OFF_MISC = OFF_AFL + 2 * 4 * 4;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 constexpr uint32_t TMEM_COLS = 512;
-__device__ __forceinline__ uint32_t s_col(int b) { return b * 128; }
-__device__ __forceinline__ uint32_t p_col(int b) { return 256 + b * 64; }
-constexpr uint32_t O_COL = 384;
+// Tensor memory (512 columns): one S buffer (the next score product is issued once the
+// softmax has read S into registers), two P buffers of 64 columns (128 bf16 weights
+// packed in pairs), and two O buffers: a unit accumulates into the O buffer its
+// predecessor did not use, so reading out one unit's O never stalls the next unit's
+// value products.
+__device__ __forceinline__ uint32_t s_col(int) { return 0; }
+__device__ __forceinline__ uint32_t p_col(int b) { return 128 + b * 64; }
+__device__ __forceinline__ uint32_t o_col(int ob) { return 256 + ob * 128; }
 }  // namespace pf
 
 struct PrefillArgs {
@@ -148,13 +153,14 @@ __device__ __forceinline__ int pf_nkv(const PrefillArgs& a, const PfSeq& s, int 
 // CTA i walks round 0, then round 1, ...; since every CTA does an equal share of a
 // round, all CTAs are inside the same chunk at any time, which keeps that chunk's
 // K/V resident in L2. The range of round c on CTA i is "virtual CTA" k = c*G + i;
-// pieces and merges work on virtual CTAs. Measured on GB300 (16 sequences, 10.7k
-// query rows, 0.33 GB of K/V), more rounds are slower: 1 round 742 TFLOP/s, 2: 730,
-// 4: 632, 8: 572, 16: 488. Every range boundary adds a partial piece (its O
-// epilogue stalls the MMA pipeline) and the K/V re-reads it saves are not what
-// limits this kernel, so the default is one round (plain stream-K).
+// pieces and merges work on virtual CTAs. Every range boundary adds a partial piece
+// whose O the softmax warps read out. Measured on GB300 (16 sequences, 10.7k query
+// rows, 0.33 GB of K/V, 4.7 GB of DRAM reads with one round): with one O buffer the
+// next unit's value products waited for that readout and more rounds were slower
+// (1 round 742 TFLOP/s, 8: 572); with two O buffers 2 rounds are fastest (1068 us
+// for 1 round, 1021 for 2, 1096 for 4, 1234 for 8).
 #ifndef PKV_PREFILL_ROUNDS
-#define PKV_PREFILL_ROUNDS 1
+#define PKV_PREFILL_ROUNDS 2
 #endif
 constexpr int kRounds = PKV_PREFILL_ROUNDS;
 
@@ -323,6 +329,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       mbar_init(bar(B_PEMPTY + i), 1);
     }
     mbar_init(bar(B_OFREE), NSM);
+    mbar_init(bar(B_OFREE + 1), NSM);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -419,7 +426,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       const int qb = piece_s % NQ;
       if (first && !mbar_wait(bar(B_QFULL + qb), (piece_s / NQ) & 1)) return false;
       if (!mbar_wait(bar(B_KFULL + st), (j / NK) & 1)) return false;
-      if (!mbar_wait(bar(B_SEMPTY + sb), ((j >> 1) & 1) ^ 1)) return false;
+      if (!mbar_wait(bar(B_SEMPTY), (j & 1) ^ 1)) return false;  // softmax has read S(j-1)
       tc_fence_after();
       // Base descriptors once per tile; each K step only adds a constant offset.
       const uint64_t qd = smem_desc(sbase + OFF_Q + qb * TILE, 16, 1024, kSwizzle128);
@@ -428,7 +435,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       for (int kk = 0; kk < 8; ++kk)
         mma_ss(tmem + s_col(sb), desc_add(qd, (kk >> 2) * HALF + (kk & 3) * 32),
                desc_add(kd, (kk >> 2) * HALF + (kk & 3) * 32), ID_S, kk > 0);
-      mma_commit(bar(B_SFULL + sb));
+      mma_commit(bar(B_SFULL));
       mma_commit(bar(B_KEMPTY + st));
       if (last) mma_commit(bar(B_QEMPTY + qb));
       pf_next(c, a);
@@ -441,14 +448,14 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       if (!mbar_wait(bar(B_PFULL + sb), (j >> 1) & 1)) return false;
       if (first) {
         ++piece_o;
-        if (!mbar_wait(bar(B_OFREE), (piece_o & 1) ^ 1)) return false;
+        if (!mbar_wait(bar(B_OFREE + (piece_o & 1)), ((piece_o >> 1) & 1) ^ 1)) return false;
       }
       tc_fence_after();
       const uint64_t vd = smem_desc(sbase + OFF_V + st * TILE, HALF, 1024, kSwizzle128);
       const uint32_t pt = tmem + p_col(sb);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tmem + O_COL, pt + kk * 8, desc_add(vd, kk * 2048), ID_O, !(first && kk == 0));
+        mma_ts(tmem + o_col(piece_o & 1), pt + kk * 8, desc_add(vd, kk * 2048), ID_O, !(first && kk == 0));
       mma_commit(bar(B_PEMPTY + sb));
       mma_commit(bar(B_VEMPTY + st));
       return true;
@@ -497,6 +504,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
     int64_t p_vcta = 0;
     PfSeq ps{};
     bool p_start = false, p_whole = false;
+    int pob = -1;  // O buffer of the piece being accumulated
 
     auto finalize = [&](int jl) {
       // Row normaliser: sum of both halves.
@@ -512,7 +520,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       const int64_t slot = p_vcta * 2 + (p_start ? 1 : 0);
       for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_off + O_COL + c0, v);
+        tmem_ld32(tmem + lane_off + o_col(pob) + c0, v);
         tmem_wait_ld();
         if (p_whole) {
           if (!row_ok) continue;
@@ -552,7 +560,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(bar(B_OFREE));
+      mbar_arrive(bar(B_OFREE + pob));
     };
 
     // The block id of a tile is loaded one tile ahead, off the path from S to P.
@@ -570,9 +578,10 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
         p_vcta = (int64_t)c.round * G + blockIdx.x;
         p_start = (c.t == c.seg_base);
         p_whole = p_start && (c.seg_base + c.n <= c.t_end);
+        pob = (pob < 0) ? 0 : (pob ^ 1);  // O buffer of this piece (alternates)
       }
-      const int sb = j & 1;
-      if (!mbar_wait(bar(B_SFULL + sb), (j >> 1) & 1)) fail();
+      const int sb = j & 1;  // P buffer
+      if (!mbar_wait(bar(B_SFULL), j & 1)) fail();
       __syncwarp();
       tc_fence_after();
       // Visible keys of this row in block c.j: key < kvlen and (causal) key <= c + tok.
@@ -586,7 +595,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       tmem_ld32(tmem + lane_off + s_col(sb) + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bar(B_SEMPTY + sb));
+      mbar_arrive(bar(B_SEMPTY));
       if (!__all_sync(0xffffffffu, nvis >= 64)) {
 #pragma unroll
         for (int k = 0; k < 64; ++k)
@@ -615,11 +624,11 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
 #pragma unroll 1
           for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
             uint32_t v[16];
-            tmem_ld16(tmem + lane_off + O_COL + c0, v);
+            tmem_ld16(tmem + lane_off + o_col(pob) + c0, v);
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * (need ? alpha : 1.f));
-            tmem_st16(tmem + lane_off + O_COL + c0, v);
+            tmem_st16(tmem + lane_off + o_col(pob) + c0, v);
           }
           tmem_wait_st();
         }
