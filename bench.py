@@ -217,6 +217,24 @@ def cpu_baseline_child(args):
 
 
 # ---------------------------------------------------------------- our arm
+def max_over_ranks(x: float, device) -> float:
+    """The largest x over all ranks: the slowest replica sets the job's time."""
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_step: float, world: int, ms_step: float) -> float:
+    """Whole-job units per second: every replica does units_per_step per step, and a
+    step takes ms_step milliseconds on the slowest replica."""
+    return units_per_step * world / (ms_step * 1e-3)
+
+
 # Caches below this size are L2-flushed between timed steps (4x the 129 MB L2).
 L2_FLUSH_BELOW = 4 * 129e6
 
@@ -345,10 +363,7 @@ def run_ours(args):
         ms_total = t_start.elapsed_time(t_end)
     else:
         ms_total = sum(a.elapsed_time(b) for a, b in ev_step)
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_dec)
     l2_note = ("inputs larger than L2 (KV cache %.2f GB vs 129 MB L2)" % (nbytes["kv"] / 1e9)
@@ -390,13 +405,10 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     e2e_s = sum(e2e_step() for _ in range(e2e_steps)) / e2e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
+    e2e_s = max_over_ranks(e2e_s, dev)
 
     hbm, _, peak_kind = peaks()
-    value = nbytes["step"] * world / (ms_step * 1e-3) / 1e9
+    value = job_throughput(nbytes["step"], world, ms_step) / 1e9
     achieved = nbytes["attention"] / (dec_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
