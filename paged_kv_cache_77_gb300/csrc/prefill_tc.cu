@@ -50,9 +50,6 @@ constexpr int M = 128;
 #ifndef PKV_PF_NK
 #define PKV_PF_NK 3
 #endif
-#ifndef PKV_PF_SAHEAD
-#define PKV_PF_SAHEAD 1
-#endif
 // Shared memory holds 7 tiles of 32 KB. A unit's Q is needed only at its start, while
 // K and V loads take ~3.9k cycles under this traffic (measured), so one Q buffer and
 // a deeper K/V ring beat two Q buffers: the next unit's Q load waits for the last
@@ -60,12 +57,9 @@ constexpr int M = 128;
 constexpr int NQ = PKV_PF_NQ;    // Q buffers
 constexpr int NK = PKV_PF_NK;    // K ring: a K tile is released once its score product is done
 constexpr int NV = 7 - NQ - NK;  // V ring: a V tile is released after its value product
-constexpr int kSAhead = PKV_PF_SAHEAD;  // score products issued ahead of the value product
-// S(j + kSAhead) reuses the S buffer of block j + kSAhead - 2, so more than two ahead
-// would wait on a softmax that itself waits on the value product not yet issued.
-static_assert(NQ >= 1 && NQ <= 2 && NK >= 2 && NV >= 2 && kSAhead == 1,
-              "prefill ring / lookahead");
-constexpr int NTHREADS = 384;    // warp 0 Q/K loads, 1 MMAs, 2 V loads, 4-11 softmax
+static_assert(NQ >= 1 && NQ <= 2 && NK >= 2 && NV >= 2,
+              "prefill ring");
+constexpr int NTHREADS = 384;    // warp 0 Q/K loads, 1 score MMAs, 2 V loads, 3 value MMAs, 4-11 softmax
 constexpr int NSM = 256;         // softmax threads: two warps per TMEM lane quarter
 constexpr int HALF = 16384;      // [128 rows x 128 bytes]
 constexpr int TILE = 2 * HALF;   // K or V tile, or a Q tile
@@ -405,50 +399,54 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       pf_next(c, a);
     }
   } else if (ntiles > 0 && warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
-    // Order S(0..kSAhead-1), then S(j + kSAhead), O(j) for each j. With kSAhead = 1
-    // the score product of the next block runs while the softmax of this one is
-    // computed; with 2, S(j+2) is queued as soon as softmax(j) has read S(j). Both
-    // orders and K/V ring splits of 2/3 and 3/2 measured within 1% of each other on
-    // GB300 (mixed prefill, 714-716 TFLOP/s): the softmax warps set the pace.
+    // ------------------------------------------------------------ score-product issuer
+    // Two issuing threads: this one issues S(j) as soon as K(j) has landed and the
+    // softmax has read S(j-1); warp 3 issues the value products. A single thread
+    // issuing both in a fixed order made O(j) wait behind S(j+1)'s waits and commits
+    // and vice versa. Each thread's commits track only its own MMAs.
     constexpr uint32_t ID_S = idesc_bf16(M, 128, 0, 0);  // Q (K-major) x K^T (K-major)
-    constexpr uint32_t ID_O = idesc_bf16(M, 128, 0, 1);  // P (TMEM) x V (MN-major)
     PfCursor c;
     pf_begin(c, a, W, G, blockIdx.x);
-    int piece_s = -1, piece_o = -1;
-    uint32_t firsts = 0;  // bit (j & 3): block j starts a piece (S runs two blocks ahead of O)
-    auto issue_s = [&](int j) -> bool {
+    int piece_s = -1;
+    bool ok = true;
+    for (int j = 0; j < ntiles && !*abort_flag; ++j) {
       const bool first = (j == 0) || (c.j == 0) || c.range_start;
       const bool last = (j + 1 == ntiles) || (c.j + 1 == c.n) || (c.t + 1 == c.t_end);
-      const int st = j % NK, sb = j & 1;
-      firsts = (firsts & ~(1u << (j & 3))) | ((first ? 1u : 0u) << (j & 3));
+      const int st = j % NK;
       if (first) ++piece_s;
       const int qb = piece_s % NQ;
-      if (first && !mbar_wait(bar(B_QFULL + qb), (piece_s / NQ) & 1)) return false;
-      if (!mbar_wait(bar(B_KFULL + st), (j / NK) & 1)) return false;
-      if (!mbar_wait(bar(B_SEMPTY), (j & 1) ^ 1)) return false;  // softmax has read S(j-1)
+      if (first && !mbar_wait(bar(B_QFULL + qb), (piece_s / NQ) & 1)) { ok = false; break; }
+      if (!mbar_wait(bar(B_KFULL + st), (j / NK) & 1)) { ok = false; break; }
+      if (!mbar_wait(bar(B_SEMPTY), (j & 1) ^ 1)) { ok = false; break; }  // softmax has read S(j-1)
       tc_fence_after();
       // Base descriptors once per tile; each K step only adds a constant offset.
       const uint64_t qd = smem_desc(sbase + OFF_Q + qb * TILE, 16, 1024, kSwizzle128);
       const uint64_t kd = smem_desc(sbase + OFF_K + st * TILE, 16, 1024, kSwizzle128);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ss(tmem + s_col(sb), desc_add(qd, (kk >> 2) * HALF + (kk & 3) * 32),
+        mma_ss(tmem + s_col(0), desc_add(qd, (kk >> 2) * HALF + (kk & 3) * 32),
                desc_add(kd, (kk >> 2) * HALF + (kk & 3) * 32), ID_S, kk > 0);
       mma_commit(bar(B_SFULL));
       mma_commit(bar(B_KEMPTY + st));
       if (last) mma_commit(bar(B_QEMPTY + qb));
       pf_next(c, a);
-      return true;
-    };
-    auto issue_o = [&](int j) -> bool {
+    }
+    if (!ok) fail();
+  } else if (ntiles > 0 && warp == 3 && lane == 0) {
+    // ------------------------------------------------------------ value-product issuer
+    constexpr uint32_t ID_O = idesc_bf16(M, 128, 0, 1);  // P (TMEM) x V (MN-major)
+    PfCursor c;
+    pf_begin(c, a, W, G, blockIdx.x);
+    int piece_o = -1;
+    bool ok = true;
+    for (int j = 0; j < ntiles && !*abort_flag; ++j) {
+      const bool first = (j == 0) || (c.j == 0) || c.range_start;
       const int st = j % NV, sb = j & 1;
-      const bool first = (firsts >> (j & 3)) & 1u;
-      if (!mbar_wait(bar(B_VFULL + st), (j / NV) & 1)) return false;
-      if (!mbar_wait(bar(B_PFULL + sb), (j >> 1) & 1)) return false;
+      if (!mbar_wait(bar(B_VFULL + st), (j / NV) & 1)) { ok = false; break; }
+      if (!mbar_wait(bar(B_PFULL + sb), (j >> 1) & 1)) { ok = false; break; }
       if (first) {
         ++piece_o;
-        if (!mbar_wait(bar(B_OFREE + (piece_o & 1)), ((piece_o >> 1) & 1) ^ 1)) return false;
+        if (!mbar_wait(bar(B_OFREE + (piece_o & 1)), ((piece_o >> 1) & 1) ^ 1)) { ok = false; break; }
       }
       tc_fence_after();
       const uint64_t vd = smem_desc(sbase + OFF_V + st * TILE, HALF, 1024, kSwizzle128);
@@ -458,13 +456,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
         mma_ts(tmem + o_col(piece_o & 1), pt + kk * 8, desc_add(vd, kk * 2048), ID_O, !(first && kk == 0));
       mma_commit(bar(B_PEMPTY + sb));
       mma_commit(bar(B_VEMPTY + st));
-      return true;
-    };
-    bool ok = true;
-    for (int j = 0; ok && j < kSAhead && j < ntiles; ++j) ok = issue_s(j);
-    for (int j = 0; ok && j < ntiles && !*abort_flag; ++j) {
-      if (j + kSAhead < ntiles && !issue_s(j + kSAhead)) { ok = false; break; }
-      if (!issue_o(j)) { ok = false; break; }
+      pf_next(c, a);
     }
     if (!ok) fail();
   } else if (ntiles > 0 && warp >= 4) {
