@@ -25,10 +25,10 @@
 // buffered and software-pipelined: tile j+1's partial is sent while tile j's softmax
 // runs.
 //
-// Warps: 0 TMA producer, 1 MMA issuer (polls and issues whichever product is ready),
-// 2..9 softmax, two per TMEM lane quarter, each with 32 of a tile's 64 score columns
-// and 128 of the 256 O columns; the two warps of a quarter agree on the row max
-// through shared memory.
+// Warps: 0 TMA producer, 1 score-product issuer, 2..9 softmax (two per TMEM lane
+// quarter, each with 32 of a tile's 64 score columns and 128 of the 256 O columns; the
+// two warps of a quarter agree on the row max through shared memory), 11 value-product
+// issuer (warp 10 is idle; 12 warps keep at most three per SM sub-partition).
 //
 // Tensor memory (512 columns): S 0..63, P 64..127 (two buffers of 64 bf16 packed in
 // pairs, the A operand of the value product), this CTA's 256 Q latent columns
@@ -71,7 +71,7 @@ constexpr int KRB = TT * DRH * 2;  // this CTA's rope part of a tile: TT rows x 
 constexpr int STAGE = NLC * KCH + KRB;  // 4 latent chunks + 32 rope columns (36 KB)
 constexpr int NST = 4;           // K stages
 constexpr int XBUF = TT * M * 4; // one partial score tile, fp32 (32 KB)
-constexpr int NTHREADS = 320;  // TMA warp, MMA warp, 8 softmax warps
+constexpr int NTHREADS = 384;  // TMA warp, S-issue warp, 8 softmax warps, idle, O-issue warp
 
 constexpr int OFF_K = 0;
 constexpr int OFF_QR = OFF_K + NST * STAGE;        // rope part of Q (64-byte swizzle)
@@ -236,32 +236,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       cursor_next(c, a.seq_lens, a.B, 1, TT, 0, cap);
     }
   } else if (ntiles > 0 && warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ score-product issuer
+    // Two issuing threads: this one issues S(j) once its tile has landed and the
+    // softmax has read S(j-1) (and, for a piece's first tile, once its Q is in place);
+    // warp 11 issues the value products. Each thread's commits track only its own MMAs.
     constexpr uint32_t ID_S = idesc_bf16(M, TT, 0, 0);  // Q (K-major) x K_tile^T (K-major)
-    constexpr uint32_t ID_O = idesc_bf16(M, DH, 0, 1);  // P (TMEM) x nope half (MN-major)
     TileCursor c;
     cursor_seek(c, a.seq_lens, a.B, 1, TT, 0, cap, t0, t1);
     int piece_s = -1;
-    // Dynamic issue order: poll (non-blocking) and issue whichever product is ready,
-    // so that O(j) never waits behind a score product that waits for its tile.
-    // Phases cannot alias: S(js) needs the softmax to have read S(js-1), and the K
-    // stage of js is refilled only after O(js-NST).
-    uint32_t first_bits = 0;  // bit (j mod 4): tile j opens a piece
-    int piece_o = -1;
-    auto ready_s = [&](int j) -> bool {
-      const bool first = (j == 0) || (c.j == 0);
-      const int st = j % NST;
-      if (first && (!mbar_try(bar(B_QFULL), (piece_s + 1) & 1) ||
-                    !mbar_try(bar(B_QTFULL), (piece_s + 1) & 1)))
-        return false;
-      return mbar_try(bar(B_KFULL + st), (j / NST) & 1) && mbar_try(bar(B_SEMPTY), (j & 1) ^ 1);
-    };
-    auto issue_s = [&](int j) {
+    for (int j = 0; j < ntiles && !*abort_flag; ++j) {
       const bool first = (j == 0) || (c.j == 0);
       const bool last = (j + 1 == ntiles) || (c.j + 1 == c.n);
       const int st = j % NST;
-      first_bits = (first_bits & ~(1u << (j & 3))) | ((uint32_t)first << (j & 3));
-      if (first) ++piece_s;
+      if (first) {
+        ++piece_s;
+        if (!mbar_wait(bar(B_QFULL), piece_s & 1) || !mbar_wait(bar(B_QTFULL), piece_s & 1)) { fail(); break; }
+      }
+      if (!mbar_wait(bar(B_KFULL + st), (j / NST) & 1) || !mbar_wait(bar(B_SEMPTY), (j & 1) ^ 1)) {
+        fail();
+        break;
+      }
       tc_fence_after();
       const uint64_t kd = smem_desc(sbase + OFF_K + st * STAGE, 16, 1024, kSwizzle128);
       // Rope parts: rows of 64 bytes, 64-byte swizzle, 8-row groups 512 bytes apart.
@@ -280,16 +274,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       mma_commit(bar(B_SFULL));
       if (last) mma_commit(bar(B_QEMPTY));
       cursor_next(c, a.seq_lens, a.B, 1, TT, 0, cap);
-    };
-    auto ready_o = [&](int j) -> bool {
-      const int pb = j & 1;
-      if (!mbar_try(bar(B_PFULL + pb), (j >> 1) & 1)) return false;
-      return !((first_bits >> (j & 3)) & 1u) || mbar_try(bar(B_OFREE), ((piece_o + 1) & 1) ^ 1);
-    };
-    auto issue_o = [&](int j) {
+    }
+  } else if (ntiles > 0 && warp == 11 && lane == 0) {
+    // ------------------------------------------------------------ value-product issuer
+    // O(j) reads the latent chunks of stage j % NST; its commit also frees the stage
+    // (S(j) completed before the softmax published P(j)).
+    constexpr uint32_t ID_O = idesc_bf16(M, DH, 0, 1);  // P (TMEM) x nope half (MN-major)
+    TileCursor c;
+    cursor_seek(c, a.seq_lens, a.B, 1, TT, 0, cap, t0, t1);
+    int piece_o = -1;
+    for (int j = 0; j < ntiles && !*abort_flag; ++j) {
+      const bool first = (j == 0) || (c.j == 0);
       const int st = j % NST, pb = j & 1;
-      const bool first = (first_bits >> (j & 3)) & 1u;
-      if (first) ++piece_o;
+      if (!mbar_wait(bar(B_PFULL + pb), (j >> 1) & 1)) { fail(); break; }
+      if (first) {
+        ++piece_o;
+        if (!mbar_wait(bar(B_OFREE), (piece_o & 1) ^ 1)) { fail(); break; }
+      }
       tc_fence_after();
       const uint64_t vd = smem_desc(sbase + OFF_K + st * STAGE, KCH, 1024, kSwizzle128);
 #pragma unroll
@@ -298,28 +299,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
                !(first && kk == 0));
       mma_commit(bar(B_PEMPTY + pb));
       mma_commit(bar(B_KEMPTY + st));
-    };
-    int js = 0, jo = 0;
-    long long idle_since = clock64();
-    while (jo < ntiles) {
-      bool done = false;
-      if (jo < js && ready_o(jo)) {
-        issue_o(jo++);
-        done = true;
-      } else if (js < ntiles && ready_s(js)) {
-        issue_s(js++);
-        done = true;
-      }
-      if (done) {
-        idle_since = clock64();
-      } else if (*abort_flag || clock64() - idle_since > kWaitCycles) {
-        fail();
-        break;
-      } else {
-        __nanosleep(32);  // leave the sub-partition's issue slots to the softmax warps
-      }
+      cursor_next(c, a.seq_lens, a.B, 1, TT, 0, cap);
     }
-  } else if (ntiles > 0 && warp >= 2) {
+  } else if (ntiles > 0 && warp >= 2 && warp < 10) {
     // ------------------------------------------------------------ softmax / epilogue
     // Eight warps, two per TMEM lane quarter: warp w takes head row r of its quarter
     // and score columns [32 hc, 32 hc + 32) of each tile, O columns [128 hc, +128).
