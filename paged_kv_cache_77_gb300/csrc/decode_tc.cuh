@@ -24,8 +24,9 @@
 //   warp 0      TMA producer: Q of each piece (box {64 d, n_rep heads, QL tokens}),
 //               K and V halves of each tile (box {64 d, 1 head, 128 tokens}),
 //               128-byte swizzle, 3-deep ring;
-//   warp 1      MMA issuer; S^T of tile j+1 is issued before O^T of tile j so
-//               that the softmax of tile j+1 overlaps the value product of j;
+//   warp 1      MMA issuer: with N = 16 the score products only (S^T of a tile as
+//               soon as its K tile has landed and its S^T buffer is free), a last warp
+//               issuing the value products; with N = 32 both, S^T(j+1) before O^T(j);
 //   warps 2..   softmax, four warps per 16 columns: thread = token lane of S^T.
 //               Block max per column by one warp redux plus a shared-memory
 //               exchange; exp2 in fp32 with q . k pre-scaled by scale * log2 e;
@@ -77,7 +78,11 @@ struct Shape {
   static constexpr int N = NR <= 16 ? 16 : 32;
   static constexpr int NCH = N / 16;
   static constexpr int CW = NCH == 1 ? NR : 16;  // columns a softmax thread carries
-  static constexpr int NTHREADS = 64 + 128 * NCH;
+  // With N = 16 a separate thread issues the value products (measured faster); with
+  // N = 32 (twice the softmax warps) one thread issues both, S^T(j+1) before O^T(j).
+  static constexpr bool SPLIT = NCH == 1;
+  static constexpr int NTHREADS = 64 + 128 * NCH + (SPLIT ? 32 : 0);
+  static constexpr int OWARP = SPLIT ? 2 + 4 * NCH : -1;  // value-product issuer warp
   static constexpr int QBUF = N * 256;           // N rows x 128 d, two 64-wide halves
   static constexpr int PBUF = N * 256;           // 128 tokens x N columns, MN-major
   // Shared-memory layout (offsets from a 1024-aligned base).
@@ -97,6 +102,38 @@ struct Shape {
 };
 
 }  // namespace tcd
+
+// O^T(j) += V^T(j) . P^T(j): waits for V(j), P^T(j) and the O^T buffer, issues the
+// value product, and commits O full, P^T free and the K/V stage free (K(j) was read by
+// S^T(j), complete before the softmax published P^T(j)). False on a wait timeout.
+template <int NREP, int QL>
+__device__ __forceinline__ bool issue_value(const DecodeArgs& a, uint32_t sbase, uint32_t tmem, int j) {
+  using namespace tcd;
+  using namespace tc;
+  using L = Shape<NREP, QL>;
+  constexpr int N = L::N, PBUF = L::PBUF, OFF_V = L::OFF_V, OFF_P = L::OFF_P, OFF_BAR = L::OFF_BAR;
+  constexpr uint32_t ID_O = idesc_bf16(128, N, 1, 1);  // V^T (MN-major) x P^T (MN-major)
+  auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
+  const int st = j % NST, ob = j & 1;
+  if (!mbar_wait(bar(B_VFULL + st), (j / NST) & 1)) return false;
+  if (!mbar_wait(bar(B_PFULL + ob), (j >> 1) & 1)) return false;
+  if (!mbar_wait(bar(B_OEMPTY + ob), ((j >> 1) & 1) ^ 1)) return false;
+  tc_fence_after();
+  const uint64_t vd = smem_desc(sbase + OFF_V + st * TILE, HALF, 1024, kSwizzle128);
+  // P^T, MN-major without swizzle: 8 columns x 8 tokens per 128-byte core matrix. In
+  // this layout the descriptor's stride field (SBO) steps along MN (column groups, 128
+  // bytes apart) and the leading field (LBO) along K (8-token groups, N * 16 bytes
+  // apart), the reverse of the swizzled MN-major forms.
+  const uint64_t pd = smem_desc(sbase + OFF_P + ob * PBUF, N * 16, 128, 0);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ss(tmem + (uint32_t)(2 * N + ob * N), desc_add(vd, kk * 2048), desc_add(pd, kk * 2 * N * 16), ID_O,
+           kk > 0);
+  mma_commit(bar(B_OFULL + ob));
+  mma_commit(bar(B_PEMPTY + ob));
+  mma_commit(bar(B_KVEMPTY + st));
+  return true;
+}
 
 template <int NREP, int QL>
 __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
@@ -217,21 +254,25 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
       cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
     }
   } else if (ntiles > 0 && warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuer(s)
+    // With SPLIT, this thread issues only the score products: S^T(j) once K(j) has
+    // landed and the softmax has read the S^T buffer of tile j-2; warp OWARP issues the
+    // value products. Otherwise this thread issues both, S^T(j+1) before O^T(j), so
+    // that the softmax of tile j+1 overlaps the value product of j. Each thread's
+    // commits track only its own MMAs.
     constexpr uint32_t ID_S = idesc_bf16(128, N, 0, 0);  // K (K-major) x Q^T (K-major)
-    constexpr uint32_t ID_O = idesc_bf16(128, N, 1, 1);  // V^T (MN-major) x P^T (MN-major)
     TileCursor c;
     cursor_seek(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap, t0, t1);
     int piece = -1;
     bool ok = true;
-    auto issue_s = [&](int j) -> bool {
+    for (int j = 0; j < ntiles && !*abort_flag; ++j) {
       const bool first = (j == 0) || (c.j == 0);
       const bool last = (j + 1 == ntiles) || (c.j + 1 == c.n);
       if (first) ++piece;
       const int qb = piece & 1, st = j % NST, sb = j & 1;
-      if (first && !mbar_wait(bar(B_QFULL + qb), (piece >> 1) & 1)) return false;
-      if (!mbar_wait(bar(B_KFULL + st), (j / NST) & 1)) return false;
-      if (!mbar_wait(bar(B_SEMPTY + sb), ((j >> 1) & 1) ^ 1)) return false;
+      if (first && !mbar_wait(bar(B_QFULL + qb), (piece >> 1) & 1)) { ok = false; break; }
+      if (!mbar_wait(bar(B_KFULL + st), (j / NST) & 1)) { ok = false; break; }
+      if (!mbar_wait(bar(B_SEMPTY + sb), ((j >> 1) & 1) ^ 1)) { ok = false; break; }
       tc_fence_after();
       // Base descriptors once per tile; each K step only adds a constant offset.
       const uint64_t kd = smem_desc(sbase + OFF_K + st * TILE, 16, 1024, kSwizzle128);
@@ -243,36 +284,21 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
       mma_commit(bar(B_SFULL + sb));
       if (last) mma_commit(bar(B_QEMPTY + qb));
       cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
-      return true;
-    };
-    auto issue_o = [&](int j) -> bool {
-      const int st = j % NST, ob = j & 1;
-      if (!mbar_wait(bar(B_VFULL + st), (j / NST) & 1)) return false;
-      if (!mbar_wait(bar(B_PFULL + ob), (j >> 1) & 1)) return false;
-      if (!mbar_wait(bar(B_OEMPTY + ob), ((j >> 1) & 1) ^ 1)) return false;
-      tc_fence_after();
-      const uint64_t vd = smem_desc(sbase + OFF_V + st * TILE, HALF, 1024, kSwizzle128);
-      // P^T, MN-major without swizzle: 8 columns x 8 tokens per 128-byte core matrix.
-      // In this layout the descriptor's stride field (SBO) steps along MN (column
-      // groups, 128 bytes apart) and the leading field (LBO) along K (8-token
-      // groups, N * 16 bytes apart), the reverse of the swizzled MN-major forms.
-      const uint64_t pd = smem_desc(sbase + OFF_P + ob * PBUF, N * 16, 128, 0);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ss(tmem + o_col(ob), desc_add(vd, kk * 2048), desc_add(pd, kk * 2 * N * 16), ID_O,
-               kk > 0);
-      mma_commit(bar(B_OFULL + ob));
-      mma_commit(bar(B_PEMPTY + ob));
-      mma_commit(bar(B_KVEMPTY + st));
-      return true;
-    };
-    ok = issue_s(0);
-    for (int j = 0; ok && j < ntiles && !*abort_flag; ++j) {
-      if (j + 1 < ntiles && !issue_s(j + 1)) { ok = false; break; }
-      if (!issue_o(j)) { ok = false; break; }
+      if constexpr (!L::SPLIT) {
+        if (j > 0 && !issue_value<NREP, QL>(a, sbase, tmem, j - 1)) { ok = false; break; }
+      }
+    }
+    if constexpr (!L::SPLIT) {
+      if (ok && ntiles > 0 && !*abort_flag && !issue_value<NREP, QL>(a, sbase, tmem, ntiles - 1)) ok = false;
     }
     if (!ok) fail();
-  } else if (ntiles > 0 && warp >= 2) {
+  } else if (L::SPLIT && ntiles > 0 && warp == L::OWARP && lane == 0) {
+    // ------------------------------------------------------------ value-product issuer
+    bool ok = true;
+    for (int j = 0; j < ntiles && !*abort_flag; ++j)
+      if (!issue_value<NREP, QL>(a, sbase, tmem, j)) { ok = false; break; }
+    if (!ok) fail();
+  } else if (ntiles > 0 && warp >= 2 && warp < 2 + 4 * NCH) {
     // ------------------------------------------------------------ softmax / epilogue
     const int chunk = (warp - 2) >> 2;            // block of 16 columns
     const int qbase = chunk * 16;                 // first column of the block
