@@ -22,12 +22,11 @@
 //
 // Work split and merge: the balanced (b, kv head, block) tile list and partial
 // pieces of the bf16 kernels (device_common.cuh), one persistent CTA per SM.
-// Warp roles (576 threads):
+// Warp roles (608 threads):
 //   warp 0       TMA: Q (bf16) per piece; per tile the K and V code tiles
 //                (box {128 bytes, 1 head, 128 tokens}, 128-byte swizzle) and the
 //                two 512-byte scale rows (bulk copy), 4-deep ring;
-//   warp 1       MMA issuer (S^T of tile j+1 before O^T of tile j; two commits
-//                and three waits per tile);
+//   warp 1       score-product issuer; warp 18 value-product issuer;
 //   warps 2-9    softmax, two groups of four warps: group g owns half of the heads
 //                of every token row (thread = token lane of S^T / d lane of O^T);
 //                both groups convert Q at each piece start;
@@ -68,7 +67,7 @@ constexpr int NSTG = PKV_F8_NSTG;      // code / scale staging ring
 // on, so the MMA thread commits only SFULL and OFULL per tile.
 constexpr int NKOP = 2;
 constexpr int NVOP = 2;
-constexpr int NTHREADS = 576;
+constexpr int NTHREADS = 608;             // + the value-product issuer (warp 18)
 constexpr int NSOFT = 256;             // softmax threads: two warps per TMEM lane quarter
 constexpr int CTILE = BS * D;          // 16 KB of codes: [128 tokens x 128 bytes], swizzled
 constexpr int HALF = 16384;            // f16 [128 rows x 64], one d half, swizzled
@@ -101,7 +100,8 @@ enum {
   B_SFULL = B_QOPE + 2,
   B_PFULL = B_SFULL + 2,
   B_OFULL = B_PFULL + 2,
-  B_COUNT = B_OFULL + 2
+  B_SEMPTY = B_OFULL + 2,  // the softmax has read S^T (count NSOFT)
+  B_COUNT = B_SEMPTY + 2
 };
 constexpr int OFF_RED = OFF_BAR + B_COUNT * 8;       // float [2][4][16] block max per head
 constexpr int OFF_FRED = OFF_RED + 2 * 4 * 16 * 4;   // float [2][4] largest V scale per warp
@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       mbar_init(bar(B_SFULL + i), 1);
       mbar_init(bar(B_PFULL + i), NSOFT);
       mbar_init(bar(B_OFULL + i), 1);
+      mbar_init(bar(B_SEMPTY + i), NSOFT);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -269,25 +270,24 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
     }
   } else if (ntiles > 0 && warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
-    // Per tile two commits (SFULL, OFULL) and the waits for K'(j), V'(j), P'(j).
-    // S(j+2) reuses the S^T buffer of S(j) and is issued after O(j), whose PFULL(j)
-    // the softmax arrives only after reading S^T(j); O(j) reuses the O^T buffer and
-    // P' buffer of tile j-2, which the softmax has folded (resp. released) before it
-    // arrives PFULL(j). So no separate "empty" barriers are needed.
+    // ------------------------------------------------------------ score-product issuer
+    // Two issuing threads: this one issues S^T(j) once K'(j) is widened and the
+    // softmax has read S^T(j-2) (SEMPTY); warp 18 issues the value products. O(j) reuses
+    // the O^T buffer and P' buffer of tile j-2, which the softmax has folded (resp.
+    // released) before it arrives PFULL(j). Each thread's commits track only its own MMAs.
     constexpr uint32_t ID_S = idesc_f16(128, N, 0, 0);  // K' (TMEM) x Q'^T (K-major smem)
-    constexpr uint32_t ID_O = idesc_f16(128, N, 1, 1);  // V'^T (MN-major) x P'^T (MN-major)
     TileCursor c;
     cursor_seek(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap, t0, t1);
     int piece = -1;
     bool ok = true;
-    auto issue_s = [&](int j) -> bool {
+    for (int j = 0; j < ntiles && !*abort_flag; ++j) {
       const bool first = (j == 0) || (c.j == 0);
       const bool last = (j + 1 == ntiles) || (c.j + 1 == c.n);
       if (first) ++piece;
       const int qb = piece & 1, kb = j % NKOP, sb = j & 1;
-      if (first && !mbar_wait(bar(B_QOPF + qb), (piece >> 1) & 1)) return false;
-      if (!mbar_wait(bar(B_KOPF + kb), (j / NKOP) & 1)) return false;
+      if (first && !mbar_wait(bar(B_QOPF + qb), (piece >> 1) & 1)) { ok = false; break; }
+      if (!mbar_wait(bar(B_KOPF + kb), (j / NKOP) & 1)) { ok = false; break; }
+      if (!mbar_wait(bar(B_SEMPTY + sb), ((j >> 1) & 1) ^ 1)) { ok = false; break; }
       tc_fence_after();
       const uint64_t qd = smem_desc(sbase + OFF_QOP + qb * QBUF, 16, 1024, kSwizzle128);
 #pragma unroll
@@ -297,12 +297,16 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       mma_commit(bar(B_SFULL + sb));
       if (last) mma_commit(bar(B_QOPE + qb));
       cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
-      return true;
-    };
-    auto issue_o = [&](int j) -> bool {
+    }
+    if (!ok) fail();
+  } else if (ntiles > 0 && warp == 18 && lane == 0) {
+    // ------------------------------------------------------------ value-product issuer
+    constexpr uint32_t ID_O = idesc_f16(128, N, 1, 1);  // V'^T (MN-major) x P'^T (MN-major)
+    bool ok = true;
+    for (int j = 0; j < ntiles && !*abort_flag; ++j) {
       const int vb = j % NVOP, ob = j & 1;
-      if (!mbar_wait(bar(B_VOPF + vb), (j / NVOP) & 1)) return false;
-      if (!mbar_wait(bar(B_PFULL + ob), (j >> 1) & 1)) return false;
+      if (!mbar_wait(bar(B_VOPF + vb), (j / NVOP) & 1)) { ok = false; break; }
+      if (!mbar_wait(bar(B_PFULL + ob), (j >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
       const uint64_t vd = smem_desc(sbase + OFF_VOP + vb * VOPB, HALF, 1024, kSwizzle128);
       // P'^T, MN-major without swizzle: 8 heads x 8 tokens per 128-byte core matrix;
@@ -314,12 +318,6 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
         mma_ss(tmem + o_col(ob), desc_add(vd, kk * 2048),
                desc_add(pd, kk * 2 * N * 16), ID_O, kk > 0);
       mma_commit(bar(B_OFULL + ob));
-      return true;
-    };
-    ok = issue_s(0);
-    for (int j = 0; ok && j < ntiles && !*abort_flag; ++j) {
-      if (j + 1 < ntiles && !issue_s(j + 1)) { ok = false; break; }
-      if (!issue_o(j)) { ok = false; break; }
     }
     if (!ok) fail();
   } else if (ntiles > 0 && warp >= 10 && warp < 14) {
@@ -358,7 +356,7 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(B_KOPF + kb));
     }
-  } else if (ntiles > 0 && warp >= 14) {
+  } else if (ntiles > 0 && warp >= 14 && warp < 18) {
     // ------------------------------------------------------------ V converters
     // Thread = token row r: codes -> f16 row r of V' (two 64-wide swizzled halves);
     // rows of positions the softmax masks are written as zeros.
@@ -398,7 +396,7 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
       if (j + 1 < ntiles) blk_next = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.jlo + c.j);
     }
-  } else if (ntiles > 0 && warp >= 2) {
+  } else if (ntiles > 0 && warp >= 2 && warp < 10) {
     // ------------------------------------------------------------ softmax / epilogue
     constexpr int HG = NREP > 1 ? NREP / 2 : 1;   // heads per group
     const int quarter = warp & 3;                 // TMEM lane quarter this warp may access
@@ -560,7 +558,8 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       uint32_t svr[16];
       tmem_ld16(tmem + lane_off + s_col(sb), svr);
       tmem_wait_ld();
-      tc_fence_before();  // ordered before PFULL(j), which frees S^T(j)
+      tc_fence_before();
+      mbar_arrive(bar(B_SEMPTY + sb));  // S^T(j) is in registers: S^T(j+2) may overwrite it
 
       const bool blk_ok = blk >= 0 && (int64_t)blk < a.num_blocks;
       const int lo = (a.window > 0 && c.len > a.window) ? c.len - a.window : 0;
