@@ -24,9 +24,9 @@
 //   warp 0      TMA producer: Q of each piece (box {64 d, n_rep heads, QL tokens}),
 //               K and V halves of each tile (box {64 d, 1 head, 128 tokens}),
 //               128-byte swizzle, 3-deep ring;
-//   warp 1      MMA issuer: with N = 16 the score products only (S^T of a tile as
-//               soon as its K tile has landed and its S^T buffer is free), a last warp
-//               issuing the value products; with N = 32 both, S^T(j+1) before O^T(j);
+//   warp 1      score-product issuer (S^T of a tile as soon as its K tile has landed
+//               and its S^T buffer is free); warp 6 (N = 16) or 11 (N = 32) issues the
+//               value products;
 //   warps 2..   softmax, four warps per 16 columns: thread = token lane of S^T.
 //               Block max per column by one warp redux plus a shared-memory
 //               exchange; exp2 in fp32 with q . k pre-scaled by scale * log2 e;
@@ -78,11 +78,10 @@ struct Shape {
   static constexpr int N = NR <= 16 ? 16 : 32;
   static constexpr int NCH = N / 16;
   static constexpr int CW = NCH == 1 ? NR : 16;  // columns a softmax thread carries
-  // With N = 16 a separate thread issues the value products (measured faster); with
-  // N = 32 (twice the softmax warps) one thread issues both, S^T(j+1) before O^T(j).
-  static constexpr bool SPLIT = NCH == 1;
-  static constexpr int NTHREADS = 64 + 128 * NCH + (SPLIT ? 32 : 0);
-  static constexpr int OWARP = SPLIT ? 2 + 4 * NCH : -1;  // value-product issuer warp
+  // A separate thread issues the value products, on the SM sub-partition with the
+  // fewest softmax warps (warp 10 is idle when N = 32).
+  static constexpr int OWARP = NCH == 1 ? 6 : 11;
+  static constexpr int NTHREADS = 32 * (OWARP + 1);
   static constexpr int QBUF = N * 256;           // N rows x 128 d, two 64-wide halves
   static constexpr int PBUF = N * 256;           // 128 tokens x N columns, MN-major
   // Shared-memory layout (offsets from a 1024-aligned base).
@@ -254,11 +253,10 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
       cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
     }
   } else if (ntiles > 0 && warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer(s)
-    // With SPLIT, this thread issues only the score products: S^T(j) once K(j) has
-    // landed and the softmax has read the S^T buffer of tile j-2; warp OWARP issues the
-    // value products. Otherwise this thread issues both, S^T(j+1) before O^T(j), so
-    // that the softmax of tile j+1 overlaps the value product of j. Each thread's
+    // ------------------------------------------------------------ score-product issuer
+    // This thread issues the score products: S^T(j) once K(j) has landed and the softmax
+    // has read the S^T buffer of tile j-2; warp OWARP issues the value products (one
+    // thread issuing both in a fixed order measured 2-4 % slower). Each thread's
     // commits track only its own MMAs.
     constexpr uint32_t ID_S = idesc_bf16(128, N, 0, 0);  // K (K-major) x Q^T (K-major)
     TileCursor c;
@@ -284,15 +282,9 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
       mma_commit(bar(B_SFULL + sb));
       if (last) mma_commit(bar(B_QEMPTY + qb));
       cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
-      if constexpr (!L::SPLIT) {
-        if (j > 0 && !issue_value<NREP, QL>(a, sbase, tmem, j - 1)) { ok = false; break; }
-      }
-    }
-    if constexpr (!L::SPLIT) {
-      if (ok && ntiles > 0 && !*abort_flag && !issue_value<NREP, QL>(a, sbase, tmem, ntiles - 1)) ok = false;
     }
     if (!ok) fail();
-  } else if (L::SPLIT && ntiles > 0 && warp == L::OWARP && lane == 0) {
+  } else if (ntiles > 0 && warp == L::OWARP && lane == 0) {
     // ------------------------------------------------------------ value-product issuer
     bool ok = true;
     for (int j = 0; j < ntiles && !*abort_flag; ++j)
