@@ -537,7 +537,7 @@ def run_fp8(args, dev):
                    "decode_us_per_call": dec_ms * 1e3,
                    "l2": "inputs larger than L2 (%.2f GB of codes and scales)" % (kv / 1e9)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None, "peak_kind": peak_kind,
+                     "frac": achieved / hbm, "traffic": traffic_from_profiles(f"fp8:{wl.name}"), "peak_kind": peak_kind,
                      "kernel": f"paged_attention_decode_fp8 (attention + merge), {dec_ms * 1e3:.1f} us"},
         "gpu_launches": 3 * args.steps, "clocks": clocks}), flush=True)
 
