@@ -283,9 +283,8 @@ size_t pkv_decode_workspace_size(int32_t B, int32_t H, int32_t H_kv, int32_t hea
 
 /* Kernel used by pkv_paged_attention_decode, process-wide (not thread-safe to change
  * while calls are in flight). PKV_KERNEL_AUTO picks the tcgen05 tensor-core kernel
- * for head groups of 4 or more query heads per kv head and the CUDA-core kernel
- * otherwise; the other values force one of them. Both produce the same partial
- * results up to fp32 rounding. */
+ * for every group size; PKV_KERNEL_CUDA_CORE forces the CUDA-core kernel. Both
+ * produce the same partial results up to fp32 rounding. */
 #define PKV_KERNEL_AUTO 0
 #define PKV_KERNEL_CUDA_CORE 1
 #define PKV_KERNEL_TENSOR_CORE 2

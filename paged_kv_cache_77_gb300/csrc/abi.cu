@@ -208,8 +208,9 @@ int pkv_paged_attention_decode(void* out, int32_t out_dtype, float* lse, const v
   if (rc0 != PKV_OK || empty) return rc0;
   clear_error();
   cudaStream_t s = (cudaStream_t)stream;
-  const bool tensor_cores = g_decode_kernel == PKV_KERNEL_TENSOR_CORE ||
-                            (g_decode_kernel == PKV_KERNEL_AUTO && a.n_rep >= 4);
+  // Automatic choice: the tcgen05 kernel for every group size (also faster for n_rep 1:
+  // 21.7 against 25.1 us on the tiny MHA workload).
+  const bool tensor_cores = g_decode_kernel != PKV_KERNEL_CUDA_CORE;
   int rc = launch_status(tensor_cores ? launch_decode_tc(a, s) : launch_decode_simt(a, s),
                          "pkv_paged_attention_decode (attention)");
   if (rc != PKV_OK) return rc;
