@@ -332,8 +332,6 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # A cache smaller than 4x the 129 MB L2 would stay L2-resident from step to step:
     # then L2 is flushed before every step (a 512 MB write, outside the timed events)
@@ -350,9 +348,7 @@ def run_ours(args):
             flush.fill_(i & 0xff)
         ev_step[i][0].record(stream)
         api.kv_cache_write(v["k_cache"], v["v_cache"], v["k_new"], v["v_new"], slots)
-        ev_dec[i][0].record(stream)
         attend(v["q"])
-        ev_dec[i][1].record(stream)
         ev_step[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -365,7 +361,20 @@ def run_ours(args):
         ms_total = sum(a.elapsed_time(b) for a, b in ev_step)
     ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_dec)
+    # The attention call's own time, for the roofline: back-to-back calls with no cache
+    # write between them. (In the step loop the attention kernel launches as a
+    # programmatic dependent of the write kernel and may start before the event placed
+    # between them, so events around it there would miss part of its run.)
+    ev_att = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(i & 0xff)
+        ev_att[i][0].record(stream)
+        attend(v["q"])
+        ev_att[i][1].record(stream)
+    torch.cuda.synchronize()
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_att)
     l2_note = ("inputs larger than L2 (KV cache %.2f GB vs 129 MB L2)" % (nbytes["kv"] / 1e9)
                if flush is None else
                "L2 flushed before every timed step (512 MB write, not timed); KV cache %.3f GB"
@@ -497,28 +506,34 @@ def run_fp8(args, dev):
     bf16_kv = int(vis.sum()) * hkv * dh * 2 * 2
     stream = torch.cuda.current_stream(dev)
 
-    def step(ev=None):
-        api.kv_cache_write_fp8(kc, vc, ks, vs, v["k_new"], v["v_new"], slots)
-        if ev:
-            ev[0].record(stream)
+    def attend():
         api.paged_attention_decode_fp8(v["q"], kc, vc, ks, vs, table, seq_lens, wl.scale, wl.window,
                                        out=out, workspace=ws)
-        if ev:
-            ev[1].record(stream)
+
+    def step():
+        api.kv_cache_write_fp8(kc, vc, ks, vs, v["k_new"], v["v_new"], slots)
+        attend()
 
     for _ in range(args.warmup):
         step()
     sampler = ClockSampler(dev.index or 0)
     sampler.start()
     time.sleep(0.3)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t0.record(stream)
     for i in range(args.steps):
-        step(ev[i])
+        step()
     t1.record(stream)
+    torch.cuda.synchronize()
+    # The attention call's own time: back-to-back calls (in the step loop it may start
+    # before an event placed after the write, as a programmatic dependent of it).
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        attend()
+        ev[i][1].record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
     ms = t0.elapsed_time(t1) / args.steps

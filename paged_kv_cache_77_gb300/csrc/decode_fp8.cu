@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
   using namespace tc;
   extern __shared__ uint8_t smem_raw[];
   pdl_launch_dependents();  // the merge may launch now; it waits for this grid
+  pdl_wait_primary();      // inputs may come from the kernel before (the cache write)
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(base);
   auto bar = [&](int i) { return sbase + OFF_BAR + 8u * i; };
@@ -681,8 +682,8 @@ static cudaError_t launch_fp8_n(const DecodeArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(decode_fp8_kernel<NREP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  decode_fp8_kernel<NREP><<<a.num_ctas, NTHREADS, SMEM_BYTES, stream>>>(a, tk, tv, tq);
-  return cudaGetLastError();
+  return launch_dependent(decode_fp8_kernel<NREP>, dim3(a.num_ctas), dim3(NTHREADS), SMEM_BYTES, stream,
+                          a, tk, tv, tq);
 }
 
 cudaError_t launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream) {

@@ -49,6 +49,7 @@ struct SimtSmem {
 template <int NREP>
 __global__ void __launch_bounds__(simt::THREADS, 1) decode_simt_kernel(DecodeArgs a) {
   pdl_launch_dependents();  // the merge may launch now; it waits for this grid
+  pdl_wait_primary();      // inputs may come from the kernel before (the cache write)
   using namespace simt;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   auto& S = *reinterpret_cast<SimtSmem<NREP>*>(smem_raw);
@@ -332,8 +333,7 @@ static cudaError_t launch_simt_n(const DecodeArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel<NREP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_simt_kernel<NREP><<<a.num_ctas, simt::THREADS, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(decode_simt_kernel<NREP>, dim3(a.num_ctas), dim3(simt::THREADS), smem, stream, a);
 }
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, cudaStream_t stream) {

@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
   using namespace tc;
   using L = Shape<NREP, QL>;
   pdl_launch_dependents();  // the merge may launch now; it waits for this grid
+  pdl_wait_primary();      // inputs may come from the kernel before (the cache write)
   constexpr int NR = L::NR, N = L::N, NCH = L::NCH, CW = L::CW;
   constexpr int QBUF = L::QBUF, PBUF = L::PBUF;
   constexpr int OFF_K = L::OFF_K, OFF_V = L::OFF_V, OFF_Q = L::OFF_Q, OFF_P = L::OFF_P;
@@ -576,8 +577,8 @@ static cudaError_t launch_tc_n(const DecodeArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NREP, QL>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<NREP, QL><<<a.num_ctas, L::NTHREADS, L::SMEM_BYTES, stream>>>(a, tk, tv, tq);
-  return cudaGetLastError();
+  return launch_dependent(decode_tc_kernel<NREP, QL>, dim3(a.num_ctas), dim3(L::NTHREADS), L::SMEM_BYTES, stream,
+                          a, tk, tv, tq);
 }
 
 }  // namespace pkv

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(256) kv_write_kernel(uint8_t* __restrict__ k_c
                                                        const int32_t* __restrict__ slots,
                                                        int64_t num_tokens, int64_t num_slots,
                                                        int ck, int cv, int* dev_status) {
+  pdl_launch_dependents();  // the attention kernel after this one may launch now
   const int per_row = ck + cv;
   const int64_t total = num_tokens * per_row;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(256) kv_write_fp8_kernel(
     float* __restrict__ v_scale, const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
     const int32_t* __restrict__ slots, int64_t num_tokens, int64_t num_slots, int hkv,
     int block_size, int* dev_status) {
+  pdl_launch_dependents();  // the attention kernel after this one may launch now
   const int lane = threadIdx.x & 31;
   const int64_t rows = num_tokens * hkv * 2;
   for (int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); w < rows;
