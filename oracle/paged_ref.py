@@ -24,7 +24,9 @@ passage it follows:
   mask (standalone guide appendix C: a multi-token decode step takes the same mask
   branch as prefill);
 * MLA absorbed: key = value = cache_nope, and q_rope . cache_rope adds to the
-  scores ("KVCache 优化技能" 模式三; standalone guide 模式三; "KV Cache 笔记" MLA).
+  scores ("KVCache 优化技能" 模式三; standalone guide 模式三; "KV Cache 笔记" MLA),
+  for one or several new query rows per sequence (the latter under the same
+  bottom-right mask as speculative decode).
 
 All arithmetic is float64; bf16 inputs are widened exactly.
 """
@@ -236,6 +238,35 @@ def mla_decode(q_nope, q_rope, cache_nope, cache_rope, block_table, seq_lens, bl
         for h in range(H):
             z = scale * (N @ q_nope[b, h] + R @ q_rope[b, h])
             o[b, h], lse[b, h], _ = softmax_combine(z, N, visible)
+    return o, lse
+
+
+def mla_spec_decode(q_nope, q_rope, cache_nope, cache_rope, block_table, seq_lens,
+                    block_size: int, scale: float, batch_indices=None):
+    """Absorbed MLA decode of Q new query rows per sequence (multi-token prediction
+    verification over an MLA cache: standalone guide appendix C, a decode step with
+    q_len > 1 takes sparse_mode 3, the bottom-right causal mask; the scores are the
+    absorbed ones of 模式三).
+
+    q_nope [B, Q, H, 512], q_rope [B, Q, H, 64]; seq_lens [B] totals including the Q
+    new rows. Row i of sequence b sits at position len_b - Q + i and sees the latent
+    rows at positions p <= len_b - Q + i. A row whose position is negative
+    (len_b < Q) sees none: o = 0, lse = -inf.
+    Returns o [B, Q, H, 512] and lse [B, Q, H] (rows not in ``batch_indices`` NaN).
+    """
+    B, Q, H, dc = q_nope.shape
+    o = np.full((B, Q, H, dc), np.nan)
+    lse = np.full((B, Q, H), np.nan)
+    for b in (range(B) if batch_indices is None else batch_indices):
+        n = int(seq_lens[b])
+        N = gather_sequence(cache_nope, block_table[b], n, block_size)[:, 0]
+        R = gather_sequence(cache_rope, block_table[b], n, block_size)[:, 0]
+        pos = np.arange(n)
+        for i in range(Q):
+            visible = pos <= n - Q + i
+            for h in range(H):
+                z = scale * (N @ q_nope[b, i, h] + R @ q_rope[b, i, h])
+                o[b, i, h], lse[b, i, h], _ = softmax_combine(z, N, visible)
     return o, lse
 
 
