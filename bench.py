@@ -281,7 +281,7 @@ def run_ours(args):
         return run_fork(args, dev)
     if args.workload == "mla_write":
         return run_mla_write(args, dev)
-    if args.workload == "mla":
+    if args.workload in ("mla", "mla_spec"):
         return run_mla(args, dev)
     if args.workload == "mixed_prefill":
         return run_prefill(args, dev)
@@ -558,12 +558,14 @@ def run_fp8(args, dev):
 
 
 def run_mla(args, dev):
-    """Absorbed MLA decode step: latent row write (nope + rope) + mla_paged_decode."""
+    """Absorbed MLA decode step: latent row write (nope + rope) + mla_paged_decode, or
+    with q_len > 1 rows per sequence (mla_spec) mla_paged_decode_spec."""
     import torch
 
     from paged_kv_cache_77_gb300 import api
 
-    wl = synth.WORKLOADS["mla"]
+    wl = synth.WORKLOADS[args.workload]
+    Q = wl.q_hi
     if args.batch:
         wl = wl.scaled(batch=args.batch)
     d = synth.draw(wl)
@@ -574,23 +576,33 @@ def run_mla(args, dev):
                                                     wl.block_size)).to(dev)
     table = torch.from_numpy(table_np).to(dev)
     seq_lens = torch.from_numpy(d.seq_lens).to(dev)
-    out = torch.empty((wl.batch, wl.num_heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(api.mla_decode_workspace_size(wl.batch, wl.num_heads), dtype=torch.uint8,
-                     device=dev)
+    rows_shape = (wl.batch, Q, wl.num_heads) if Q > 1 else (wl.batch, wl.num_heads)
+    out = torch.empty(rows_shape + (wl.head_dim,), dtype=torch.bfloat16, device=dev)
+    ws_bytes = (api.mla_decode_spec_workspace_size(wl.batch, Q, wl.num_heads) if Q > 1
+                else api.mla_decode_workspace_size(wl.batch, wl.num_heads))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     lens = d.seq_lens.astype(np.int64)
     row = (wl.head_dim + wl.rope_dim) * 2
-    attn_bytes = int(lens.sum()) * row + wl.batch * wl.num_heads * (wl.head_dim + wl.rope_dim) * 2 \
-        + wl.batch * wl.num_heads * wl.head_dim * 2 + int((-(-lens // 128)).sum()) * 4
-    write_bytes = wl.batch * row * 2 + wl.batch * 4
-    flops = int(lens.sum()) * wl.num_heads * (2 * (wl.head_dim + wl.rope_dim) + 2 * wl.head_dim)
+    T = int(d.num_new.sum())
+    # Algorithmic bytes: each latent row once, q and o of every query row, the table.
+    attn_bytes = int(lens.sum()) * row + wl.batch * Q * wl.num_heads * (wl.head_dim + wl.rope_dim) * 2 \
+        + wl.batch * Q * wl.num_heads * wl.head_dim * 2 + int((-(-lens // 128)).sum()) * 4
+    write_bytes = T * row * 2 + T * 4
+    # Positions seen by query row i of sequence b: len_b - Q + 1 + i (at least 0).
+    seen = sum(int(np.maximum(lens - Q + 1 + i, 0).sum()) for i in range(Q))
+    flops = seen * wl.num_heads * (2 * (wl.head_dim + wl.rope_dim) + 2 * wl.head_dim)
 
     def write():
         api.kv_cache_write(v["cache_nope"], v["cache_rope"], v["nope_new"], v["rope_new"], slots)
 
     def attend():
-        api.mla_paged_decode(v["q_nope"], v["q_rope"], v["cache_nope"], v["cache_rope"], table,
-                             seq_lens, wl.scale, out=out, workspace=ws)
+        if Q > 1:
+            api.mla_paged_decode_spec(v["q_nope"], v["q_rope"], v["cache_nope"], v["cache_rope"],
+                                      table, seq_lens, wl.scale, out=out, workspace=ws)
+        else:
+            api.mla_paged_decode(v["q_nope"], v["q_rope"], v["cache_nope"], v["cache_rope"], table,
+                                 seq_lens, wl.scale, out=out, workspace=ws)
 
     for _ in range(args.warmup):
         write()
@@ -623,16 +635,18 @@ def run_mla(args, dev):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "seq_steps_per_s": wl.batch / (ms * 1e-3),
-        "config": {"workload": f"mla: B={wl.batch} H={wl.num_heads} latent {wl.head_dim} + rope "
-                               f"{wl.rope_dim} bs {wl.block_size}",
+        "config": {"workload": f"{wl.name}: B={wl.batch} q_len={Q} H={wl.num_heads} latent "
+                               f"{wl.head_dim} + rope {wl.rope_dim} bs {wl.block_size}",
                    "seq_lens": f"U[{wl.len_lo},{wl.len_hi}] (sum {int(lens.sum())})",
                    "l2": "inputs larger than L2 (latent cache %.2f GB)" % (int(lens.sum()) * row / 1e9)},
         "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                     "traffic": traffic_from_profiles("mla:mla"),
-                     "kernel": f"mla_paged_decode (attention + merge), {dec_ms * 1e3:.1f} us per call",
+                     "traffic": traffic_from_profiles(f"mla:{wl.name}"),
+                     "kernel": f"mla_paged_decode{'_spec' if Q > 1 else ''} (attention + merge), "
+                               f"{dec_ms * 1e3:.1f} us per call",
                      "peak_kind": peak_kind},
         "tensor": {"achieved_tflops": tfl, "peak_tflops": tf, "frac": tfl / tf,
-                   "note": "algorithmic flops; each score product is split along K across a CTA pair, none is computed twice"},
+                   "note": "algorithmic flops; each score product is split along K across a CTA pair, none is computed twice"
+                           + ("; each query row reads the latent rows it sees, repeats are meant to hit L2" if Q > 1 else "")},
         "gpu_launches": 3 * args.steps, "clocks": clocks}), flush=True)
 
 
@@ -896,7 +910,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa_long",
-                    choices=["gqa_long", "swa", "mha_tiny", "spec_decode", "scatter", "mla",
+                    choices=["gqa_long", "swa", "mha_tiny", "spec_decode", "scatter", "mla", "mla_spec",
                              "mixed_prefill",
                              "fork", "mla_write"])
     ap.add_argument("--batch", type=int, default=0,

@@ -373,6 +373,30 @@ int pkv_mla_paged_decode(void* out, int32_t out_dtype, float* lse, const void* q
                          int32_t rope_dim, int32_t block_size, int64_t num_blocks, float scale,
                          void* workspace, size_t workspace_bytes, int* dev_status, void* stream);
 
+/* Absorbed MLA decode of q_len new query rows per sequence (multi-token prediction
+ * over an MLA cache: standalone guide appendix C, a decode step with q_len > 1 takes
+ * sparse_mode 3, the bottom-right causal mask; scores as in pkv_mla_paged_decode).
+ * All q_len new latent rows are already in the cache. Query row i of sequence b sits
+ * at position len_b - q_len + i and attends to the positions p <= len_b - q_len + i;
+ * a row whose position is negative (len_b < q_len) returns o = 0, lse = -inf.
+ *   out [B, q_len, H, kv_lora_rank] (bf16 or fp32), lse [B, q_len, H] fp32 (nullable)
+ *   q_nope [B, q_len, H, kv_lora_rank] bf16, q_rope [B, q_len, H, rope_dim] bf16
+ *   caches, block_table as for pkv_mla_paged_decode; seq_lens [B] int32 totals
+ * Supported: q_len 1..4 and the shapes of pkv_mla_paged_decode (PKV_ERR_UNSUPPORTED
+ * otherwise); q_len = 1 is pkv_mla_paged_decode. Each row is its own problem: the
+ * rows of one sequence run on different CTA pairs at the same time, so their reads
+ * of a latent tile meet in L2 rather than each coming from HBM.
+ * Workspace: pkv_mla_decode_spec_workspace_size(B, q_len, H) bytes, 256-byte
+ * aligned. Device pointers; asynchronous on `stream`. */
+size_t pkv_mla_decode_spec_workspace_size(int32_t B, int32_t q_len, int32_t H);
+int pkv_mla_paged_decode_spec(void* out, int32_t out_dtype, float* lse, const void* q_nope,
+                              const void* q_rope, const void* cache_nope, const void* cache_rope,
+                              const int32_t* block_table, int32_t max_blocks_per_seq,
+                              const int32_t* seq_lens, int32_t B, int32_t q_len, int32_t H,
+                              int32_t kv_lora_rank, int32_t rope_dim, int32_t block_size,
+                              int64_t num_blocks, float scale, void* workspace,
+                              size_t workspace_bytes, int* dev_status, void* stream);
+
 /* FP8 (E4M3) KV cache: write and decode. A quantised cache halves the bytes a decode
  * step reads. The pages list KV quantisation (skill note 高阶特性: INT8 / W8A8C8;
  * "KV Cache 笔记": KIVI-style grouped quantisation) and warn that dequantising into

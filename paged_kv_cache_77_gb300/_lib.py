@@ -67,6 +67,9 @@ SIGNATURES = {
     "pkv_mla_decode_workspace_size": (sz, [i32, i32]),
     "pkv_mla_paged_decode": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
                                        i32, i64, f32, vp, sz, vp, vp]),
+    "pkv_mla_decode_spec_workspace_size": (sz, [i32, i32, i32]),
+    "pkv_mla_paged_decode_spec": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
+                                            i32, i32, i32, i64, f32, vp, sz, vp, vp]),
     "pkv_paged_attention_decode_static": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, i32,
                                                     i32, i32, i32, i64, f32, i32, vp, vp]),
 }

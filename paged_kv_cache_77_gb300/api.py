@@ -464,6 +464,37 @@ def mla_paged_decode(q_nope, q_rope, cache_nope, cache_rope, block_table, seq_le
     return out
 
 
+def mla_decode_spec_workspace_size(B: int, q_len: int, H: int) -> int:
+    return load().pkv_mla_decode_spec_workspace_size(B, q_len, H)
+
+
+def mla_paged_decode_spec(q_nope, q_rope, cache_nope, cache_rope, block_table, seq_lens,
+                          scale: float, out=None, lse=None, out_dtype=torch.float32, workspace=None,
+                          dev_status=None, stream=None):
+    """Absorbed MLA decode of q_len new rows per sequence (bottom-right causal);
+    q_nope [B, q_len, H, 512], q_rope [B, q_len, H, 64]; returns out [B, q_len, H, 512]."""
+    for t, n in ((q_nope, "q_nope"), (q_rope, "q_rope"), (cache_nope, "cache_nope"),
+                 (cache_rope, "cache_rope")):
+        _dev_bf16(t, n)
+    _dev_i32(block_table, "block_table")
+    _dev_i32(seq_lens, "seq_lens")
+    B, Q, H, dc = q_nope.shape
+    dr = q_rope.shape[3]
+    nb, bs, _, _ = cache_nope.shape
+    if out is None:
+        out = torch.empty((B, Q, H, dc), dtype=out_dtype, device=q_nope.device)
+    code = PKV_F32 if out.dtype == torch.float32 else PKV_BF16
+    if workspace is None:
+        need = mla_decode_spec_workspace_size(B, Q, H)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q_nope.device)
+    check(load().pkv_mla_paged_decode_spec(
+        _ptr(out), code, _ptr(lse), _ptr(q_nope), _ptr(q_rope), _ptr(cache_nope), _ptr(cache_rope),
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, Q, H, dc, dr, bs, nb,
+        float(scale), _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream)),
+        "pkv_mla_paged_decode_spec")
+    return out
+
+
 STATIC_SCRATCH_BYTES = 8 * 1024 * 1024  # PKV_DECODE_STATIC_SCRATCH_BYTES
 
 

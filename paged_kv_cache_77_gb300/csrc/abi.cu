@@ -337,6 +337,47 @@ int pkv_paged_attention_prefill(void* out, int32_t out_dtype, float* lse, const 
                        "pkv_paged_attention_prefill");
 }
 
+// Absorbed MLA decode of q_len query rows per sequence (q_len = 1: plain decode).
+static int mla_decode(const char* name, void* out, int32_t out_dtype, float* lse,
+                      const void* q_nope, const void* q_rope, const void* cache_nope,
+                      const void* cache_rope, const int32_t* block_table, int32_t max_blocks_per_seq,
+                      const int32_t* seq_lens, int32_t B, int32_t q_len, int32_t H,
+                      int32_t kv_lora_rank, int32_t rope_dim, int32_t block_size, int64_t num_blocks,
+                      float scale, void* workspace, size_t workspace_bytes, int* dev_status,
+                      void* stream) {
+  PKV_REQUIRE(B >= 0 && H > 0 && max_blocks_per_seq > 0 && num_blocks > 0, PKV_ERR_INVALID_ARG,
+              "%s: bad sizes", name);
+  PKV_REQUIRE(q_len >= 1 && q_len <= 4, PKV_ERR_UNSUPPORTED, "%s: q_len must be 1..4", name);
+  PKV_REQUIRE(kv_lora_rank == 512 && rope_dim == 64 && block_size == 128 && H <= 128,
+              PKV_ERR_UNSUPPORTED,
+              "%s: implemented for kv_lora_rank 512, rope 64, block_size 128, H <= 128", name);
+  PKV_REQUIRE(out_dtype == PKV_BF16 || out_dtype == PKV_F32, PKV_ERR_INVALID_ARG,
+              "%s: bad out_dtype", name);
+  PKV_REQUIRE(std::isfinite(scale) && scale > 0.f, PKV_ERR_INVALID_ARG,
+              "%s: scale must be a positive finite number", name);
+  PKV_REQUIRE(num_blocks * block_size <= INT32_MAX, PKV_ERR_UNSUPPORTED,
+              "%s: num_blocks * block_size must fit in int32", name);
+  PKV_REQUIRE((int64_t)B * q_len * H <= INT32_MAX, PKV_ERR_UNSUPPORTED,
+              "%s: B * q_len * H must fit in int32", name);
+  if (B == 0) return PKV_OK;
+  PKV_REQUIRE(out && q_nope && q_rope && cache_nope && cache_rope && block_table && seq_lens,
+              PKV_ERR_INVALID_ARG, "%s: null pointer", name);
+  PKV_REQUIRE(aligned16(out) && aligned16(q_nope) && aligned16(q_rope) && aligned16(cache_nope) &&
+                  aligned16(cache_rope),
+              PKV_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", name);
+  const int G = current_num_sms();
+  PKV_REQUIRE(G >= 2, PKV_ERR_LAUNCH, "%s: no CUDA device", name);
+  const size_t need = mla_workspace_bytes(B * q_len, G / 2);
+  PKV_REQUIRE(workspace && workspace_bytes >= need && (((uintptr_t)workspace) & 255) == 0,
+              PKV_ERR_WORKSPACE, "%s: workspace needs %zu bytes, 256-aligned", name, need);
+  clear_error();
+  return launch_status(launch_mla_decode(q_nope, q_rope, cache_nope, cache_rope, block_table,
+                                         max_blocks_per_seq, seq_lens, out, out_dtype == PKV_F32,
+                                         lse, B, q_len, H, num_blocks, scale, workspace, dev_status,
+                                         G, (cudaStream_t)stream),
+                       name);
+}
+
 size_t pkv_mla_decode_workspace_size(int32_t B, int32_t H) {
   if (B < 0 || H <= 0) return 0;
   return mla_workspace_bytes(B, current_num_sms() / 2);
@@ -348,35 +389,28 @@ int pkv_mla_paged_decode(void* out, int32_t out_dtype, float* lse, const void* q
                          const int32_t* seq_lens, int32_t B, int32_t H, int32_t kv_lora_rank,
                          int32_t rope_dim, int32_t block_size, int64_t num_blocks, float scale,
                          void* workspace, size_t workspace_bytes, int* dev_status, void* stream) {
-  PKV_REQUIRE(B >= 0 && H > 0 && max_blocks_per_seq > 0 && num_blocks > 0, PKV_ERR_INVALID_ARG,
-              "pkv_mla_paged_decode: bad sizes");
-  PKV_REQUIRE(kv_lora_rank == 512 && rope_dim == 64 && block_size == 128 && H <= 128,
-              PKV_ERR_UNSUPPORTED,
-              "pkv_mla_paged_decode: implemented for kv_lora_rank 512, rope 64, block_size 128, "
-              "H <= 128");
-  PKV_REQUIRE(out_dtype == PKV_BF16 || out_dtype == PKV_F32, PKV_ERR_INVALID_ARG,
-              "pkv_mla_paged_decode: bad out_dtype");
-  PKV_REQUIRE(std::isfinite(scale) && scale > 0.f, PKV_ERR_INVALID_ARG,
-              "pkv_mla_paged_decode: scale must be a positive finite number");
-  PKV_REQUIRE(num_blocks * block_size <= INT32_MAX, PKV_ERR_UNSUPPORTED,
-              "pkv_mla_paged_decode: num_blocks * block_size must fit in int32");
-  if (B == 0) return PKV_OK;
-  PKV_REQUIRE(out && q_nope && q_rope && cache_nope && cache_rope && block_table && seq_lens,
-              PKV_ERR_INVALID_ARG, "pkv_mla_paged_decode: null pointer");
-  PKV_REQUIRE(aligned16(out) && aligned16(q_nope) && aligned16(q_rope) && aligned16(cache_nope) &&
-                  aligned16(cache_rope),
-              PKV_ERR_INVALID_ARG, "pkv_mla_paged_decode: pointers must be 16-byte aligned");
-  const int G = current_num_sms();
-  PKV_REQUIRE(G >= 2, PKV_ERR_LAUNCH, "pkv_mla_paged_decode: no CUDA device");
-  const size_t need = mla_workspace_bytes(B, G / 2);
-  PKV_REQUIRE(workspace && workspace_bytes >= need && (((uintptr_t)workspace) & 255) == 0,
-              PKV_ERR_WORKSPACE, "pkv_mla_paged_decode: workspace needs %zu bytes, 256-aligned", need);
-  clear_error();
-  return launch_status(launch_mla_decode(q_nope, q_rope, cache_nope, cache_rope, block_table,
-                                         max_blocks_per_seq, seq_lens, out, out_dtype == PKV_F32,
-                                         lse, B, H, num_blocks, scale, workspace, dev_status, G,
-                                         (cudaStream_t)stream),
-                       "pkv_mla_paged_decode");
+  return mla_decode("pkv_mla_paged_decode", out, out_dtype, lse, q_nope, q_rope, cache_nope,
+                    cache_rope, block_table, max_blocks_per_seq, seq_lens, B, 1, H, kv_lora_rank,
+                    rope_dim, block_size, num_blocks, scale, workspace, workspace_bytes, dev_status,
+                    stream);
+}
+
+size_t pkv_mla_decode_spec_workspace_size(int32_t B, int32_t q_len, int32_t H) {
+  if (B < 0 || q_len < 1 || H <= 0) return 0;
+  return mla_workspace_bytes(B * q_len, current_num_sms() / 2);
+}
+
+int pkv_mla_paged_decode_spec(void* out, int32_t out_dtype, float* lse, const void* q_nope,
+                              const void* q_rope, const void* cache_nope, const void* cache_rope,
+                              const int32_t* block_table, int32_t max_blocks_per_seq,
+                              const int32_t* seq_lens, int32_t B, int32_t q_len, int32_t H,
+                              int32_t kv_lora_rank, int32_t rope_dim, int32_t block_size,
+                              int64_t num_blocks, float scale, void* workspace,
+                              size_t workspace_bytes, int* dev_status, void* stream) {
+  return mla_decode("pkv_mla_paged_decode_spec", out, out_dtype, lse, q_nope, q_rope, cache_nope,
+                    cache_rope, block_table, max_blocks_per_seq, seq_lens, B, q_len, H,
+                    kv_lora_rank, rope_dim, block_size, num_blocks, scale, workspace,
+                    workspace_bytes, dev_status, stream);
 }
 
 }  // extern "C"

@@ -61,13 +61,14 @@ cudaError_t launch_decode_spec(const DecodeArgs& a, cudaStream_t stream);
 // partials and merge as above.
 cudaError_t launch_decode_fp8(const DecodeArgs& a, cudaStream_t stream);
 
-// Absorbed MLA decode (tcgen05) plus its merge. Workspace: mla_workspace_bytes.
-size_t mla_workspace_bytes(int B, int g_half);
+// Absorbed MLA decode (tcgen05) plus its merge, q_len query rows per sequence
+// (1 for plain decode). Workspace: mla_workspace_bytes(B * q_len, num_sms / 2).
+size_t mla_workspace_bytes(int rows, int g_half);
 cudaError_t launch_mla_decode(const void* q_nope, const void* q_rope, const void* cache_nope,
                               const void* cache_rope, const int32_t* block_table, int max_blocks,
                               const int32_t* seq_lens, void* out, int out_f32, float* lse, int B,
-                              int H, int64_t num_blocks, float scale, void* ws, int* dev_status,
-                              int num_sms, cudaStream_t stream);
+                              int q_len, int H, int64_t num_blocks, float scale, void* ws,
+                              int* dev_status, int num_sms, cudaStream_t stream);
 
 // Causal paged prefill (tcgen05, stream-K) plus its merge.
 size_t prefill_workspace_bytes(int G);

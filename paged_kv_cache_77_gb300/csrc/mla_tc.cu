@@ -114,23 +114,103 @@ static_assert(Q_COL + NLC * 32 <= O_COL, "tensor memory");
 }  // namespace mla
 
 // Arguments of the MLA decode kernel and its merge.
+// With q_len query rows per sequence, query row i of sequence b is its own attention
+// problem over the first len_b - q_len + 1 + i positions. The kernels walk those
+// problems in "row order" p = i * B + b (query rows major): the q_len rows of a
+// sequence then fall G / q_len pair ranges apart (G a multiple of q_len), run at
+// the same time, and read each latent tile within a few tiles of one another, so
+// that the repeats are served by L2. Row p is stored at index b * q_len + i of the
+// [B, q_len, H, ...] query, output and lse arrays.
 struct MlaArgs {
-  const uint16_t* q_nope;     // [B, H, 512] bf16
-  const uint16_t* q_rope;     // [B, H, 64] bf16
+  const uint16_t* q_nope;     // [B, q_len, H, 512] bf16
+  const uint16_t* q_rope;     // [B, q_len, H, 64] bf16
   const int32_t* block_table;
   const int32_t* seq_lens;
-  void* out;            // [B, H, 512]
-  float* lse;           // [B, H] or null
-  float* ws_o;          // [(B + Gh) * 2 * 128 * 256]
-  float* ws_lse;        // [(B + Gh) * 2 * 128]
-  long long* ws_bnd;    // [Gh][4]: first sequence of pair i's range (-1: empty range),
-                        // that sequence's first tile, its tile count, total tiles
+  void* out;            // [B, q_len, H, 512]
+  float* lse;           // [B, q_len, H] or null
+  float* ws_o;          // [(Bq + Gh) * 2 * 128 * 256]
+  float* ws_lse;        // [(Bq + Gh) * 2 * 128]
+  long long* ws_bnd;    // [Gh][4]: first row p of pair i's range (-1: empty range),
+                        // that row's first tile, its tile count, total tiles
   int* dev_status;
   int64_t num_blocks;
   int B, H, max_blocks, out_f32;
+  int q_len, Bq;        // query rows per sequence, Bq = B * q_len
   int g_half;           // CTA pairs (clusters)
   float scale_log2;
 };
+
+namespace mla {
+__device__ __forceinline__ int seq_of(const MlaArgs& a, int p) { return a.q_len == 1 ? p : p % a.B; }
+// Index of row p in the [B, q_len, ...] arrays.
+__device__ __forceinline__ int64_t row_index(const MlaArgs& a, int p) {
+  return a.q_len == 1 ? (int64_t)p : (int64_t)(p % a.B) * a.q_len + p / a.B;
+}
+// Positions row p attends to: len_b - (q_len - 1 - i), at least 0.
+__device__ __forceinline__ int row_len(const MlaArgs& a, int p, int cap) {
+  const int len = clamp_len(__ldg(a.seq_lens + seq_of(a, p)), cap);
+  if (a.q_len == 1) return len;
+  const int n = len - (a.q_len - 1 - p / a.B);
+  return n > 0 ? n : 0;
+}
+// Tiles of TT positions over all rows (one warp, result in every lane).
+__device__ __forceinline__ int64_t total_tiles(const MlaArgs& a, int cap) {
+  int64_t s = 0;
+  for (int b = threadIdx.x & 31; b < a.B; b += 32) {
+    const int raw = __ldg(a.seq_lens + b);
+    const int len = clamp_len(raw, cap);
+    if (len != raw && blockIdx.x == 0) flag_status(a.dev_status, PKV_DEV_BAD_LENGTH);
+    for (int i = 0; i < a.q_len; ++i) {
+      const int n = len - (a.q_len - 1 - i);
+      if (n > 0) s += (n + TT - 1) / TT;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s;
+}
+// Cursor over a pair's tiles in row order (c.b holds the row p; one kv head, no
+// window, so c.g and c.jlo stay 0).
+__device__ inline void seek(TileCursor& c, const MlaArgs& a, int cap, int64_t t, int64_t t_end) {
+  c.t = t;
+  c.t_end = t_end;
+  c.b = a.Bq;
+  c.g = 0;
+  c.j = 0;
+  c.jlo = 0;
+  c.n = 0;
+  c.len = 0;
+  c.seg_base = 0;
+  if (t >= t_end) return;
+  int64_t base = 0;
+  for (int p = 0; p < a.Bq; ++p) {
+    const int len = row_len(a, p, cap);
+    const int n = (len + TT - 1) / TT;
+    if (t < base + n) {
+      c.b = p;
+      c.j = (int)(t - base);
+      c.n = n;
+      c.len = len;
+      c.seg_base = base;
+      return;
+    }
+    base += n;
+  }
+}
+__device__ inline bool next(TileCursor& c, const MlaArgs& a, int cap) {
+  ++c.t;
+  if (c.t >= c.t_end) return false;
+  if (++c.j < c.n) return true;
+  c.j = 0;
+  c.seg_base += c.n;
+  for (;;) {
+    if (++c.b >= a.Bq) return false;
+    c.len = row_len(a, c.b, cap);
+    c.n = (c.len + TT - 1) / TT;
+    if (c.n > 0) return true;
+  }
+}
+}  // namespace mla
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
     mla_tc_kernel(const __grid_constant__ MlaArgs a, const __grid_constant__ CUtensorMap tm_qn,
@@ -173,7 +253,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
   }
   if (warp == 0) {
     // Tiles of TT tokens: the cursor runs with "block size" TT and one kv head.
-    const int64_t tot = total_live_blocks(a.seq_lens, a.B, TT, 0, cap, a.dev_status);
+    const int64_t tot = total_tiles(a, cap);
     if (lane == 0) {
       *total_s = tot;
       tma_prefetch_desc(&tm_qn);
@@ -204,7 +284,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
   if (ntiles > 0 && warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     TileCursor c;
-    cursor_seek(c, a.seq_lens, a.B, 1, TT, 0, cap, t0, t1);
+    seek(c, a, cap, t0, t1);
     if (half == 0) {
       long long* e = a.ws_bnd + 4 * ci;
       e[0] = c.b;
@@ -218,12 +298,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       if (j == 0 || c.j == 0) {
         if (!mbar_wait_sleepy(bar(B_QEMPTY), (piece & 1) ^ 1)) { fail(); break; }
         mbar_expect_tx(bar(B_QFULL), QRB);
-        tma_load_2d(sbase + OFF_QR, &tm_qr, bar(B_QFULL), DRH * half, c.b * a.H);
+        tma_load_2d(sbase + OFF_QR, &tm_qr, bar(B_QFULL), DRH * half, (int)row_index(a, c.b) * a.H);
         ++piece;
       }
       const int st = j % NST;
       const int tok0 = c.j * TT;  // first token of the tile within the sequence
-      const int blk = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + tok0 / BS);
+      const int blk = __ldg(a.block_table + (int64_t)seq_of(a, c.b) * a.max_blocks + tok0 / BS);
       const bool ok = blk >= 0 && (int64_t)blk < a.num_blocks;
       const int row = ok ? blk * BS + (tok0 % BS) : rows_oob;
       if (!mbar_wait_sleepy(bar(B_KEMPTY + st), ((j / NST) & 1) ^ 1)) { fail(); break; }
@@ -233,7 +313,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       for (int ch = 0; ch < NLC; ++ch)
         tma_load_2d(ks + ch * KCH, &tm_cn, bar(B_KFULL + st), (NLC * half + ch) * 64, row);
       tma_load_2d(ks + NLC * KCH, &tm_cr, bar(B_KFULL + st), DRH * half, row);
-      cursor_next(c, a.seq_lens, a.B, 1, TT, 0, cap);
+      next(c, a, cap);
     }
   } else if (ntiles > 0 && warp == 1 && lane == 0) {
     // ------------------------------------------------------------ score-product issuer
@@ -242,7 +322,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
     // warp 11 issues the value products. Each thread's commits track only its own MMAs.
     constexpr uint32_t ID_S = idesc_bf16(M, TT, 0, 0);  // Q (K-major) x K_tile^T (K-major)
     TileCursor c;
-    cursor_seek(c, a.seq_lens, a.B, 1, TT, 0, cap, t0, t1);
+    seek(c, a, cap, t0, t1);
     int piece_s = -1;
     for (int j = 0; j < ntiles && !*abort_flag; ++j) {
       const bool first = (j == 0) || (c.j == 0);
@@ -273,7 +353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       for (int kk = 0; kk < 2; ++kk) mma_ss(sd, desc_add(qd, kk * 32), desc_add(krd, kk * 32), ID_S, 1);
       mma_commit(bar(B_SFULL));
       if (last) mma_commit(bar(B_QEMPTY));
-      cursor_next(c, a.seq_lens, a.B, 1, TT, 0, cap);
+      next(c, a, cap);
     }
   } else if (ntiles > 0 && warp == 11 && lane == 0) {
     // ------------------------------------------------------------ value-product issuer
@@ -281,7 +361,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
     // (S(j) completed before the softmax published P(j)).
     constexpr uint32_t ID_O = idesc_bf16(M, DH, 0, 1);  // P (TMEM) x nope half (MN-major)
     TileCursor c;
-    cursor_seek(c, a.seq_lens, a.B, 1, TT, 0, cap, t0, t1);
+    seek(c, a, cap, t0, t1);
     int piece_o = -1;
     for (int j = 0; j < ntiles && !*abort_flag; ++j) {
       const bool first = (j == 0) || (c.j == 0);
@@ -299,7 +379,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
                !(first && kk == 0));
       mma_commit(bar(B_PEMPTY + pb));
       mma_commit(bar(B_KEMPTY + st));
-      cursor_next(c, a.seq_lens, a.B, 1, TT, 0, cap);
+      next(c, a, cap);
     }
   } else if (ntiles > 0 && warp >= 2 && warp < 10) {
     // ------------------------------------------------------------ softmax / epilogue
@@ -318,19 +398,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
     float* red = reinterpret_cast<float*>(base + OFF_RED);
     const int qbar = 1 + quarter;                            // named barrier of the two warps
     TileCursor c;
-    cursor_seek(c, a.seq_lens, a.B, 1, TT, 0, cap, t0, t1);
-    float m_ref = -INFINITY, l = 0.f;  // l: normaliser over this warp's columns
+    seek(c, a, cap, t0, t1);
+    // Normalisers over this warp's columns: l of the weights as the value product uses
+    // them (bf16), which divides the output; le of the exact fp32 weights, which gives
+    // the log-sum-exp (the reported lse and the weight of a split piece in the merge).
+    float m_ref = -INFINITY, l = 0.f, le = 0.f;
     bool aborted = false;
     int piece_sm = 0;
     // This CTA's 256 latent columns of Q for head row r into tensor memory (the A
     // operand of the score product), once the previous piece's score products no
     // longer read them. Column half hc writes chunks 2 hc and 2 hc + 1.
-    auto load_q_tmem = [&](int b) {
+    auto load_q_tmem = [&](int64_t qi) {
       if (!mbar_wait(bar(B_QEMPTY), (piece_sm & 1) ^ 1)) fail();
       __syncwarp();
       tc_fence_after();
       const bool have = r < a.H;
-      const int64_t qrow = (int64_t)b * a.H + r;
+      const int64_t qrow = qi * a.H + r;
       for (int ch = 2 * hc; ch < 2 * hc + 2; ++ch) {
         const uint4* src = reinterpret_cast<const uint4*>(a.q_nope + qrow * DC + half * DH + ch * 64);
         uint32_t lo[16], hi[16];
@@ -377,21 +460,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
     };
 
     auto finalize = [&](int jl) {
-      const float lt = pair_sum(l);
+      const float lt = pair_sum(l), lte = pair_sum(le);
       if (!mbar_wait(bar(B_ODONE + (jl & 1)), (jl >> 1) & 1)) fail();
       __syncwarp();
       tc_fence_after();
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      const float lse2 = lt > 0.f ? m_ref + log2f(lt) : -INFINITY;
+      const float lse2 = lte > 0.f ? m_ref + log2f(lte) : -INFINITY;
       const bool store = r < a.H;
-      const int64_t slot = (p_first == p_segbase) ? (int64_t)pb : (int64_t)a.B + ci;
+      const int64_t slot = (p_first == p_segbase) ? (int64_t)pb : (int64_t)a.Bq + ci;
+      const int64_t orow = row_index(a, pb);
       for (int c0 = 128 * hc; c0 < 128 * hc + 128; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_off + O_COL + c0, v);
         tmem_wait_ld();
         if (!store) continue;
         if (p_whole) {
-          const int64_t off = ((int64_t)pb * a.H + r) * DC + half * DH + c0;
+          const int64_t off = (orow * a.H + r) * DC + half * DH + c0;
           if (a.out_f32) {
             float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off);
 #pragma unroll
@@ -422,7 +506,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       }
       if (store && hc == 0) {
         if (p_whole) {
-          if (a.lse && half == 0) a.lse[(int64_t)pb * a.H + r] = lse2 * kLn2;
+          if (a.lse && half == 0) a.lse[orow * a.H + r] = lse2 * kLn2;
         } else {
           a.ws_lse[(slot * 2 + half) * M + r] = lse2;
         }
@@ -454,11 +538,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
         st_async_v4(x_peer + xo + g * (M * 16), sv[4 * g], sv[4 * g + 1], sv[4 * g + 2], sv[4 * g + 3], xbar);
     };
     auto lookup_block = [&](const TileCursor& cc) {
-      return __ldg(a.block_table + (int64_t)cc.b * a.max_blocks + (cc.j * TT) / BS);
+      return __ldg(a.block_table + (int64_t)seq_of(a, cc.b) * a.max_blocks + (cc.j * TT) / BS);
     };
     auto begin_piece = [&]() {
       m_ref = -INFINITY;
       l = 0.f;
+      le = 0.f;
       pb = c.b;
       p_first = c.t;
       p_segbase = c.seg_base;
@@ -466,7 +551,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
     };
     const bool opener = (hc == 0 && quarter == 2 && lane == 0);  // opens each XFULL phase
 
-    load_q_tmem(c.b);
+    load_q_tmem(row_index(a, c.b));
     begin_piece();
     int blk = lookup_block(c);
     fetch_send(0);
@@ -477,7 +562,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       const int xb = j & 1;
       // Block id of tile j+1, loaded a whole tile before it is used.
       TileCursor cn = c;
-      cursor_next(cn, a.seq_lens, a.B, 1, TT, 0, cap);
+      next(cn, a, cap);
       const int blk_next = more ? lookup_block(cn) : 0;
       // Peer's partial scores of tile j, added to this CTA's.
       if (opener) mbar_expect_tx(bar(B_XFULL + xb), XBUF);
@@ -541,28 +626,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
         }
         if (need) {
           l *= alpha;
+          le *= alpha;
           m_ref = m_new;
         }
       }
       // p = exp2(s * scale_log2 - m_ref): one fma.f32x2 per two scores; a masked
       // score (-inf) gives 0, and a row that has seen no visible key (m_ref = -inf)
-      // keeps all weights 0. The normaliser sums the fp32 weights (the value product
-      // uses them rounded to bf16; the difference averages out).
+      // keeps all weights 0. The normaliser sums the weights as the value product
+      // sees them, rounded to bf16: with the lazy reference max a dominant key's
+      // weight is 2^d (0 < d <= 8) rather than exactly 1, and its rounding error (up to
+      // 2^-8) would otherwise scale the whole output row.
       const float mneg = (m_ref == -INFINITY) ? 0.f : -m_ref;
       const uint64_t cs2 = f2pack(a.scale_log2, a.scale_log2), mn2 = f2pack(mneg, mneg);
       uint32_t pk[16];
-      uint64_t ps2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+      uint64_t ps2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)}, pe2[2] = {ps2[0], ps2[1]};
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
         const float2 t = f2unpack(ffma2(x2[q], cs2, mn2));
         const float p0 = exp2f(t.x), p1 = exp2f(t.y);
         __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-        ps2[q & 1] = fadd2(ps2[q & 1], f2pack(p0, p1));
         pk[q] = *reinterpret_cast<uint32_t*>(&h2);
+        ps2[q & 1] = fadd2(ps2[q & 1], f2pack(__uint_as_float(pk[q] << 16), __uint_as_float(pk[q] & 0xffff0000u)));
+        pe2[q & 1] = fadd2(pe2[q & 1], f2pack(p0, p1));
       }
       {
         const float2 s0 = f2unpack(ps2[0]), s1 = f2unpack(ps2[1]);
         l += (s0.x + s0.y) + (s1.x + s1.y);
+        const float2 e0 = f2unpack(pe2[0]), e1 = f2unpack(pe2[1]);
+        le += (e0.x + e0.y) + (e1.x + e1.y);
       }
       // Tokens past the sequence's end (the tile's tail) hold any bytes: the score
       // product is done with this tile (SFULL), so zero those rows of the latent
@@ -592,7 +683,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
           // The score product of a new piece needs that piece's Q in tensor memory
           // (free once this piece's last score product is done): write it first, so
           // that S(j+1) runs while this piece's O is read out and stored.
-          load_q_tmem(c.b);
+          load_q_tmem(row_index(a, c.b));
           fetch_send(j + 1);
           finalize(j);
           begin_piece();
@@ -626,8 +717,8 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cap = a.max_blocks * BS;
   const int64_t G = a.g_half;
-  auto put = [&](int b, int h, int half, const float (&v)[8]) {
-    const int64_t off = ((int64_t)b * a.H + h) * DC + half * DH + lane * 8;
+  auto put = [&](int64_t orow, int h, int half, const float (&v)[8]) {
+    const int64_t off = (orow * a.H + h) * DC + half * DH + lane * 8;
     if (a.out_f32) {
       float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off);
       o[0] = make_float4(v[0], v[1], v[2], v[3]);
@@ -644,14 +735,15 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
   };
   const int row0 = (blockIdx.y * 8 + warp) * kRows;  // first (head, half) row of this warp
   pdl_wait_primary();
-  for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
-    if (clamp_len(__ldg(a.seq_lens + b), cap) > 0) continue;
+  for (int p = blockIdx.x; p < a.Bq; p += gridDim.x) {
+    if (row_len(a, p, cap) > 0) continue;
     const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    const int64_t orow = row_index(a, p);
     for (int q = 0; q < kRows; ++q) {
       const int h = (row0 + q) >> 1, half = (row0 + q) & 1;
       if (h >= a.H) continue;
-      put(b, h, half, z);
-      if (a.lse && half == 0 && lane == 0) a.lse[(int64_t)b * a.H + h] = -INFINITY;
+      put(orow, h, half, z);
+      if (a.lse && half == 0 && lane == 0) a.lse[orow * a.H + h] = -INFINITY;
     }
   }
   const int64_t i = (int64_t)blockIdx.x + 1;  // pair whose range start may cut a sequence
@@ -681,7 +773,7 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
     int np = 0;
     for (; k <= i1 && np < kMaxPieces; ++k) {
       if (k > i0 && cta_tile_start(k + 1, T, G) == cta_tile_start(k, T, G)) continue;
-      slots[np++] = (k == i0) ? (int64_t)b : (int64_t)a.B + k;
+      slots[np++] = (k == i0) ? (int64_t)b : (int64_t)a.Bq + k;
     }
     float l2[kMaxPieces][kRows];
     float4 x[kMaxPieces][kRows][2];
@@ -729,14 +821,14 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
     float v[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) v[c] = acc[q][c] * inv;
-    put((int)b, h, half, v);
+    put(row_index(a, (int)b), h, half, v);
     if (a.lse && half == 0 && lane == 0)
-      a.lse[(int64_t)b * a.H + h] = wsum[q] > 0.f ? (mx[q] + log2f(wsum[q])) * kLn2 : -INFINITY;
+      a.lse[row_index(a, (int)b) * a.H + h] = wsum[q] > 0.f ? (mx[q] + log2f(wsum[q])) * kLn2 : -INFINITY;
   }
 }
 
-size_t mla_workspace_bytes(int B, int g_half) {
-  const int64_t slots = (int64_t)B + g_half;
+size_t mla_workspace_bytes(int rows, int g_half) {
+  const int64_t slots = (int64_t)rows + g_half;
   const size_t o_bytes = (size_t)(slots * 2 * mla::M * mla::DH * 4 + 255) / 256 * 256;
   const size_t l_bytes = (size_t)(slots * 2 * mla::M * 4 + 255) / 256 * 256;
   const size_t b_bytes = (size_t)(g_half * 4 * 8 + 255) / 256 * 256;
@@ -768,8 +860,8 @@ static int mla_resident_pairs(int num_sms) {
 cudaError_t launch_mla_decode(const void* q_nope, const void* q_rope, const void* cache_nope,
                               const void* cache_rope, const int32_t* block_table, int max_blocks,
                               const int32_t* seq_lens, void* out, int out_f32, float* lse, int B,
-                              int H, int64_t num_blocks, float scale, void* ws, int* dev_status,
-                              int num_sms, cudaStream_t stream) {
+                              int q_len, int H, int64_t num_blocks, float scale, void* ws,
+                              int* dev_status, int num_sms, cudaStream_t stream) {
   using namespace mla;
   cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -786,9 +878,13 @@ cudaError_t launch_mla_decode(const void* q_nope, const void* q_rope, const void
   a.H = H;
   a.max_blocks = max_blocks;
   a.out_f32 = out_f32;
+  a.q_len = q_len;
+  a.Bq = B * q_len;
   a.g_half = mla_resident_pairs(num_sms);
+  // A multiple of q_len pairs keeps the rows of a sequence in step (see MlaArgs).
+  if (a.g_half >= q_len) a.g_half -= a.g_half % q_len;
   a.scale_log2 = scale * 1.4426950408889634f;
-  const int64_t slots = (int64_t)B + a.g_half;
+  const int64_t slots = (int64_t)a.Bq + a.g_half;
   const size_t o_bytes = (size_t)(slots * 2 * M * DH * 4 + 255) / 256 * 256;
   a.ws_o = reinterpret_cast<float*>(ws);
   const size_t l_bytes = (size_t)(slots * 2 * M * 4 + 255) / 256 * 256;
@@ -796,7 +892,7 @@ cudaError_t launch_mla_decode(const void* q_nope, const void* q_rope, const void
   a.ws_bnd = reinterpret_cast<long long*>(reinterpret_cast<uint8_t*>(ws) + o_bytes + l_bytes);
 
   CUtensorMap tqn, tqr, tcn, tcr;
-  const uint64_t rows_q = (uint64_t)B * H, rows_c = (uint64_t)num_blocks * BS;
+  const uint64_t rows_q = (uint64_t)a.Bq * H, rows_c = (uint64_t)num_blocks * BS;
   const uint64_t dqn[2] = {DC, rows_q}, sqn[1] = {DC * 2};
   const uint64_t dqr[2] = {DR, rows_q}, sqr[1] = {DR * 2};
   const uint64_t dcn[2] = {DC, rows_c}, scn[1] = {DC * 2};
@@ -811,7 +907,7 @@ cudaError_t launch_mla_decode(const void* q_nope, const void* q_rope, const void
   mla_tc_kernel<<<2 * a.g_half, NTHREADS, SMEM_BYTES, stream>>>(a, tqn, tqr, tcn, tcr);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (B > 0) return launch_dependent(mla_merge_kernel, dim3(a.g_half > 1 ? a.g_half - 1 : 1, 16), dim3(256), 0, stream, a);
+  if (a.Bq > 0) return launch_dependent(mla_merge_kernel, dim3(a.g_half > 1 ? a.g_half - 1 : 1, 16), dim3(256), 0, stream, a);
   return cudaSuccess;
 }
 

@@ -47,7 +47,8 @@ class Workload:
     max_seq_len: int = 0  # arange layout only: tokens per sequence slice
     len_lo: int = 1  # total-length draw bounds (decode) or prior-context bounds (prefill)
     len_hi: int = 1
-    q_lo: int = 1  # prefill: new-token count bounds; spec_decode: q_lo = q_hi = q_len
+    q_lo: int = 1  # prefill: new-token count bounds; spec_decode and multi-row MLA
+                   # (mla_decode with q_hi > 1): q_lo = q_hi = q_len
     q_hi: int = 1
     forced_q1: int = 0  # prefill: leading sequences forced to q_len 1
     seed: int = 0
@@ -84,6 +85,12 @@ def _wl():
             name="mla", kind="mla_decode", batch=128, num_heads=128, num_kv_heads=1,
             head_dim=512, rope_dim=64, scale=inv(192), len_lo=1, len_hi=8192, seed=1003,
             notes="seq_len ~ U[1,8192]; scale 1/sqrt(128+64)"),
+        # MLA decode of 2 new rows per sequence (the verified token plus one draft,
+        # multi-token prediction), bottom-right causal, on the MLA shape above.
+        "mla_spec": Workload(
+            name="mla_spec", kind="mla_decode", batch=128, num_heads=128, num_kv_heads=1,
+            head_dim=512, rope_dim=64, scale=inv(192), len_lo=2, len_hi=8192, q_lo=2, q_hi=2,
+            seed=1006, notes="seq_len ~ U[2,8192] incl. the 2 new rows; scale 1/sqrt(128+64)"),
         # Speculative (MTP) decode on the GQA long-context shape: 4 new rows per
         # sequence (the verified token plus 3 drafts), bottom-right causal.
         "spec_decode": Workload(
@@ -128,7 +135,7 @@ def draw(wl: Workload) -> Draw:
         qlen[: wl.forced_q1] = 1
         seq_lens = prior + qlen
         num_new = qlen
-    elif wl.kind == "spec_decode":
+    elif wl.kind == "spec_decode" or (wl.kind == "mla_decode" and wl.q_hi > 1):
         seq_lens = rng.integers(wl.len_lo, wl.len_hi, size=B, endpoint=True)
         num_new = np.minimum(seq_lens, wl.q_hi)
     elif wl.layout == "arange":
@@ -173,8 +180,9 @@ def values(wl: Workload, d: Draw, device="cpu", poison_null: bool = False) -> di
     T = int(d.num_new.sum())
     out = {}
     if wl.kind == "mla_decode":
-        out["q_nope"] = _randn_bf16((B, H, dh), g, device)
-        out["q_rope"] = _randn_bf16((B, H, wl.rope_dim), g, device)
+        rows = (B, wl.q_hi, H) if wl.q_hi > 1 else (B, H)  # q_hi > 1: q_len rows per sequence
+        out["q_nope"] = _randn_bf16(rows + (dh,), g, device)
+        out["q_rope"] = _randn_bf16(rows + (wl.rope_dim,), g, device)
         out["nope_new"] = _randn_bf16((T, 1, dh), g, device)
         out["rope_new"] = _randn_bf16((T, 1, wl.rope_dim), g, device)
         out["cache_nope"] = _randn_bf16((d.num_blocks, bs, 1, dh), g, device)
