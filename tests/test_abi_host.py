@@ -154,3 +154,23 @@ def test_spec_decode_rejects_unsupported_shapes_before_launch():
     one = lib.pkv_decode_spec_workspace_size(4, 1, 64, 8, 128)
     four = lib.pkv_decode_spec_workspace_size(4, 4, 64, 8, 128)
     assert one == lib.pkv_decode_workspace_size(4, 64, 8, 128) and four > 3 * one
+
+
+def test_mla_spec_rejects_unsupported_shapes_before_launch():
+    lib = load()
+    args = lambda q_len, H, rank, scale=0.1: (None, 1, None, None, None, None, None, None, 16, None, 2,
+                                              q_len, H, rank, 64, 128, 10, scale, None, 0, None, None)
+    # q_len outside 1..4.
+    assert lib.pkv_mla_paged_decode_spec(*args(5, 128, 512)) == -2
+    assert b"q_len" in lib.pkv_last_error()
+    assert lib.pkv_mla_paged_decode_spec(*args(0, 128, 512)) == -2
+    # More heads than the 128-row tile, or a latent width other than 512.
+    assert lib.pkv_mla_paged_decode_spec(*args(2, 129, 512)) == -2
+    assert lib.pkv_mla_paged_decode_spec(*args(2, 128, 256)) == -2
+    # No silent default scale.
+    assert lib.pkv_mla_paged_decode_spec(*args(2, 128, 512, 0.0)) == -1
+    assert b"scale" in lib.pkv_last_error()
+    # Every query row is its own problem: the workspace of q_len rows over B sequences
+    # is the one-row workspace of B * q_len sequences.
+    assert lib.pkv_mla_decode_spec_workspace_size(4, 1, 128) == lib.pkv_mla_decode_workspace_size(4, 128)
+    assert lib.pkv_mla_decode_spec_workspace_size(4, 3, 128) == lib.pkv_mla_decode_workspace_size(12, 128)
