@@ -74,6 +74,25 @@ def decode_bytes(wl: synth.Workload, d: synth.Draw, out_bytes: int = 2) -> dict:
     return {"attention": attn, "write": write, "step": attn + write, "kv": kv}
 
 
+def mla_bytes(wl: synth.Workload, lens: np.ndarray, num_new: np.ndarray) -> dict:
+    """Algorithmic bytes of one MLA step: each latent row (nope + rope) once, q and o of
+    every query row, the table; the write reads and writes each new row once."""
+    lens = np.asarray(lens, dtype=np.int64)
+    Q, B, H = wl.q_hi, len(lens), wl.num_heads
+    row = (wl.head_dim + wl.rope_dim) * 2
+    T = int(np.asarray(num_new).sum())
+    attn = int(lens.sum()) * row + B * Q * H * (wl.head_dim + wl.rope_dim) * 2 \
+        + B * Q * H * wl.head_dim * 2 + int((-(-lens // wl.block_size)).sum()) * 4
+    write = T * row * 2 + T * 4
+    return {"attention": attn, "write": write, "step": attn + write}
+
+
+def prefill_row_flops(wl: synth.Workload, prior: int, r: int) -> int:
+    """Algorithmic flops of query row r (0-based) of a sequence with `prior` cached
+    positions: q.k and p.v over its prior + r + 1 visible keys, for every head."""
+    return (prior + r + 1) * wl.num_heads * 4 * wl.head_dim
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -181,36 +200,126 @@ def time_oracle(wl, d, budget_s: float, max_seq: int, min_s: float = 10.0, max_r
 
 
 # ---------------------------------------------------------------- reference arm
-def run_reference(args):
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
-        return
-    wl = synth.WORKLOADS[args.workload]
-    d = synth.draw(wl)
-    per_step_budget = max(0.05, 150.0 / max(1, args.steps + args.warmup))
+def _decode_leg(wl, d, budget):
+    """Oracle write + decode over a bounded sample of the workload's sequences."""
     sub, sd, vals = oracle_sub_instance(wl, d, min(8, wl.batch))
     t = time.perf_counter()
     oracle_sample_step(sub, sd, vals, [0])
     one = time.perf_counter() - t
-    nseq = int(max(1, min(sub.batch, per_step_budget / max(one, 1e-3))))
+    nseq = int(max(1, min(sub.batch, budget / max(one, 1e-3))))
     seqs = list(range(nseq))
     step_bytes = decode_bytes(sub.scaled(batch=nseq), synth.Draw(
         sd.seq_lens[:nseq], sd.num_new[:nseq], sd.start_pos[:nseq], None, 1, 1))["step"]
+    return (METRIC, "GB/s", 1e9, lambda: oracle_sample_step(sub, sd, vals, seqs), step_bytes,
+            f"{nseq} of {wl.batch} sequences per step")
+
+
+def _mla_leg(wl, d, budget):
+    """Oracle latent-row write + MLA decode (one or q_len rows per sequence) over a
+    bounded sample of the workload's sequences."""
+    from oracle import block_pool_ref as bp
+    from oracle import paged_ref as ref
+
+    nmax = min(8, wl.batch)
+    sub = wl.scaled(batch=nmax)
+    lens = d.seq_lens[:nmax]
+    sd = synth.draw_explicit(sub, lens, d.num_new[:nmax])
+    v = synth.values(sub, sd, "cpu")
+    table = bp.prepare_block_tables(bp.BlockPool(sd.num_blocks, sd.pool_order), lens,
+                                    wl.block_size, 0, sd.max_blocks_per_seq)
+    slots = bp.slot_mapping(table, sd.start_pos, sd.num_new, wl.block_size)
+    bits = {k: synth.bf16_bits(v[k]) for k in ("cache_nope", "cache_rope", "nope_new", "rope_new")}
+    qn, qr = v["q_nope"].double().numpy(), v["q_rope"].double().numpy()
+    fn = ref.mla_spec_decode if wl.q_hi > 1 else ref.mla_decode
+
+    def step(seqs):
+        rows = int(sd.num_new[:len(seqs)].sum())  # the sampled sequences' new rows
+        pn = ref.cache_write(bits["cache_nope"], bits["nope_new"][:rows], slots[:rows])
+        pr = ref.cache_write(bits["cache_rope"], bits["rope_new"][:rows], slots[:rows])
+        fn(qn, qr, pn, pr, table, sd.seq_lens, wl.block_size, wl.scale, batch_indices=seqs)
+
+    t = time.perf_counter()
+    step([0])
+    one = time.perf_counter() - t
+    nseq = int(max(1, min(nmax, budget / max(one, 1e-3))))
+    seqs = list(range(nseq))
+    step_bytes = mla_bytes(wl, sd.seq_lens[:nseq], sd.num_new[:nseq])["step"]
+    return ("MLA absorbed paged decode: achieved HBM GB/s and TFLOP/s", "GB/s", 1e9,
+            lambda: step(seqs), step_bytes, f"{nseq} of {wl.batch} sequences per step")
+
+
+def _prefill_leg(wl, d, budget):
+    """Oracle K/V write + causal prefill of a bounded sample of query rows, spread over
+    the first sequences of the workload (decode rows and prefill rows alike)."""
+    from oracle import block_pool_ref as bp
+    from oracle import paged_ref as ref
+
+    nmax = min(6, wl.batch)  # sequences 0-3 are decode rows, 4-5 prefill rows
+    sub = wl.scaled(batch=nmax)
+    lens = d.seq_lens[:nmax]
+    sd = synth.draw_explicit(sub, lens, d.num_new[:nmax])
+    v = synth.values(sub, sd, "cpu")
+    table = bp.prepare_block_tables(bp.BlockPool(sd.num_blocks, sd.pool_order), lens,
+                                    wl.block_size, 0, sd.max_blocks_per_seq)
+    slots = bp.slot_mapping(table, sd.start_pos, sd.num_new, wl.block_size)
+    bits = {k: synth.bf16_bits(v[k]) for k in ("k_cache", "v_cache", "k_new", "v_new")}
+    q = v["q"].double().numpy()
+    cu = np.cumsum(sd.num_new).astype(np.int64)
+    T = int(cu[-1])
+    seq_of_row = np.searchsorted(cu, np.arange(T), side="right")
+    prior = (sd.seq_lens - sd.num_new).astype(np.int64)
+    starts = cu - sd.num_new
+
+    def flops(rows):
+        return sum(prefill_row_flops(wl, int(prior[seq_of_row[r]]), int(r - starts[seq_of_row[r]]))
+                   for r in rows)
+
+    def step(rows):
+        pk = ref.cache_write(bits["k_cache"], bits["k_new"], slots)
+        pv = ref.cache_write(bits["v_cache"], bits["v_new"], slots)
+        ref.paged_prefill(q, cu, pk, pv, table, sd.seq_lens, wl.block_size, wl.scale, True, rows=rows)
+
+    probe = [T - 1]
+    t = time.perf_counter()
+    step(probe)
+    one = time.perf_counter() - t
+    n = int(max(1, min(T, budget / max(one, 1e-3))))
+    rows = sorted(set(np.linspace(0, T - 1, n).round().astype(int).tolist()))
+    return ("causal paged prefill (mixed with decode rows): achieved TFLOP/s", "TFLOP/s", 1e12,
+            lambda: step(rows), flops(rows),
+            f"{len(rows)} of {T} query rows of the first {nmax} sequences per step")
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    if args.workload not in synth.WORKLOADS or args.kv_dtype != "bf16":
+        what = args.workload + ("" if args.kv_dtype == "bf16" else f" over an {args.kv_dtype} cache")
+        print(json.dumps({"impl": "reference", "unavailable":
+                          f"no oracle timing leg for the {what} workload; its oracle functions "
+                          "are exercised by the tests"}), flush=True)
+        return
+    wl = synth.WORKLOADS[args.workload]
+    d = synth.draw(wl)
+    per_step_budget = max(0.05, args.ref_budget_s / max(1, args.steps + args.warmup))
+    leg = {"mla_decode": _mla_leg, "prefill": _prefill_leg}.get(wl.kind, _decode_leg)
+    metric, unit, scale, step, units, sample = leg(wl, d, per_step_budget)
     for _ in range(args.warmup):
-        oracle_sample_step(sub, sd, vals, seqs)
+        step()
     t = time.perf_counter()
     for _ in range(args.steps):
-        oracle_sample_step(sub, sd, vals, seqs)
+        step()
     el = time.perf_counter() - t
-    value = step_bytes * args.steps / el / 1e9
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+    value = units * args.steps / el / scale
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": unit,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "sample_sequences": nseq, "batch": wl.batch},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{nseq} of {wl.batch} sequences per step"},
-            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+            "config": {"workload": wl.name, "sample": sample, "batch": wl.batch},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -589,11 +698,8 @@ def run_mla(args, dev):
     stream = torch.cuda.current_stream(dev)
     lens = d.seq_lens.astype(np.int64)
     row = (wl.head_dim + wl.rope_dim) * 2
-    T = int(d.num_new.sum())
-    # Algorithmic bytes: each latent row once, q and o of every query row, the table.
-    attn_bytes = int(lens.sum()) * row + wl.batch * Q * wl.num_heads * (wl.head_dim + wl.rope_dim) * 2 \
-        + wl.batch * Q * wl.num_heads * wl.head_dim * 2 + int((-(-lens // 128)).sum()) * 4
-    write_bytes = T * row * 2 + T * 4
+    mb = mla_bytes(wl, lens, d.num_new)
+    attn_bytes, write_bytes = mb["attention"], mb["write"]
     # Positions seen by query row i of sequence b: len_b - Q + 1 + i (at least 0).
     seen = sum(int(np.maximum(lens - Q + 1 + i, 0).sum()) for i in range(Q))
     flops = seen * wl.num_heads * (2 * (wl.head_dim + wl.rope_dim) + 2 * wl.head_dim)
@@ -921,6 +1027,8 @@ def main():
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget-s", type=float, default=150.0,
+                    help="reference arm: seconds of oracle work over the whole run")
     ap.add_argument("--decode-kernel", default="auto", choices=["auto", "cuda_core", "tensor_core"])
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="fp8: decode workloads over an E4M3 cache with per-row scales")

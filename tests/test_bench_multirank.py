@@ -78,3 +78,28 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_zero():
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["value"] > 0 and line["unit"] == "GB/s"
     assert line["e2e"]["value"] == line["value"]
+
+
+@pytest.mark.parametrize("workload,metric,unit", [
+    ("mla_spec", "MLA absorbed paged decode: achieved HBM GB/s and TFLOP/s", "GB/s"),
+    ("mixed_prefill", "causal paged prefill (mixed with decode rows): achieved TFLOP/s", "TFLOP/s"),
+])
+def test_reference_arm_times_the_oracle_on_the_workloads_own_metric(workload, metric, unit):
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", workload, "--steps", "1",
+           "--warmup", "0", "--ref-budget-s", "1"]
+    env = {**os.environ, "CUDA_VISIBLE_DEVICES": "", "OMP_NUM_THREADS": "1"}
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+    assert line["impl"] == "reference" and line["metric"] == metric and line["unit"] == unit
+    assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["value"] == line["value"]
+
+
+def test_reference_arm_without_an_oracle_leg_says_so():
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", "scatter"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300,
+                       env={**os.environ, "CUDA_VISIBLE_DEVICES": ""})
+    assert r.returncode == 0
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and "unavailable" in line
