@@ -108,3 +108,26 @@ def test_mla_spec_workload_full_size():
     out, lse, o_ref, lse_ref = _run(case, rows)
     mx, mean = compare(out, lse, o_ref, lse_ref, rows, "mla spec full")
     print(f"mla spec full: rows {rows} max abs {mx:.2e} mean abs {mean:.2e}")
+
+
+@pytest.mark.parametrize("H,Q", [(1, 4), (40, 2), (40, 3)])
+def test_mla_spec_head_counts_below_the_tile(H, Q):
+    # The 128-row Q box reaches past the last row of q when H < 128; those rows must
+    # neither be read as data nor written.
+    lens = [1, 4, 64, 65, 200, 777, 3000]
+    case = _case(Q, H, lens, seed=50 + H + Q)
+    rows = list(range(len(lens)))
+    out, lse, o_ref, lse_ref = _run(case, rows)
+    compare(out, lse, o_ref, lse_ref, rows, f"mla spec H{H} Q{Q}")
+
+
+def test_mla_spec_many_short_rows_split_across_pairs():
+    # 64 sequences of 0..300 positions at q_len 4: 256 rows, most of them cut by pair
+    # range boundaries (a few tiles per pair), empty rows in between.
+    rng = np.random.default_rng(57)
+    lens = rng.integers(0, 300, size=64)
+    lens[::9] = 0
+    case = _case(4, 128, lens.tolist(), seed=57)
+    rows = list(range(len(lens)))
+    out, lse, o_ref, lse_ref = _run(case, rows)
+    compare(out, lse, o_ref, lse_ref, rows, "mla spec many short rows")
