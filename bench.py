@@ -290,10 +290,69 @@ def _prefill_leg(wl, d, budget):
             f"{len(rows)} of {T} query rows of the first {nmax} sequences per step")
 
 
+def _sized(total: int, budget: float, one_pass) -> int:
+    """Rows of a bounded sample: all of them if one pass fits the budget, else a
+    proportional share (at least 4096)."""
+    t = time.perf_counter()
+    one_pass(total)
+    one = time.perf_counter() - t
+    return total if one <= budget else max(min(total, 4096), int(total * budget / one))
+
+
+def _scatter_leg(args, budget):
+    """Oracle row copy through slot_mapping of K and V rows (the scatter workload)."""
+    import torch
+
+    from oracle import paged_ref as ref
+
+    rows, hkv, d, bs = args.batch or 262144, 8, 128, 128
+    nb = rows // bs
+    g = torch.Generator()
+    g.manual_seed(1005)
+    k = synth.bf16_bits(torch.randn((rows, hkv, d), generator=g).to(torch.bfloat16))
+    v = synth.bf16_bits(torch.randn((rows, hkv, d), generator=g).to(torch.bfloat16))
+    kc = np.zeros((nb, bs, hkv, d), dtype=np.uint16)
+    vc = np.zeros_like(kc)
+    perm = np.random.default_rng(1005).permutation(nb * bs).astype(np.int32)
+
+    def step(n):
+        ref.cache_write(kc, k[:n], perm[:n])
+        ref.cache_write(vc, v[:n], perm[:n])
+
+    n = _sized(rows, budget, step)
+    return ("kv_cache_write scatter: achieved HBM GB/s", "GB/s", 1e9, lambda: step(n),
+            n * hkv * d * 2 * 2 * 2 + n * 4, f"{n} of {rows} rows per step")
+
+
+def _mla_write_leg(args, budget):
+    """Oracle RMSNorm + RoPE + write of latent rows (the mla_write workload)."""
+    from oracle import mla_write_ref as mref
+
+    T = args.batch or 262144
+    nb = -(-T // 128) + 8
+    v = synth.draw_mla_write(T, nb, 1007, device="cpu")
+    bits = {k: synth.bf16_bits(v[k]) for k in ("cache_nope", "cache_rope", "latent", "gamma")}
+    cos, sin = v["cos"].double().numpy(), v["sin"].double().numpy()
+    slots = v["slots"].numpy()
+
+    def step(n):
+        mref.mla_rmsnorm_rope_write(bits["cache_nope"], bits["cache_rope"], bits["latent"][:n],
+                                    bits["gamma"], cos[:n], sin[:n], slots[:n], 512, 1e-6)
+
+    n = _sized(T, budget, step)
+    return ("fused MLA RMSNorm+RoPE cache write: achieved HBM GB/s", "GB/s", 1e9,
+            lambda: step(n), n * (1152 + 512 + 1152 + 4), f"{n} of {T} tokens per step")
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    extra = {"scatter": _scatter_leg, "mla_write": _mla_write_leg}
+    if args.workload in extra and args.kv_dtype == "bf16":
+        per_step_budget = max(0.05, args.ref_budget_s / max(1, args.steps + args.warmup))
+        return _report_reference(args, args.workload, args.batch or 262144,
+                                 *extra[args.workload](args, per_step_budget))
     if args.workload not in synth.WORKLOADS or args.kv_dtype != "bf16":
         what = args.workload + ("" if args.kv_dtype == "bf16" else f" over an {args.kv_dtype} cache")
         print(json.dumps({"impl": "reference", "unavailable":
@@ -304,7 +363,11 @@ def run_reference(args):
     d = synth.draw(wl)
     per_step_budget = max(0.05, args.ref_budget_s / max(1, args.steps + args.warmup))
     leg = {"mla_decode": _mla_leg, "prefill": _prefill_leg}.get(wl.kind, _decode_leg)
-    metric, unit, scale, step, units, sample = leg(wl, d, per_step_budget)
+    _report_reference(args, wl.name, wl.batch, *leg(wl, d, per_step_budget))
+
+
+def _report_reference(args, name, batch, metric, unit, scale, step, units, sample):
+    """Time K oracle steps after W warm-ups and print the reference arm's line."""
     for _ in range(args.warmup):
         step()
     t = time.perf_counter()
@@ -316,7 +379,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "sample": sample, "batch": wl.batch},
+            "config": {"workload": name, "sample": sample, "batch": batch},
             "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,

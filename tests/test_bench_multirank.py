@@ -83,10 +83,14 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_zero():
 @pytest.mark.parametrize("workload,metric,unit", [
     ("mla_spec", "MLA absorbed paged decode: achieved HBM GB/s and TFLOP/s", "GB/s"),
     ("mixed_prefill", "causal paged prefill (mixed with decode rows): achieved TFLOP/s", "TFLOP/s"),
+    ("scatter", "kv_cache_write scatter: achieved HBM GB/s", "GB/s"),
+    ("mla_write", "fused MLA RMSNorm+RoPE cache write: achieved HBM GB/s", "GB/s"),
 ])
 def test_reference_arm_times_the_oracle_on_the_workloads_own_metric(workload, metric, unit):
     cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", workload, "--steps", "1",
            "--warmup", "0", "--ref-budget-s", "1"]
+    if workload in ("scatter", "mla_write"):
+        cmd += ["--batch", "8192"]
     env = {**os.environ, "CUDA_VISIBLE_DEVICES": "", "OMP_NUM_THREADS": "1"}
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
     assert r.returncode == 0, r.stderr[-2000:]
@@ -97,7 +101,7 @@ def test_reference_arm_times_the_oracle_on_the_workloads_own_metric(workload, me
 
 
 def test_reference_arm_without_an_oracle_leg_says_so():
-    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", "scatter"]
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", "fork"]
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300,
                        env={**os.environ, "CUDA_VISIBLE_DEVICES": ""})
     assert r.returncode == 0
