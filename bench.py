@@ -87,6 +87,22 @@ def mla_bytes(wl: synth.Workload, lens: np.ndarray, num_new: np.ndarray) -> dict
     return {"attention": attn, "write": write, "step": attn + write}
 
 
+def fp8_decode_bytes(wl: synth.Workload, lens: np.ndarray, num_new: np.ndarray) -> dict:
+    """Algorithmic bytes of one decode step over the FP8 cache: codes (1 B per element)
+    and one fp32 scale per (token, kv head) row of the visible keys, K and V; q and o;
+    the table; the write reads bf16 rows and writes codes + scales."""
+    lens = np.asarray(lens, dtype=np.int64)
+    B, hkv, dh = len(lens), wl.num_kv_heads, wl.head_dim
+    vis = np.minimum(lens, wl.window) if wl.window > 0 else lens
+    kv = int(vis.sum()) * hkv * (dh + 4) * 2
+    nblk = -(-lens // wl.block_size)
+    live = nblk - (np.maximum(lens - wl.window, 0) // wl.block_size if wl.window > 0 else 0)
+    attn = kv + B * wl.num_heads * dh * 4 + int(live.sum()) * 4 + B * 4
+    new_rows = int(np.asarray(num_new).sum())
+    write = new_rows * hkv * (dh * 2 + dh + 4) * 2 + new_rows * 4
+    return {"attention": attn, "write": write, "step": attn + write, "kv": kv}
+
+
 def prefill_row_flops(wl: synth.Workload, prior: int, r: int) -> int:
     """Algorithmic flops of query row r (0-based) of a sequence with `prior` cached
     positions: q.k and p.v over its prior + r + 1 visible keys, for every head."""
@@ -290,6 +306,37 @@ def _prefill_leg(wl, d, budget):
             f"{len(rows)} of {T} query rows of the first {nmax} sequences per step")
 
 
+def _fp8_leg(wl, d, budget):
+    """Oracle quantising write of the new rows + dequantisation + decode over a bounded
+    sample of the workload's sequences (the cache is quantised once beforehand)."""
+    from oracle import fp8_ref
+    from oracle import paged_ref as ref
+
+    # At most two sequences: the oracle quantises and dequantises whole caches in fp64.
+    sub, sd, vals = oracle_sub_instance(wl, d, min(2, wl.batch))
+    nb, bs, hkv, dh = vals["k_cache"].shape
+    every = np.arange(nb * bs)
+    zc, zs = np.zeros((nb, bs, hkv, dh), np.uint8), np.zeros((nb, hkv, bs), np.float32)
+    kc, ks = fp8_ref.cache_write_fp8(zc, zs, vals["k_cache"].reshape(nb * bs, hkv, dh), every)
+    vc, vs = fp8_ref.cache_write_fp8(zc, zs, vals["v_cache"].reshape(nb * bs, hkv, dh), every)
+
+    def step(seqs):
+        k2, ks2 = fp8_ref.cache_write_fp8(kc, ks, vals["k_new"], vals["slots"])
+        v2, vs2 = fp8_ref.cache_write_fp8(vc, vs, vals["v_new"], vals["slots"])
+        ref.paged_decode(vals["q"], fp8_ref.dequantize_cache(k2, ks2), fp8_ref.dequantize_cache(v2, vs2),
+                         vals["table"], sd.seq_lens, wl.block_size, wl.scale, wl.window,
+                         batch_indices=seqs)
+
+    t = time.perf_counter()
+    step([0])
+    one = time.perf_counter() - t
+    nseq = int(max(1, min(sub.batch, budget / max(one, 1e-3))))
+    seqs = list(range(nseq))
+    step_bytes = fp8_decode_bytes(wl, sd.seq_lens[:nseq], sd.num_new[:nseq])["step"]
+    return ("paged decode over an FP8 E4M3 cache: achieved HBM GB/s", "GB/s", 1e9,
+            lambda: step(seqs), step_bytes, f"{nseq} of {wl.batch} sequences per step")
+
+
 def _sized(total: int, budget: float, one_pass) -> int:
     """Rows of a bounded sample: all of them if one pass fits the budget, else a
     proportional share (at least 4096)."""
@@ -353,6 +400,10 @@ def run_reference(args):
         per_step_budget = max(0.05, args.ref_budget_s / max(1, args.steps + args.warmup))
         return _report_reference(args, args.workload, args.batch or 262144,
                                  *extra[args.workload](args, per_step_budget))
+    if args.kv_dtype == "fp8" and args.workload in ("gqa_long", "swa"):
+        wl = synth.WORKLOADS[args.workload]
+        per_step_budget = max(0.05, args.ref_budget_s / max(1, args.steps + args.warmup))
+        return _report_reference(args, wl.name, wl.batch, *_fp8_leg(wl, synth.draw(wl), per_step_budget))
     if args.workload not in synth.WORKLOADS or args.kv_dtype != "bf16":
         what = args.workload + ("" if args.kv_dtype == "bf16" else f" over an {args.kv_dtype} cache")
         print(json.dumps({"impl": "reference", "unavailable":
@@ -674,12 +725,8 @@ def run_fp8(args, dev):
                      device=dev)
     lens = d.seq_lens.astype(np.int64)
     vis = np.minimum(lens, wl.window) if wl.window > 0 else lens
-    kv = int(vis.sum()) * hkv * (dh + 4) * 2            # codes + scales, K and V
-    nblk = -(-lens // wl.block_size)
-    live = nblk - (np.maximum(lens - wl.window, 0) // wl.block_size if wl.window > 0 else 0)
-    attn = kv + wl.batch * wl.num_heads * dh * 4 + int(live.sum()) * 4 + wl.batch * 4
-    new_rows = int(d.num_new.sum())
-    write = new_rows * hkv * (dh * 2 + dh + 4) * 2 + new_rows * 4
+    fb = fp8_decode_bytes(wl, lens, d.num_new)
+    kv, attn, write = fb["kv"], fb["attention"], fb["write"]
     bf16_kv = int(vis.sum()) * hkv * dh * 2 * 2
     stream = torch.cuda.current_stream(dev)
 
