@@ -36,9 +36,13 @@
 // stays in shared memory (two K-steps from shared memory).
 //
 // Softmax: thread = head row; exp2 in fp32 with the scale folded into log2 units; P
-// rounded to bf16; the normaliser sums the rounded weights. The reference max is
+// rounded to bf16. The output is divided by the sum of the rounded weights, and the
+// log-sum-exp is taken from the sum of the exact fp32 weights. The reference max is
 // raised only when a tile's max exceeds it by more than 8 (log2 units), so P stays
 // below 2^8 and O in TMEM is rescaled only then.
+//
+// Work: one attention problem per (query row, sequence); q_len rows per sequence
+// (1 for plain decode) are walked query-row major, see MlaArgs.
 //
 // Roofline: HBM and tensor both matter. Algorithmic bytes per token = 1152 (nope +
 // rope row); algorithmic flops per token = 128 * (2*576 + 2*512).
@@ -704,13 +708,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
 }
 
 // LSE merge of split MLA pieces: lse = log2 sum_i 2^lse_i, o = sum_i 2^(lse_i - lse) o_i.
-// Only a sequence whose tiles straddle a boundary between two pairs' tile ranges was
-// split. The attention kernel records, per pair, the sequence its range starts in;
-// block (k, g) takes pair i = k + 1 and merges that sequence if pair i's range starts
-// at the sequence's first cut. Warp = two (head, latent half) rows of row group g,
+// Only a row (one query row of one sequence) whose tiles straddle a boundary between
+// two pairs' tile ranges was split. The attention kernel records, per pair, the row its
+// range starts in; block (k, g) takes pair i = k + 1 and merges that row if pair i's
+// range starts at the row's first cut. Warp = two (head, latent half) rows of row group g,
 // lane = 8 consecutive latent columns; the loads of two pieces are issued before any
 // is used. Block (k, g) also writes o = 0, lse = -inf into row group g of the empty
-// sequences b = k (mod gridDim.x).
+// rows p = k (mod gridDim.x).
 __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
   using namespace mla;
   constexpr int kRows = 2, kMaxPieces = 2;
@@ -746,7 +750,7 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
       if (a.lse && half == 0 && lane == 0) a.lse[orow * a.H + h] = -INFINITY;
     }
   }
-  const int64_t i = (int64_t)blockIdx.x + 1;  // pair whose range start may cut a sequence
+  const int64_t i = (int64_t)blockIdx.x + 1;  // pair whose range start may cut a row
   if (i >= G || row0 >= 2 * a.H) return;
   const long long* e = a.ws_bnd + 4 * i;
   const long long b = e[0];
@@ -754,7 +758,7 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(MlaArgs a) {
   const int64_t base = e[1], n = e[2], T = e[3];
   const int64_t t = cta_tile_start(i, T, G);
   const int64_t i0 = cta_of_tile(base, T, G), i1 = cta_of_tile(base + n - 1, T, G);
-  // The sequence's first cut is at tile start(i0 + 1); pairs with empty ranges share
+  // The row's first cut is at tile start(i0 + 1); pairs with empty ranges share
   // that start with the one non-empty pair that holds it, which merges.
   if (t == base || cta_tile_start(i0 + 1, T, G) != t) return;
   int64_t slots[kMaxPieces];
