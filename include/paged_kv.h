@@ -444,8 +444,12 @@ int pkv_paged_attention_decode_fp8(void* out, int32_t out_dtype, float* lse, con
  *     size (pkv_decode_workspace_size(B, H, H_kv, head_dim) tells).
  *   - Allocates nothing and calls no allocating routine.
  *   - The first call on a device, with that device current, looks up the array's
- *     device address (cudaGetSymbolAddress) and caches it; make that first call
- *     before any stream capture.
+ *     device address (cudaGetSymbolAddress) and caches it for the process; make
+ *     that first call before any stream capture. The cached address belongs to the
+ *     device's primary context: it is not valid across cudaDeviceReset or in a
+ *     non-primary driver context.
+ *   - Runs on the current device, with its copy of the array: the pointers and
+ *     `stream` must belong to that device.
  *   - All calls share the one array, which keeps the last call's contents. No part
  *     of it needs to start at zero. Calls that overlap on the GPU (other streams,
  *     other host threads) race on it: serialise them. */
