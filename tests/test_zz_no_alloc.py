@@ -29,24 +29,50 @@ def _check(got, want, lse_got, lse_want):
     assert (lse_got[fin] - lse_want[fin]).abs().max().item() <= 2e-3
 
 
+def _reference(case, q, window, out_dtype):
+    """The workspace-taking entry point on a NaN-filled workspace: any partial the
+    merge read without the attention kernel having written it would show."""
+    wl = case.wl
+    need = api.decode_workspace_size(wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim)
+    ws = torch.full((need // 4 + 64,), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.empty((wl.batch, wl.num_heads), device="cuda")
+    out = api.paged_attention_decode(q, case.v["k_cache"], case.v["v_cache"], case.table,
+                                     case.seq_lens, wl.scale, window, lse=lse, out_dtype=out_dtype,
+                                     workspace=ws)
+    return out, lse
+
+
+def _static(case, q, window, out_dtype):
+    wl = case.wl
+    lse = torch.empty((wl.batch, wl.num_heads), device="cuda")
+    out = api.paged_attention_decode_static(q, case.v["k_cache"], case.v["v_cache"], case.table,
+                                            case.seq_lens, wl.scale, window, lse=lse,
+                                            out_dtype=out_dtype)
+    return out, lse
+
+
 def test_static_scratch_decode_matches_workspace_decode_twice():
-    # Long sequences so that segments are split across CTAs and the partials (the
-    # scratch) are actually written and merged.
-    lens = [20000, 15000, 3000, 1, 0, 9000]
-    wl = synth.WORKLOADS["gqa_long"].scaled(batch=len(lens), seed=21)
-    case = DecodeCase(wl, synth.draw_explicit(wl, lens), poison=True)
-    assert api.decode_workspace_size(wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim) \
-        <= api.STATIC_SCRATCH_BYTES
-    q2 = torch.randn_like(case.v["q"], dtype=torch.float32).to(torch.bfloat16)
-    for q in (case.v["q"], q2):  # two calls in a row; the second reuses the array
-        lse_a = torch.empty((wl.batch, wl.num_heads), device="cuda")
-        lse_b = torch.empty_like(lse_a)
-        want = api.paged_attention_decode(q, case.v["k_cache"], case.v["v_cache"], case.table,
-                                          case.seq_lens, wl.scale, lse=lse_a)
-        got = api.paged_attention_decode_static(q, case.v["k_cache"], case.v["v_cache"], case.table,
-                                                case.seq_lens, wl.scale, lse=lse_b)
+    # Two calls in a row with different batches, lengths (so different cut points of
+    # the split-KV pieces and a different set of scratch slots), window and output
+    # type; long sequences so that segments are split across CTAs and the partials in
+    # the array are written and merged. Each call is checked against the
+    # workspace-taking entry point.
+    first = DecodeCase(synth.WORKLOADS["gqa_long"].scaled(batch=6, seed=21),
+                       synth.draw_explicit(synth.WORKLOADS["gqa_long"].scaled(batch=6, seed=21),
+                                           [20000, 15000, 3000, 1, 0, 9000]), poison=True)
+    wl2 = synth.WORKLOADS["gqa_long"].scaled(batch=3, num_heads=32, seed=23)
+    second = DecodeCase(wl2, synth.draw_explicit(wl2, [7777, 30001, 129]), poison=True)
+    runs = ((first, 0, torch.float32), (second, 4096, torch.bfloat16))
+    for case, window, out_dtype in runs:
+        wl = case.wl
+        assert api.decode_workspace_size(wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim) \
+            <= api.STATIC_SCRATCH_BYTES
+        q = case.v["q"]
+        got, lse_got = _static(case, q, window, out_dtype)
+        want, lse_want = _reference(case, q, window, out_dtype)
         torch.cuda.synchronize()
-        _check(got, want, lse_b, lse_a)
+        assert got.dtype == out_dtype
+        _check(got.float(), want.float(), lse_got, lse_want)
 
 
 def test_static_scratch_decode_rejects_oversized_problems():
