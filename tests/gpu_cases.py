@@ -130,3 +130,113 @@ def sample_rows(seq_lens: np.ndarray, k: int, seed: int) -> list[int]:
     pick = {int(np.argmax(seq_lens)), int(np.argmin(seq_lens))}
     pick |= set(int(x) for x in rng.choice(B, size=k, replace=False))
     return sorted(pick)
+
+
+# ------------------------------------------------------------------ whole-batch oracle
+# Full-size parity compares every row of a workload. The unchanged oracle runs once
+# per sequence (or per run of query rows of one sequence) in a spawn process pool on
+# the host's cores; the caches reach the workers as memory-mapped files.
+def _pool_run(shared: dict, tasks: list, costs):
+    from oracle.pool import OraclePool
+
+    order = np.argsort(-np.asarray(costs, dtype=np.float64), kind="stable")
+    with OraclePool(shared) as pool:
+        res = pool.map([tasks[i] for i in order])
+    out = [None] * len(tasks)
+    for k, i in enumerate(order):
+        out[i] = res[k]
+    print(f"oracle: {len(tasks)} parts on {pool.workers} processes in {pool.seconds:.1f} s")
+    return out
+
+
+def oracle_decode_all(case: DecodeCase, window: int | None = None):
+    """(o, lse) of the oracle for every sequence of a decode or speculative-decode case,
+    on the caches after the oracle's write (case.post)."""
+    from oracle.pool import task
+
+    wl = case.wl
+    window = wl.window if window is None else window
+    q64 = case.v["q"].double().cpu().numpy()
+    fn = "paged_spec_decode" if wl.kind == "spec_decode" else "paged_decode"
+    shared = {"k": case.post["k_cache"], "v": case.post["v_cache"]}
+    tasks = [task(fn, shared_kwargs={"k_cache": "k", "v_cache": "v"}, q=q64[b:b + 1],
+                  block_table=case.table_np[b:b + 1], seq_lens=case.d.seq_lens[b:b + 1],
+                  block_size=wl.block_size, scale=wl.scale, window=window)
+             for b in range(wl.batch)]
+    res = _pool_run(shared, tasks, case.d.seq_lens)
+    return np.concatenate([r[0] for r in res]), np.concatenate([r[1] for r in res])
+
+
+def oracle_mla_all(case: DecodeCase):
+    """(o, lse) of the oracle for every sequence of an MLA case (one or q_len rows)."""
+    from oracle.pool import task
+
+    wl = case.wl
+    qn = case.v["q_nope"].double().cpu().numpy()
+    qr = case.v["q_rope"].double().cpu().numpy()
+    fn = "mla_spec_decode" if qn.ndim == 4 else "mla_decode"
+    shared = {"nope": case.post["cache_nope"], "rope": case.post["cache_rope"]}
+    tasks = [task(fn, shared_kwargs={"cache_nope": "nope", "cache_rope": "rope"},
+                  q_nope=qn[b:b + 1], q_rope=qr[b:b + 1], block_table=case.table_np[b:b + 1],
+                  seq_lens=case.d.seq_lens[b:b + 1], block_size=wl.block_size, scale=wl.scale)
+             for b in range(wl.batch)]
+    res = _pool_run(shared, tasks, case.d.seq_lens)
+    return np.concatenate([r[0] for r in res]), np.concatenate([r[1] for r in res])
+
+
+def oracle_prefill_all(case: DecodeCase, causal: bool = True, rows_per_part: int = 64):
+    """(o, lse) of the oracle for every query row of a prefill case.
+
+    Rows [r0, r1) of a sequence with c prior keys and q new rows form the prefill
+    problem with c + r0 prior keys and r1 - r0 new rows under the bottom-right mask:
+    row r0 + i sees keys j <= c + r0 + i in both. Without the causal mask every row
+    sees all len keys, so the part keeps the sequence's length."""
+    from oracle.pool import task
+
+    wl = case.wl
+    q64 = case.v["q"].double().cpu().numpy()
+    shared = {"k": case.post["k_cache"], "v": case.post["v_cache"]}
+    tasks, costs = [], []
+    begin = 0
+    for b in range(wl.batch):
+        qlen, n = int(case.d.num_new[b]), int(case.d.seq_lens[b])
+        c = n - qlen
+        for r0 in range(0, qlen, rows_per_part):
+            r1 = min(qlen, r0 + rows_per_part)
+            kv = c + r1 if causal else n
+            tasks.append(task("paged_prefill", shared_kwargs={"k_cache": "k", "v_cache": "v"},
+                              q=q64[begin + r0:begin + r1], cu_seqlens_q=np.array([r1 - r0]),
+                              block_table=case.table_np[b:b + 1], seq_lens_kv=np.array([kv]),
+                              block_size=wl.block_size, scale=wl.scale, causal=causal))
+            costs.append((r1 - r0) * kv)
+        begin += qlen
+    res = _pool_run(shared, tasks, costs)
+    return np.concatenate([r[0] for r in res]), np.concatenate([r[1] for r in res])
+
+
+def oracle_fp8_all(base: DecodeCase, codes: dict):
+    """(o, lse, mismatches) of the oracle for every sequence of an FP8 decode case.
+
+    ``codes`` holds host copies of the GPU's FP8 cache right after its writes (before
+    any poisoning): {"kc", "ks", "vc", "vs"}. Each worker quantises the sequence's
+    blocks of the bf16 cache, applies the sequence's quantising write, counts entries
+    that differ from the GPU's, and decodes over the dequantised blocks."""
+    from oracle.pool import task
+
+    wl = base.wl
+    q64 = base.v["q"].double().cpu().numpy()
+    shared = {"kp": base.pre["k_cache"], "vp": base.pre["v_cache"], **codes}
+    kn, vn = synth.bf16_bits(base.v["k_new"]), synth.bf16_bits(base.v["v_new"])
+    ends = np.cumsum(base.d.num_new)
+    starts = ends - base.d.num_new
+    tasks = [task("fp8_sequence", module="tests.oracle_tasks",
+                  shared_kwargs={"k_pre": "kp", "v_pre": "vp", "gpu_kc": "kc", "gpu_ks": "ks",
+                                 "gpu_vc": "vc", "gpu_vs": "vs"},
+                  q_row=q64[b:b + 1], table_row=base.table_np[b], seq_len=int(base.d.seq_lens[b]),
+                  slots=base.slots_np[starts[b]:ends[b]], k_new=kn[starts[b]:ends[b]],
+                  v_new=vn[starts[b]:ends[b]], block_size=wl.block_size, scale=wl.scale,
+                  window=wl.window)
+             for b in range(wl.batch)]
+    res = _pool_run(shared, tasks, base.d.seq_lens)
+    return (np.concatenate([r[0] for r in res]), np.concatenate([r[1] for r in res]),
+            sum(r[2] for r in res))
