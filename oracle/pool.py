@@ -27,6 +27,7 @@ import time
 import numpy as np
 
 _SHARED: dict = {}
+_THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
 
 
 def _init(paths: dict) -> None:
@@ -101,7 +102,18 @@ class OraclePool:
                 np.save(path, np.ascontiguousarray(arr))
                 paths[name] = path
             ctx = mp.get_context("spawn")
-            self.pool = ctx.Pool(self.workers, initializer=_init, initargs=(paths,))
+            # One BLAS thread per worker: the pool already has a process per core,
+            # and numpy's threaded matrix-vector products would oversubscribe them.
+            saved = {k: os.environ.get(k) for k in _THREAD_VARS}
+            os.environ.update({k: "1" for k in _THREAD_VARS})
+            try:
+                self.pool = ctx.Pool(self.workers, initializer=_init, initargs=(paths,))
+            finally:
+                for k, v in saved.items():
+                    if v is None:
+                        os.environ.pop(k, None)
+                    else:
+                        os.environ[k] = v
         except BaseException:
             shutil.rmtree(self.dir, ignore_errors=True)
             raise

@@ -121,17 +121,6 @@ def compare(out: torch.Tensor, lse: torch.Tensor | None, o_ref: np.ndarray, lse_
     return float(err.max()), float(err.mean())
 
 
-def sample_rows(seq_lens: np.ndarray, k: int, seed: int) -> list[int]:
-    """The longest and shortest sequences plus k random others."""
-    B = len(seq_lens)
-    if B <= k + 2:
-        return list(range(B))
-    rng = np.random.default_rng(seed)
-    pick = {int(np.argmax(seq_lens)), int(np.argmin(seq_lens))}
-    pick |= set(int(x) for x in rng.choice(B, size=k, replace=False))
-    return sorted(pick)
-
-
 # ------------------------------------------------------------------ whole-batch oracle
 # Full-size parity compares every row of a workload. The unchanged oracle runs once
 # per sequence (or per run of query rows of one sequence) in a spawn process pool on

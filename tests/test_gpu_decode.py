@@ -6,7 +6,7 @@ import torch
 import synth
 from oracle import paged_ref as ref
 from paged_kv_cache_77_gb300 import api
-from tests.gpu_cases import DecodeCase, compare, sample_rows
+from tests.gpu_cases import DecodeCase, compare, oracle_decode_all
 
 pytestmark = pytest.mark.gpu
 
@@ -80,14 +80,30 @@ def test_decode_bf16_output_and_many_splits(kernel):
     compare(out, lse, o_ref, lse_ref, [0, 1, 2, 3], "bf16 out")
 
 
+_FULL_ORACLE = {}  # workload name -> (o, lse): the inputs are seeded, so both kernels share it
+
+
 @pytest.mark.parametrize("name", ["mha_tiny", "gqa_long", "swa"])
 def test_decode_workloads_full_size(name, kernel):
+    # Every sequence and head of the workload is compared with the oracle, which runs
+    # one sequence per task in a process pool on the host's cores.
     wl = synth.WORKLOADS[name]
     case = DecodeCase(wl)
-    rows = sample_rows(case.d.seq_lens, 4, wl.seed)
-    out, lse, o_ref, lse_ref = _run_decode(case, rows)
+    case.gpu_write()
+    case.oracle_write()
+    lse = torch.full((wl.batch, wl.num_heads), float("nan"), device="cuda")
+    out = api.paged_attention_decode(case.v["q"], case.v["k_cache"], case.v["v_cache"], case.table,
+                                     case.seq_lens, wl.scale, wl.window, lse=lse,
+                                     dev_status=case.status)
+    torch.cuda.synchronize()
+    case.check_write_bit_exact()
+    if name not in _FULL_ORACLE:
+        _FULL_ORACLE[name] = oracle_decode_all(case)
+    o_ref, lse_ref = _FULL_ORACLE[name]
+    rows = list(range(wl.batch))
     mx, mean = compare(out, lse, o_ref, lse_ref, rows, f"{kernel} {name}")
-    print(f"{kernel} {name}: rows {rows} max abs {mx:.2e} mean abs {mean:.2e}")
+    print(f"{kernel} {name}: {len(rows)} of {wl.batch} sequences, max abs {mx:.2e} "
+          f"mean abs {mean:.2e}")
 
 
 def test_worked_slot_marker_row():

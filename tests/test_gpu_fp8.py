@@ -9,7 +9,7 @@ import synth
 from oracle import fp8_ref as f8
 from oracle import paged_ref as ref
 from paged_kv_cache_77_gb300 import api
-from tests.gpu_cases import DecodeCase, compare, sample_rows
+from tests.gpu_cases import DecodeCase, compare, oracle_fp8_all
 
 pytestmark = pytest.mark.gpu
 
@@ -21,7 +21,10 @@ class Fp8Case:
     against the oracle's own quantisation), with the new rows then written by the
     FP8 write and the tails of the last blocks poisoned with NaN codes and scales."""
 
-    def __init__(self, wl, d=None, check_rows=None):
+    def __init__(self, wl, d=None, check_rows=None, whole=False):
+        """``whole``: the oracle's side is left to ``oracle_fp8_all`` (per sequence, in
+        a process pool), which gets host copies of the codes and scales taken here
+        right after the GPU's writes; only the GPU's tails are poisoned."""
         self.base = DecodeCase(wl, d, poison=True)
         c, wl = self.base, self.base.wl
         nb, bs, hkv, dh = c.v["k_cache"].shape
@@ -39,6 +42,12 @@ class Fp8Case:
                                dev_status=self.status)
         torch.cuda.synchronize()
         assert int(self.status.item()) == 0
+        if whole:
+            self.gpu_codes = {"kc": self.kc.cpu().numpy(), "ks": self.ks.cpu().numpy(),
+                              "vc": self.vc.cpu().numpy(), "vs": self.vs.cpu().numpy()}
+            self.codes = None
+            self._poison_tails()
+            return
         # The oracle quantises the same bf16 rows (blocks in `check_rows`' tables, or all
         # but the NaN-poisoned null block) and applies the same write.
         blocks = self._blocks(check_rows)
@@ -83,7 +92,7 @@ class Fp8Case:
             for cc, sc in ((self.kc, self.ks), (self.vc, self.vs)):
                 cc[blk, off:] = 0x7F
                 sc[blk, :, off:] = float("nan")
-            for name in ("k", "v"):
+            for name in (("k", "v") if self.codes is not None else ()):
                 codes, scales = self.codes[name]
                 codes[blk, off:] = 0x7F
                 scales[blk, :, off:] = np.nan
@@ -150,10 +159,20 @@ def test_fp8_write_zero_rows_and_bad_slot():
 
 @pytest.mark.parametrize("name", ["gqa_long", "swa"])
 def test_fp8_decode_workloads_full_size(name):
+    # Every sequence: each pool task quantises the sequence's blocks of the bf16 cache
+    # and applies its quantising write with the oracle, counts codes and scales that
+    # differ from the GPU's (bit for bit), and decodes over the dequantised blocks.
     wl = synth.WORKLOADS[name]
-    d = synth.draw(wl)
-    rows = sample_rows(d.seq_lens, 3, wl.seed)
-    case = Fp8Case(wl, d, check_rows=rows)
-    out, lse, o_ref, lse_ref = case.run(rows)
+    case = Fp8Case(wl, synth.draw(wl), whole=True)
+    c = case.base
+    lse = torch.full((wl.batch, wl.num_heads), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = api.paged_attention_decode_fp8(c.v["q"], case.kc, case.vc, case.ks, case.vs, c.table,
+                                         c.seq_lens, wl.scale, wl.window, lse=lse, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    o_ref, lse_ref, mismatches = oracle_fp8_all(c, case.gpu_codes)
+    assert mismatches == 0, f"{mismatches} FP8 codes or scales differ from the oracle's"
+    rows = list(range(wl.batch))
     mx, mean = compare(out, lse, o_ref, lse_ref, rows, f"fp8 {name}")
-    print(f"fp8 {name}: rows {rows} max abs {mx:.2e} mean abs {mean:.2e}")
+    print(f"fp8 {name}: {len(rows)} of {wl.batch} sequences, max abs {mx:.2e} mean abs {mean:.2e}")

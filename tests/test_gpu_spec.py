@@ -3,7 +3,7 @@
 q_len new rows per sequence are written through slot_mapping (bit-exact against
 the oracle's write), the tails of the last blocks are poisoned with NaN, and the
 tensor-core kernel's output is compared with oracle.paged_spec_decode on every
-row (small cases) or on sampled sequences (the full-size workload)."""
+row, at the small cases and at the full-size workload."""
 import numpy as np
 import pytest
 import torch
@@ -11,7 +11,7 @@ import torch
 import synth
 from oracle import paged_ref as ref
 from paged_kv_cache_77_gb300 import api
-from tests.gpu_cases import DecodeCase, compare, sample_rows
+from tests.gpu_cases import DecodeCase, compare, oracle_decode_all
 
 pytestmark = pytest.mark.gpu
 
@@ -94,13 +94,25 @@ def test_spec_decode_q_len_one_is_the_decode_kernel():
 
 
 @pytest.mark.parametrize("window", [0, 4096])
-def test_spec_decode_full_size_sampled(window):
+def test_spec_decode_full_size(window):
     """The bench's workload (64 sequences up to 32768 tokens, 64 heads over 8 kv
-    heads, 4 new rows each); the oracle checks sampled sequences."""
+    heads, 4 new rows each): every row compared with the oracle, run one sequence
+    per task in a process pool on the host's cores."""
     wl = SPEC.scaled(window=window)
-    d = synth.draw(wl)
-    rows = sample_rows(d.seq_lens, 3, wl.seed)
-    case = DecodeCase(wl, d)
-    out, lse, o_ref, lse_ref = _run(case, rows)
+    case = DecodeCase(wl, synth.draw(wl))
+    case.gpu_write()
+    case.oracle_write()
+    case.check_write_bit_exact()
+    case.poison_tails()
+    lse = torch.full((wl.batch, wl.q_hi, wl.num_heads), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = api.paged_attention_decode_spec(case.v["q"], case.v["k_cache"], case.v["v_cache"],
+                                          case.table, case.seq_lens, wl.scale, wl.window, lse=lse,
+                                          dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    o_ref, lse_ref = oracle_decode_all(case)
+    rows = list(range(wl.batch))
     mx, mean = compare(out, lse, o_ref, lse_ref, rows, f"spec full W{window}")
-    print(f"spec_decode W{window}: rows {rows} max abs {mx:.2e} mean abs {mean:.2e}")
+    print(f"spec_decode W{window}: {wl.batch} of {wl.batch} sequences x {wl.q_hi} rows, "
+          f"max abs {mx:.2e} mean abs {mean:.2e}")
