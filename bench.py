@@ -15,7 +15,9 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -36,6 +38,13 @@ import synth  # noqa: E402
 METRIC = "paged-KV decode attention: achieved HBM GB/s (% of peak), seq-steps/s"
 
 
+# Nominal HBM3e bandwidth of one GB300. The roofline's `peak` is the measured copy
+# bandwidth (MEASURED_PEAKS.json); a copy moves half its bytes each way, and a
+# read-only stream such as decode runs a little faster than that, so `frac` can pass
+# 1.0. The fraction of this nominal figure is reported beside it.
+NOMINAL_HBM_GBS = 7900.0
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -43,6 +52,16 @@ def peaks():
         return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
     except Exception:
         return 6800.0, 1900.0, "fallback"
+
+
+def hbm_roofline(achieved: float, traffic, kernel: str, leg: dict) -> dict:
+    """The HBM roofline object: achieved GB/s against the measured copy peak, and
+    against the nominal bandwidth."""
+    hbm, _, peak_kind = peaks()
+    return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "traffic": traffic, "peak_kind": peak_kind,
+            "frac_of_nominal": achieved / NOMINAL_HBM_GBS, "nominal_peak": NOMINAL_HBM_GBS,
+            "kernel": kernel, **leg}
 
 
 # ---------------------------------------------------------------- byte accounting
@@ -154,7 +173,167 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- roofline leg
+def timed_leg(fn, stream, min_s: float = 1.0, flush=None, max_calls: int = 200000):
+    """Mean CUDA-event time of one fn() call over back-to-back calls that keep the GPU
+    busy for at least min_s, so that the 100 ms clock sampler sees the load.
+
+    With `flush` (a buffer larger than L2), L2 is flushed before every call, outside
+    that call's events. Returns a dict with the mean time in ms, the number of calls
+    and the clocks sampled during the leg, with time x median SM clock (kcycles)."""
+    import torch
+
+    def one_pass(n, with_flush):
+        if not with_flush:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(n):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / n
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for i in range(n):
+            flush.fill_(i & 0xff)
+            evs[i][0].record(stream)
+            fn()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(x.elapsed_time(y) for x, y in evs)
+
+    est = max(one_pass(5, flush is not None), 1e-4)
+    per_call_wall = est
+    if flush is not None:
+        t = time.perf_counter()
+        for i in range(5):
+            flush.fill_(i)
+        torch.cuda.synchronize()
+        per_call_wall += (time.perf_counter() - t) * 1e3 / 5
+    n = int(min(max_calls, max(20, math.ceil(min_s * 1e3 / per_call_wall))))
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    ms = one_pass(n, flush is not None)
+    clocks = sampler.stop()
+    leg = {"call_us": ms * 1e3, "calls": n, "leg_clocks": clocks,
+           "l2": "flushed before every call (512 MB write, not timed)" if flush is not None
+                 else "not flushed: inputs larger than L2"}
+    if clocks.get("sm_mhz"):
+        leg["kcycles_per_call"] = ms * clocks["sm_mhz"]  # ms x MHz = thousands of cycles
+    return ms, leg
+
+
+def kernel_breakdown(fn, calls: int = 10) -> dict:
+    """Device time of each of our kernels over `calls` calls of fn, from CUDA activity
+    records (torch.profiler, no replay or serialisation). A merge kernel launches as a
+    programmatic dependent of the attention kernel and may start before it ends, so
+    its `tail_us` (end of the merge minus end of the kernel launched before it) is the
+    time it adds to the call."""
+    try:
+        import torch
+        from torch.profiler import ProfilerActivity, profile
+
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            for _ in range(calls):
+                fn()
+            torch.cuda.synchronize()
+        recs = []
+        for e in prof.events():
+            if e.device_type == torch.autograd.DeviceType.CUDA and "pkv::" in e.name:
+                short = e.name.split("pkv::", 1)[1].split("(", 1)[0].split("<", 1)[0]
+                recs.append((float(e.time_range.start), float(e.time_range.end), short))
+        recs.sort()
+        out = {}
+        prev_end = None
+        for start, end, name in recs:
+            r = out.setdefault(name, {"launches": 0, "us": [], "tail_us": []})
+            r["launches"] += 1
+            r["us"].append(end - start)
+            if "merge" in name and prev_end is not None:
+                r["tail_us"].append(end - prev_end)
+            if "merge" not in name:
+                prev_end = end
+        res = {}
+        for name, r in out.items():
+            res[name] = {"launches_per_call": r["launches"] / calls,
+                         "mean_us": statistics.mean(r["us"])}
+            if r["tail_us"]:
+                res[name]["tail_us"] = statistics.mean(r["tail_us"])
+        return res
+    except Exception as exc:  # the profiler's CUDA activity tracing may be unavailable
+        return {"error": str(exc)[:200]}
+
+
 # ---------------------------------------------------------------- oracle timing
+def host_info() -> dict:
+    """The CPU the oracle is timed on: logical cores, the cores this process may use,
+    and the CPU model (lscpu, else /proc/cpuinfo)."""
+    info = {"machine": platform.machine(), "nproc": os.cpu_count()}
+    try:
+        info["usable_cores"] = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        info["usable_cores"] = os.cpu_count()
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            fields = {}
+            for line in open("/proc/cpuinfo"):
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip().lower(), v.strip())
+            model = fields.get("model name") or " ".join(
+                f"{k} {fields[k]}" for k in ("cpu implementer", "cpu part") if k in fields) or None
+        except OSError:
+            pass
+    info["cpu_model"] = model
+    return info
+
+
+def time_oracle_all_cores(wl, d, max_seq: int, min_s: float = 10.0, max_reps: int = 5) -> dict:
+    """The same oracle step (write, then decode of every sampled sequence) with the
+    decode of each sequence as one task of a process pool over all usable cores; the
+    write runs in this process, as it does in the one-thread leg."""
+    from oracle import paged_ref as ref
+    from oracle.pool import OraclePool, default_workers, task
+
+    sub, sd, vals = oracle_sub_instance(wl, d, max_seq)
+    post_k = ref.cache_write(vals["k_cache"], vals["k_new"], vals["slots"])
+    post_v = ref.cache_write(vals["v_cache"], vals["v_new"], vals["slots"])
+    fn = "paged_spec_decode" if wl.kind == "spec_decode" else "paged_decode"
+    order = np.argsort(-sd.seq_lens, kind="stable")  # longest first: shorter tail
+    tasks = [task(fn, shared_kwargs={"k_cache": "k", "v_cache": "v"}, q=vals["q"][b:b + 1],
+                  block_table=vals["table"][b:b + 1], seq_lens=sd.seq_lens[b:b + 1],
+                  block_size=wl.block_size, scale=wl.scale, window=wl.window)
+             for b in order]
+    step_bytes = decode_bytes(sub, sd)["step"]
+    workers = default_workers()
+    reps, el = 0, 0.0
+    with OraclePool({"k": post_k, "v": post_v}, workers) as pool:
+        while True:
+            t = time.perf_counter()
+            ref.cache_write(vals["k_cache"], vals["k_new"], vals["slots"])
+            ref.cache_write(vals["v_cache"], vals["v_new"], vals["slots"])
+            pool.map(tasks)
+            el += time.perf_counter() - t
+            reps += 1
+            if el >= min_s or reps >= max_reps:
+                break
+    return {"value": step_bytes * reps / el / 1e9, "unit": "GB/s", "cores": workers,
+            "kind": "oracle", "seq_steps_per_s": max_seq * reps / el,
+            "sample": f"{max_seq} of {wl.batch} sequences x {reps} passes (write in one "
+                      f"process, decode of each sequence a task of a {workers}-process pool, "
+                      f"fp64, one BLAS thread each), {el:.1f} s"}
+
+
 def oracle_sample_step(wl, d, vals, seqs):
     """One oracle pass (write + decode) over the sequences `seqs` of a sub-instance."""
     from oracle import paged_ref as ref
@@ -439,9 +618,18 @@ def _report_reference(args, name, batch, metric, unit, scale, step, units, sampl
 
 
 def cpu_baseline_child(args):
+    """The oracle timed on this host: one thread over a sample of the sequences, then
+    a process pool over all usable cores on (up to) every sequence of the workload."""
     wl = synth.WORKLOADS[args.workload]
     d = synth.draw(wl)
-    print(json.dumps(time_oracle(wl, d, budget_s=15.0, max_seq=min(8, wl.batch))), flush=True)
+    line = time_oracle(wl, d, budget_s=15.0, max_seq=min(8, wl.batch))
+    line["host"] = host_info()
+    if not args.no_all_cores:
+        try:
+            line["all_cores"] = time_oracle_all_cores(wl, d, max_seq=min(wl.batch, 128))
+        except Exception as exc:
+            line["all_cores"] = {"value": None, "error": str(exc)[:300]}
+    print(json.dumps(line), flush=True)
 
 
 # ---------------------------------------------------------------- our arm
@@ -499,20 +687,72 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     api.set_decode_kernel({"auto": api.KERNEL_AUTO, "cuda_core": api.KERNEL_CUDA_CORE,
                            "tensor_core": api.KERNEL_TENSOR_CORE}[args.decode_kernel])
+    line = run_workload(args, dev, world, rank)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_workload(args, dev, world: int = 1, rank: int = 0):
+    """The line of one workload (every rank computes it; rank 0 prints it)."""
     if args.kv_dtype == "fp8":
         if args.workload not in ("gqa_long", "swa"):
             raise SystemExit("--kv-dtype fp8 applies to the gqa_long and swa workloads")
         return run_fp8(args, dev)
-    if args.workload == "scatter":
-        return run_scatter(args, dev)
-    if args.workload == "fork":
-        return run_fork(args, dev)
-    if args.workload == "mla_write":
-        return run_mla_write(args, dev)
-    if args.workload in ("mla", "mla_spec"):
-        return run_mla(args, dev)
-    if args.workload == "mixed_prefill":
-        return run_prefill(args, dev)
+    other = {"scatter": run_scatter, "fork": run_fork, "mla_write": run_mla_write,
+             "mla": run_mla, "mla_spec": run_mla, "mixed_prefill": run_prefill}
+    if args.workload in other:
+        return other[args.workload](args, dev)
+    return run_decode(args, dev, world, rank)
+
+
+# The other workloads, run briefly after the default one so that a single default run
+# records every configuration: (label, workload, kv dtype).
+PER_CONFIG = (("mha_tiny", "mha_tiny", "bf16"), ("swa", "swa", "bf16"),
+              ("spec_decode", "spec_decode", "bf16"), ("mla", "mla", "bf16"),
+              ("mla_spec", "mla_spec", "bf16"), ("mixed_prefill", "mixed_prefill", "bf16"),
+              ("gqa_long_fp8", "gqa_long", "fp8"), ("scatter", "scatter", "bf16"),
+              ("mla_write", "mla_write", "bf16"), ("fork", "fork", "bf16"))
+
+
+def per_config(args, dev) -> dict:
+    """Short runs of the other workloads (20 steps, 3 warm-ups, and a roofline leg of at
+    least a second each): their metric, the call's time, the roofline fraction, the L2
+    condition, the clocks and the per-kernel split."""
+    import torch
+
+    res = {}
+    for label, name, kv in PER_CONFIG:
+        sub = argparse.Namespace(**{**vars(args), "workload": name, "kv_dtype": kv, "batch": 0,
+                                    "steps": min(args.steps, 20), "warmup": 3,
+                                    "no_cpu_baseline": True, "no_per_config": True})
+        try:
+            line = run_workload(sub, dev)
+        except Exception as exc:
+            res[label] = {"error": str(exc)[:300]}
+            continue
+        finally:
+            torch.cuda.empty_cache()
+        r = line["roofline"]
+        keep = ("bound", "achieved", "peak", "unit", "frac", "peak_kind", "frac_of_nominal",
+                "traffic", "call_us", "calls", "l2", "kcycles_per_call", "kernels")
+        res[label] = {"metric": line["metric"], "value": line["value"], "unit": line["unit"],
+                      "ms_per_step": line["ms_per_step"], "config": line["config"]["workload"],
+                      "roofline": {k: r[k] for k in keep if k in r},
+                      "sm_mhz": (r.get("leg_clocks") or {}).get("sm_mhz"),
+                      "clock_reasons": (r.get("leg_clocks") or {}).get("reasons")}
+        if "tensor" in line:
+            res[label]["tensor"] = line["tensor"]
+    return res
+
+
+def run_decode(args, dev, world: int = 1, rank: int = 0):
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_cache_77_gb300 import api
+
     wl = synth.WORKLOADS[args.workload]
     if args.batch:
         wl = wl.scaled(batch=args.batch)
@@ -590,19 +830,11 @@ def run_ours(args):
     ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
     # The attention call's own time, for the roofline: back-to-back calls with no cache
-    # write between them. (In the step loop the attention kernel launches as a
-    # programmatic dependent of the write kernel and may start before the event placed
-    # between them, so events around it there would miss part of its run.)
-    ev_att = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    for i in range(args.steps):
-        if flush is not None:
-            flush.fill_(i & 0xff)
-        ev_att[i][0].record(stream)
-        attend(v["q"])
-        ev_att[i][1].record(stream)
-    torch.cuda.synchronize()
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_att)
+    # write between them, for at least a second. (In the step loop the attention kernel
+    # launches as a programmatic dependent of the write kernel and may start before the
+    # event placed between them, so events around it there would miss part of its run.)
+    dec_ms, leg = timed_leg(lambda: attend(v["q"]), stream, flush=flush)
+    breakdown = kernel_breakdown(lambda: attend(v["q"]))
     l2_note = ("inputs larger than L2 (KV cache %.2f GB vs 129 MB L2)" % (nbytes["kv"] / 1e9)
                if flush is None else
                "L2 flushed before every timed step (512 MB write, not timed); KV cache %.3f GB"
@@ -662,19 +894,21 @@ def run_ours(args):
                    "step_bytes": nbytes["step"],
                    "l2": l2_note,
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": traffic_from_profiles(f"decode:{wl.name}"),
-                     "kernel": f"paged_attention_decode{'_spec' if spec else ''} "
-                               "(split-KV attention + merge), "
-                               f"{dec_ms * 1e3:.1f} us per call",
-                     "decode_kernel": ["auto", "cuda_core", "tensor_core"][api.get_decode_kernel()],
-                     "peak_kind": peak_kind},
+        "roofline": {**hbm_roofline(
+            achieved, traffic_from_profiles(f"decode:{wl.name}"),
+            f"paged_attention_decode{'_spec' if spec else ''} (split-KV attention + merge), "
+            f"{dec_ms * 1e3:.1f} us per call", leg),
+            "decode_kernel": ["auto", "cuda_core", "tensor_core"][api.get_decode_kernel()],
+            "kernels": breakdown},
         "e2e": {"value": nbytes["step"] * world / e2e_s / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": e2e_s * 1e3},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
+    if rank == 0 and world == 1 and wl.name == "gqa_long" and not args.batch \
+            and not args.no_per_config:
+        line["per_config"] = per_config(args, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child",
                             "--workload", wl.name], capture_output=True, text=True,
@@ -684,10 +918,7 @@ def run_ours(args):
             line["cpu_baseline"] = json.loads(r.stdout.strip().splitlines()[-1])
         except Exception:
             line["cpu_baseline"] = {"value": None, "error": r.stderr[-300:]}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    return line
 
 
 def run_fp8(args, dev):
@@ -750,21 +981,15 @@ def run_fp8(args, dev):
         step()
     t1.record(stream)
     torch.cuda.synchronize()
-    # The attention call's own time: back-to-back calls (in the step loop it may start
-    # before an event placed after the write, as a programmatic dependent of it).
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        attend()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
     clocks = sampler.stop()
     ms = t0.elapsed_time(t1) / args.steps
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    hbm, _, peak_kind = peaks()
+    # The attention call's own time: back-to-back calls for at least a second (in the
+    # step loop it may start before an event placed after the write, as a programmatic
+    # dependent of it).
+    dec_ms, leg = timed_leg(attend, stream)
+    breakdown = kernel_breakdown(attend)
     achieved = attn / (dec_ms * 1e-3) / 1e9
-    print(json.dumps({
+    return {
         "metric": "paged decode over an FP8 E4M3 cache: achieved HBM GB/s", "impl": "ours",
         "value": (attn + write) / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -775,10 +1000,10 @@ def run_fp8(args, dev):
                    "kv_bytes": kv, "kv_bytes_if_bf16": bf16_kv,
                    "decode_us_per_call": dec_ms * 1e3,
                    "l2": "inputs larger than L2 (%.2f GB of codes and scales)" % (kv / 1e9)},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": traffic_from_profiles(f"fp8:{wl.name}"), "peak_kind": peak_kind,
-                     "kernel": f"paged_attention_decode_fp8 (attention + merge), {dec_ms * 1e3:.1f} us"},
-        "gpu_launches": 3 * args.steps, "clocks": clocks}), flush=True)
+        "roofline": {**hbm_roofline(achieved, traffic_from_profiles(f"fp8:{wl.name}"),
+                                    f"paged_attention_decode_fp8 (attention + merge), "
+                                    f"{dec_ms * 1e3:.1f} us", leg), "kernels": breakdown},
+        "gpu_launches": 3 * args.steps, "clocks": clocks}
 
 
 def run_mla(args, dev):
@@ -832,25 +1057,25 @@ def run_mla(args, dev):
     sampler = ClockSampler(dev.index or 0)
     sampler.start()
     time.sleep(0.3)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t0.record(stream)
     for i in range(args.steps):
         write()
-        evs[i][0].record(stream)
         attend()
-        evs[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
     ms = t0.elapsed_time(t1) / args.steps
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    # The attention call alone, back to back for at least a second (in the step loop it
+    # launches as a programmatic dependent of the write and may start before an event
+    # placed between them).
+    dec_ms, leg = timed_leg(attend, stream)
+    breakdown = kernel_breakdown(attend)
     hbm, tf, peak_kind = peaks()
     ach = attn_bytes / (dec_ms * 1e-3) / 1e9
     tfl = flops / (dec_ms * 1e-3) / 1e12
-    print(json.dumps({
+    return {
         "metric": "MLA absorbed paged decode: achieved HBM GB/s and TFLOP/s", "value":
         (attn_bytes + write_bytes) / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -860,15 +1085,14 @@ def run_mla(args, dev):
                                f"{wl.head_dim} + rope {wl.rope_dim} bs {wl.block_size}",
                    "seq_lens": f"U[{wl.len_lo},{wl.len_hi}] (sum {int(lens.sum())})",
                    "l2": "inputs larger than L2 (latent cache %.2f GB)" % (int(lens.sum()) * row / 1e9)},
-        "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                     "traffic": traffic_from_profiles(f"mla:{wl.name}"),
-                     "kernel": f"mla_paged_decode{'_spec' if Q > 1 else ''} (attention + merge), "
-                               f"{dec_ms * 1e3:.1f} us per call",
-                     "peak_kind": peak_kind},
+        "roofline": {**hbm_roofline(ach, traffic_from_profiles(f"mla:{wl.name}"),
+                                    f"mla_paged_decode{'_spec' if Q > 1 else ''} (attention + "
+                                    f"merge), {dec_ms * 1e3:.1f} us per call", leg),
+                     "kernels": breakdown},
         "tensor": {"achieved_tflops": tfl, "peak_tflops": tf, "frac": tfl / tf,
                    "note": "algorithmic flops; each score product is split along K across a CTA pair, none is computed twice"
                            + ("; each query row reads the latent rows it sees, repeats are meant to hit L2" if Q > 1 else "")},
-        "gpu_launches": 3 * args.steps, "clocks": clocks}), flush=True)
+        "gpu_launches": 3 * args.steps, "clocks": clocks}
 
 
 def run_prefill(args, dev):
@@ -915,24 +1139,21 @@ def run_prefill(args, dev):
     sampler = ClockSampler(dev.index or 0)
     sampler.start()
     time.sleep(0.3)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t0.record(stream)
     for i in range(args.steps):
         write()
-        evs[i][0].record(stream)
         attend()
-        evs[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
     ms = t0.elapsed_time(t1) / args.steps
-    pf_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    pf_ms, leg = timed_leg(attend, stream)  # the prefill call alone, for at least a second
+    breakdown = kernel_breakdown(attend)
     hbm, tf, peak_kind = peaks()
     tfl = flops / (pf_ms * 1e-3) / 1e12
-    print(json.dumps({
+    return {
         "metric": "causal paged prefill (mixed with decode rows): achieved TFLOP/s",
         "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -949,8 +1170,8 @@ def run_prefill(args, dev):
         "roofline": {"bound": "tensor", "achieved": tfl, "peak": tf, "unit": "TFLOP/s",
                      "frac": tfl / tf, "traffic": traffic_from_profiles("prefill:mixed_prefill"),
                      "kernel": f"paged_attention_prefill (attention + merge), {pf_ms * 1e3:.1f} us",
-                     "peak_kind": peak_kind + " bf16 dense burst"},
-        "gpu_launches": 3 * args.steps, "clocks": clocks}), flush=True)
+                     "peak_kind": peak_kind + " bf16 dense burst", **leg, "kernels": breakdown},
+        "gpu_launches": 3 * args.steps, "clocks": clocks}
 
 
 def run_scatter(args, dev):
@@ -986,19 +1207,18 @@ def run_scatter(args, dev):
     torch.cuda.synchronize()
     clocks = sampler.stop()
     ms = t0.elapsed_time(t1) / args.steps
-    hbm, _, peak_kind = peaks()
     gbs = nbytes / (ms * 1e-3) / 1e9
-    print(json.dumps({
+    leg_ms, leg = timed_leg(lambda: api.kv_cache_write(kc, vc, k, v, slots), stream)
+    return {
         "metric": "kv_cache_write scatter: achieved HBM GB/s", "value": gbs, "unit": "GB/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": f"scatter: {rows} rows x (K+V) H_kv {hkv} d {d}, random slots",
                    "l2": "inputs larger than L2 (%.2f GB moved per step)" % (nbytes / 1e9)},
-        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": gbs / hbm, "traffic": traffic_from_profiles("write:scatter"),
-                     "peak_kind": peak_kind},
-        "gpu_launches": args.steps, "clocks": clocks}), flush=True)
+        "roofline": hbm_roofline(nbytes / (leg_ms * 1e-3) / 1e9, traffic_from_profiles("write:scatter"),
+                                 f"kv_cache_write, {leg_ms * 1e3:.1f} us per call", leg),
+        "gpu_launches": args.steps, "clocks": clocks}
 
 
 def run_fork(args, dev):
@@ -1059,9 +1279,14 @@ def run_fork(args, dev):
     torch.cuda.synchronize()
     clocks = sampler.stop()
     ms = t0.elapsed_time(t1) / args.steps
-    hbm, _, peak_kind = peaks()
     gbs = nbytes / (ms * 1e-3) / 1e9
-    print(json.dumps({
+
+    def both():
+        api.copy_blocks(kc, src, dst)
+        api.copy_blocks(vc, src, dst)
+
+    leg_ms, leg = timed_leg(both, stream)
+    return {
         "metric": "fork block copy: achieved HBM GB/s", "value": gbs, "unit": "GB/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -1072,9 +1297,9 @@ def run_fork(args, dev):
                    "l2": "inputs larger than L2 (%.2f GB moved per step)" % (nbytes / 1e9),
                    "host_us_per_fork": t_fork * 1e6, "host_us_per_prefill_allocate": t_alloc * 1e6,
                    "host_us_per_decode_allocate": t_dec * 1e6},
-        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": gbs / hbm, "traffic": None, "peak_kind": peak_kind},
-        "gpu_launches": 2 * args.steps, "clocks": clocks}), flush=True)
+        "roofline": hbm_roofline(nbytes / (leg_ms * 1e-3) / 1e9, None,
+                                 f"copy_blocks on K and V, {leg_ms * 1e3:.1f} us per fork", leg),
+        "gpu_launches": 2 * args.steps, "clocks": clocks}
 
 
 def run_mla_write(args, dev):
@@ -1110,18 +1335,18 @@ def run_mla_write(args, dev):
     torch.cuda.synchronize()
     clocks = sampler.stop()
     ms = t0.elapsed_time(t1) / args.steps
-    hbm, _, peak_kind = peaks()
     gbs = nbytes / (ms * 1e-3) / 1e9
-    print(json.dumps({
+    leg_ms, leg = timed_leg(step, stream)
+    return {
         "metric": "fused MLA RMSNorm+RoPE cache write: achieved HBM GB/s", "value": gbs,
         "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"mla_write: {T} tokens x (latent 512 + rope 64), random slots",
                    "l2": "inputs larger than L2 (%.2f GB moved per step)" % (nbytes / 1e9)},
-        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": gbs / hbm, "traffic": None, "peak_kind": peak_kind},
-        "gpu_launches": args.steps, "clocks": clocks}), flush=True)
+        "roofline": hbm_roofline(nbytes / (leg_ms * 1e-3) / 1e9, None,
+                                 f"mla_rmsnorm_rope_write, {leg_ms * 1e3:.1f} us per call", leg),
+        "gpu_launches": args.steps, "clocks": clocks}
 
 
 def main():
@@ -1143,6 +1368,10 @@ def main():
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="fp8: decode workloads over an E4M3 cache with per-row scales")
     ap.add_argument("--cpu-baseline-child", action="store_true")
+    ap.add_argument("--no-all-cores", action="store_true",
+                    help="CPU baseline: skip the leg that runs the oracle on every core")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="default workload: skip the short runs of the other workloads")
     args = ap.parse_args()
     if args.cpu_baseline_child:
         cpu_baseline_child(args)

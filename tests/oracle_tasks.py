@@ -4,6 +4,7 @@ Imports numpy and the oracle only (the workers are spawned processes). Each step
 an oracle function, called in the order the test applies them on the GPU:
 
 1. quantise the sequence's live blocks of the bf16 cache (``fp8_ref.quantize_rows``);
+   the null block, which the GPU test fills with NaN, is never quantised or read;
 2. the quantising write of the sequence's new rows (``fp8_ref.cache_write_fp8``);
 3. compare codes and scales bit for bit with the GPU's;
 4. NaN codes and scales past the sequence's end in its last block (never read);
@@ -38,9 +39,14 @@ def fp8_sequence(k_pre, v_pre, gpu_kc, gpu_ks, gpu_vc, gpu_vs, q_row, table_row,
     mismatches = 0
     dq = []
     for pre, new, gc, gs in ((k_pre, k_new, gpu_kc, gpu_ks), (v_pre, v_new, gpu_vc, gpu_vs)):
-        sub = np.asarray(pre[phys])
-        codes, scales = f8.quantize_rows(sub)
-        scales = scales.transpose(0, 2, 1)
+        # The live blocks are quantised; the compact block 0 stands for the null block
+        # (its rows are only ever masked), with zero codes and scales.
+        live_codes, live_scales = f8.quantize_rows(np.asarray(pre[phys[1:]]))
+        codes = np.zeros((len(phys),) + live_codes.shape[1:], dtype=live_codes.dtype)
+        codes[1:] = live_codes
+        scales = np.zeros((len(phys), live_scales.shape[2], live_scales.shape[1]),
+                          dtype=live_scales.dtype)
+        scales[1:] = live_scales.transpose(0, 2, 1)
         # new rows of this sequence, their slots remapped to the compact cache
         sub_slots = []
         for s in np.asarray(slots).reshape(-1):

@@ -16,7 +16,7 @@ from tests import gpu_cases as gc
 
 def _cpu_case(wl, lens, num_new=None):
     d = synth.draw_explicit(wl, lens, num_new)
-    v = synth.values(wl, d, "cpu")
+    v = synth.values(wl, d, "cpu", poison_null=True)  # as on the GPU: the null block is NaN
     win = wl.window + wl.q_hi - 1 if wl.kind == "spec_decode" and wl.window > 0 else wl.window
     table = bp.prepare_block_tables(bp.BlockPool(d.num_blocks, d.pool_order), d.seq_lens,
                                     wl.block_size, win, d.max_blocks_per_seq)
@@ -109,8 +109,12 @@ def test_pool_fp8_sequence_equals_whole_cache_oracle(window):
     c = _cpu_case(wl, [700, 1, 300])
     codes = {}
     for n, pre, new in (("k", c.pre["k_cache"], c.v["k_new"]), ("v", c.pre["v_cache"], c.v["v_new"])):
-        q8, s8 = f8.quantize_rows(pre)
-        q8, s8 = f8.cache_write_fp8(q8, s8.transpose(0, 2, 1), synth.bf16_bits(new), c.slots_np)
+        # every block but the NaN null block quantised; the null block holds zeros
+        lq, ls = f8.quantize_rows(pre[1:])
+        q8 = np.zeros(pre.shape, dtype=np.uint8)
+        s8 = np.zeros((pre.shape[0], pre.shape[2], pre.shape[1]), dtype=np.float32)
+        q8[1:], s8[1:] = lq, ls.transpose(0, 2, 1)
+        q8, s8 = f8.cache_write_fp8(q8, s8, synth.bf16_bits(new), c.slots_np)
         codes[n + "c"], codes[n + "s"] = q8, s8
     o, lse, bad = gc.oracle_fp8_all(c, codes)
     assert bad == 0
