@@ -797,7 +797,7 @@ def run_decode(args, dev, world: int = 1, rank: int = 0):
     torch.cuda.synchronize()
 
     # ---- device-resident timing: K steps, events around each decode call too
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(dev.index or 0)
     sampler.start()
     time.sleep(0.3)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
