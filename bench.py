@@ -224,6 +224,9 @@ def timed_leg(fn, stream, min_s: float = 1.0, flush=None, max_calls: int = 20000
     return ms, leg
 
 
+_PROFILER_WARM = False
+
+
 def kernel_breakdown(fn, calls: int = 10) -> dict:
     """Device time of each of our kernels over `calls` calls of fn, from CUDA activity
     records (torch.profiler, no replay or serialisation). A merge kernel launches as a
@@ -234,6 +237,12 @@ def kernel_breakdown(fn, calls: int = 10) -> dict:
         import torch
         from torch.profiler import ProfilerActivity, profile
 
+        global _PROFILER_WARM
+        if not _PROFILER_WARM:  # the first profiled region of a process can come back empty
+            with profile(activities=[ProfilerActivity.CUDA]):
+                fn()
+                torch.cuda.synchronize()
+            _PROFILER_WARM = True
         with profile(activities=[ProfilerActivity.CUDA]) as prof:
             for _ in range(calls):
                 fn()
@@ -1209,6 +1218,7 @@ def run_scatter(args, dev):
     ms = t0.elapsed_time(t1) / args.steps
     gbs = nbytes / (ms * 1e-3) / 1e9
     leg_ms, leg = timed_leg(lambda: api.kv_cache_write(kc, vc, k, v, slots), stream)
+    leg["kernels"] = kernel_breakdown(lambda: api.kv_cache_write(kc, vc, k, v, slots))
     return {
         "metric": "kv_cache_write scatter: achieved HBM GB/s", "value": gbs, "unit": "GB/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -1286,6 +1296,7 @@ def run_fork(args, dev):
         api.copy_blocks(vc, src, dst)
 
     leg_ms, leg = timed_leg(both, stream)
+    leg["kernels"] = kernel_breakdown(both)
     return {
         "metric": "fork block copy: achieved HBM GB/s", "value": gbs, "unit": "GB/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -1337,6 +1348,7 @@ def run_mla_write(args, dev):
     ms = t0.elapsed_time(t1) / args.steps
     gbs = nbytes / (ms * 1e-3) / 1e9
     leg_ms, leg = timed_leg(step, stream)
+    leg["kernels"] = kernel_breakdown(step)
     return {
         "metric": "fused MLA RMSNorm+RoPE cache write: achieved HBM GB/s", "value": gbs,
         "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
