@@ -183,6 +183,14 @@ def timed_leg(fn, stream, min_s: float = 1.0, flush=None, max_calls: int = 20000
     and the clocks sampled during the leg, with time x median SM clock (kcycles)."""
     import torch
 
+    if BARE:  # profiling runs: no long leg (every launch is slow under a profiler)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b), {"call_us": a.elapsed_time(b) * 1e3, "calls": 1, "bare": True}
+
     def one_pass(n, with_flush):
         if not with_flush:
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -225,6 +233,9 @@ def timed_leg(fn, stream, min_s: float = 1.0, flush=None, max_calls: int = 20000
 
 
 _PROFILER_WARM = False
+# --bare: the timed steps only, one call per leg, no activity profiler, no end-to-end
+# leg, no other workloads, no CPU baseline (a short run to capture under ncu).
+BARE = False
 
 
 def kernel_breakdown(fn, calls: int = 10) -> dict:
@@ -233,6 +244,8 @@ def kernel_breakdown(fn, calls: int = 10) -> dict:
     programmatic dependent of the attention kernel and may start before it ends, so
     its `tail_us` (end of the merge minus end of the kernel launched before it) is the
     time it adds to the call."""
+    if BARE:
+        return {}
     try:
         import torch
         from torch.profiler import ProfilerActivity, profile
@@ -877,13 +890,16 @@ def run_decode(args, dev, world: int = 1, rank: int = 0):
         torch.cuda.current_stream().synchronize()
         return time.perf_counter() - t
 
-    for _ in range(max(3, args.warmup)):
-        e2e_step()
-    e2e_steps = max(10, args.steps // 4)
-    if world > 1:
-        dist.barrier()
-    e2e_s = sum(e2e_step() for _ in range(e2e_steps)) / e2e_steps
-    e2e_s = max_over_ranks(e2e_s, dev)
+    if BARE:
+        e2e_s = float("nan")
+    else:
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        e2e_steps = max(10, args.steps // 4)
+        if world > 1:
+            dist.barrier()
+        e2e_s = sum(e2e_step() for _ in range(e2e_steps)) / e2e_steps
+        e2e_s = max_over_ranks(e2e_s, dev)
 
     hbm, _, peak_kind = peaks()
     value = job_throughput(nbytes["step"], world, ms_step) / 1e9
@@ -1384,7 +1400,14 @@ def main():
                     help="CPU baseline: skip the leg that runs the oracle on every core")
     ap.add_argument("--no-per-config", action="store_true",
                     help="default workload: skip the short runs of the other workloads")
+    ap.add_argument("--bare", action="store_true",
+                    help="only the timed steps (one call per roofline leg, no profiler, no e2e, "
+                         "no other workloads, no CPU baseline): a short run to capture under ncu")
     args = ap.parse_args()
+    if args.bare:
+        global BARE
+        BARE = True
+        args.no_cpu_baseline = args.no_per_config = True
     if args.cpu_baseline_child:
         cpu_baseline_child(args)
     elif args.impl == "reference":
