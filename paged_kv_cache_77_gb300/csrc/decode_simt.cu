@@ -280,31 +280,66 @@ __global__ void __launch_bounds__(512) decode_merge_kernel(DecodeArgs a) {
   };
   const int64_t i0 = n ? cta_of_tile(base, T, G) : 0, i1 = n ? cta_of_tile(base + n - 1, T, G) : 0;
   if (n > 0 && i0 == i1) return;  // finished by the attention kernel
+  // The pieces' workspace slots, found before the wait (they depend on the inputs
+  // only), so that after it every piece's loads are issued at once.
+  constexpr int kMaxPieces = 8;
+  auto slot_of = [&](int64_t i) { return (i == i0) ? (int64_t)seg : (int64_t)a.B * a.Hkv + i; };
+  int64_t slots[kMaxPieces];
+  int np = 0;
+  for (int64_t i = i0; n > 0 && i <= i1; ++i) {
+    if (i > i0 && cta_tile_start(i + 1, T, G) == cta_tile_start(i, T, G)) continue;  // empty CTA
+    if (np < kMaxPieces) slots[np] = slot_of(i);
+    ++np;
+  }
   pdl_wait_primary();
   if (n == 0) {
     put(make_float4(0.f, 0.f, 0.f, 0.f));
     if (a.lse && lane == 0) a.lse[row] = -INFINITY;
     return;
   }
-  auto slot_of = [&](int64_t i) { return (i == i0) ? (int64_t)seg : (int64_t)a.B * a.Hkv + i; };
-  float mx = -INFINITY;
-  for (int64_t i = i0; i <= i1; ++i) {
-    if (i > i0 && cta_tile_start(i + 1, T, G) == cta_tile_start(i, T, G)) continue;  // empty CTA
-    mx = fmaxf(mx, a.ws_lse[slot_of(i) * n_rep + h]);
-  }
+  float mx = -INFINITY, wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  for (int64_t i = i0; i <= i1; ++i) {
-    if (i > i0 && cta_tile_start(i + 1, T, G) == cta_tile_start(i, T, G)) continue;
-    const int64_t slot = slot_of(i);
-    const float l2 = a.ws_lse[slot * n_rep + h];
-    const float w = (l2 == -INFINITY) ? 0.f : exp2f(l2 - mx);
-    const float4 x = reinterpret_cast<const float4*>(a.ws_o + (slot * n_rep + h) * D)[lane];
-    acc.x += w * x.x;
-    acc.y += w * x.y;
-    acc.z += w * x.z;
-    acc.w += w * x.w;
-    wsum += w;
+  if (np <= kMaxPieces) {
+    float l2[kMaxPieces];
+    float4 x[kMaxPieces];
+#pragma unroll
+    for (int p = 0; p < kMaxPieces; ++p) {
+      if (p < np) {
+        l2[p] = a.ws_lse[slots[p] * n_rep + h];
+        x[p] = reinterpret_cast<const float4*>(a.ws_o + (slots[p] * n_rep + h) * D)[lane];
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < kMaxPieces; ++p)
+      if (p < np) mx = fmaxf(mx, l2[p]);
+#pragma unroll
+    for (int p = 0; p < kMaxPieces; ++p) {
+      if (p >= np) continue;
+      const float w = (l2[p] == -INFINITY) ? 0.f : exp2f(l2[p] - mx);
+      acc.x += w * x[p].x;
+      acc.y += w * x[p].y;
+      acc.z += w * x[p].z;
+      acc.w += w * x[p].w;
+      wsum += w;
+    }
+  } else {
+    // More pieces than registers hold (segments far longer than a CTA's share).
+    for (int64_t i = i0; i <= i1; ++i) {
+      if (i > i0 && cta_tile_start(i + 1, T, G) == cta_tile_start(i, T, G)) continue;
+      mx = fmaxf(mx, a.ws_lse[slot_of(i) * n_rep + h]);
+    }
+    for (int64_t i = i0; i <= i1; ++i) {
+      if (i > i0 && cta_tile_start(i + 1, T, G) == cta_tile_start(i, T, G)) continue;
+      const int64_t slot = slot_of(i);
+      const float l2 = a.ws_lse[slot * n_rep + h];
+      const float w = (l2 == -INFINITY) ? 0.f : exp2f(l2 - mx);
+      const float4 x = reinterpret_cast<const float4*>(a.ws_o + (slot * n_rep + h) * D)[lane];
+      acc.x += w * x.x;
+      acc.y += w * x.y;
+      acc.z += w * x.z;
+      acc.w += w * x.w;
+      wsum += w;
+    }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   put(make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));

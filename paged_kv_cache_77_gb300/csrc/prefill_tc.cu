@@ -20,12 +20,13 @@
 // 8 (log2 units), and O in TMEM is rescaled only then (warp-uniform).
 // Loads: warp 0 streams Q and K tiles (K ring 2 deep, a tile freed as soon as its
 // score product completes), warp 2 streams V tiles (3 deep). Warp 1 issues the
-// score products and warp 7 the value products, so neither waits behind the other.
+// score products and warp 3 the value products, so neither waits behind the other.
 // Work split: stream-K over all (unit, key block) tiles in kRounds rounds (see
 // pf_vbound), one persistent CTA per SM with an equal share of every round; a unit
 // cut by a range boundary leaves partial (o, lse) pieces that prefill_merge_kernel
 // combines by LSE. Each range owns at most two such pieces: one that starts inside
-// a unit ("head") and one that starts a unit it does not finish ("tail").
+// a unit ("head") and one that starts a unit it does not finish ("tail"). The kernel
+// records where each range starts, so the merge needs no search.
 //
 // Roofline: tensor cores (dense contraction). Algorithmic flops per visible
 // (query row, key) pair = 4 * 128 (q.k and p.v).
@@ -109,6 +110,9 @@ struct PrefillArgs {
   float* lse;                 // [T, H] or null
   float* ws_o;                // [kRounds * G][2][128][128]
   float* ws_lse;              // [kRounds * G][2][128]
+  long long* ws_bnd;          // [kRounds * G][8]: per virtual CTA, its range's first tile
+                              // (-1: empty range), that tile's unit (first tile, blocks,
+                              // b, g, q tile) and the total tile count
   int* dev_status;
   int64_t num_blocks;
   int B, H, Hkv, n_rep, qt_tokens, max_blocks, causal, out_f32, T;
@@ -352,6 +356,25 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
     flag_status(a.dev_status, PKV_DEV_TIMEOUT);
   };
 
+  if (warp == 2 && lane >= 1 && lane <= kRounds) {
+    // Where each of this CTA's ranges starts, for the merge: lane r + 1 takes round r.
+    const int64_t k = (int64_t)(lane - 1) * G + blockIdx.x;
+    long long* e = a.ws_bnd + 8 * k;
+    const int64_t lo = pf_vbound(k, W, G), hi = pf_vbound(k + 1, W, G);
+    if (lo < hi) {
+      PfCursor c;
+      pf_locate(c, a, lo);
+      e[1] = c.seg_base;
+      e[2] = c.n;
+      e[3] = c.b;
+      e[4] = c.g;
+      e[5] = c.qt;
+      e[6] = W;
+      e[0] = lo;
+    } else {
+      e[0] = -1;
+    }
+  }
   if (ntiles > 0 && warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
     PfCursor c;
@@ -690,53 +713,96 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
   }
 }
 
-// LSE merge of units cut by range boundaries. Block k looks at the boundary where
-// virtual CTA k's range starts; if it falls inside a unit and k is the first
-// non-empty virtual CTA after the one that started that unit, it merges the unit:
-// the tail piece of that virtual CTA plus the head pieces of every later virtual
-// CTA the unit reaches. Warp = 16 rows, lane = 4 output columns.
+// LSE merge of units cut by range boundaries. Block (k, y) looks at the boundary
+// where virtual CTA k's range starts; if it falls inside a unit and k is the first
+// non-empty virtual CTA after the one that started that unit (whose "tail" piece it
+// is), it merges rows [32 y, 32 y + 32) of the unit: the tail piece plus the head
+// piece of every later virtual CTA the unit reaches. The attention kernel records
+// where each range starts, and the other ranges are found in closed form, so the
+// merge does no search: one record, then one round of loads per row. Warp = 4 rows,
+// lane = 4 output columns; all pieces' loads of a row are issued before any is used.
 __global__ void __launch_bounds__(256) prefill_merge_kernel(PrefillArgs a, int G) {
   using namespace pf;
-  const int64_t k = blockIdx.x, V = (int64_t)kRounds * G;
+  constexpr int kRowsPerWarp = 4, kMaxPieces = 5;
+  const int64_t k = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t W = pf_total_work(a);
-  auto empty = [&](int64_t v) { return pf_vbound(v + 1, W, G) == pf_vbound(v, W, G); };
-  const int64_t start = pf_vbound(k, W, G);
-  if (k == 0 || start >= W || empty(k)) return;
-  PfCursor c;
-  pf_locate(c, a, start);
-  if (c.b >= a.B || c.t == c.seg_base) return;  // boundary at a unit start: nothing cut here
-  const int64_t seg_end = c.seg_base + c.n;
-  const int64_t i0 = pf_vcta_of_tile(c.seg_base, W, G);
-  int64_t first_after = i0 + 1;
-  while (first_after < V && empty(first_after)) ++first_after;
-  if (first_after != k) return;
-  const int64_t i1 = pf_vcta_of_tile(seg_end - 1, W, G);
-  pdl_wait_primary();
-  for (int rr = warp; rr < M; rr += 8) {
-    const int tok = c.qt * a.qt_tokens + rr / a.n_rep;
-    if (tok >= c.s.qlen) continue;
-    float mx = a.ws_lse[(i0 * 2 + 1) * M + rr];
-    for (int64_t v = i0 + 1; v <= i1; ++v) {
-      if (empty(v)) continue;
-      mx = fmaxf(mx, a.ws_lse[(v * 2) * M + rr]);
-    }
+  pdl_wait_primary();  // the attention kernel wrote the range records and the pieces
+  if (k == 0) return;
+  const long long* e = a.ws_bnd + 8 * k;
+  const int64_t start = e[0], seg_base = e[1];
+  if (start < 0 || start == seg_base) return;  // empty range, or it starts a unit: nothing cut here
+  const int64_t seg_end = seg_base + e[2], W = e[6];
+  const int b = (int)e[3], g = (int)e[4], qt = (int)e[5];
+  const PfSeq s = pf_seq(a, b);
+  const int64_t i0 = pf_vcta_of_tile(seg_base, W, G);
+  // The first non-empty virtual CTA after i0 owns the tile right after i0's range.
+  if (pf_vcta_of_tile(pf_vbound(i0 + 1, W, G), W, G) != k) return;
+  // Pieces: the tail slot of i0, then the head slot of each non-empty virtual CTA
+  // whose range starts inside the unit.
+  int64_t slot[kMaxPieces];
+  int np = 0;
+  slot[np++] = i0 * 2 + 1;
+  for (int64_t nxt = pf_vbound(i0 + 1, W, G); nxt < seg_end;) {
+    const int64_t v = pf_vcta_of_tile(nxt, W, G);
+    if (np < kMaxPieces) slot[np] = v * 2;
+    ++np;
+    nxt = pf_vbound(v + 1, W, G);
+  }
+  const int row0 = blockIdx.y * 32 + warp * kRowsPerWarp;
+  for (int q = 0; q < kRowsPerWarp; ++q) {
+    const int rr = row0 + q;
+    const int tok = qt * a.qt_tokens + rr / a.n_rep;
+    if (tok >= s.qlen) continue;
+    float mx = -INFINITY, wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-    for (int64_t v = i0; v <= i1; ++v) {
-      if (v > i0 && empty(v)) continue;
-      const int64_t slot = v * 2 + (v == i0 ? 1 : 0);
-      const float l2 = a.ws_lse[slot * M + rr];
-      const float w = (l2 == -INFINITY) ? 0.f : exp2f(l2 - mx);
-      const float4 x = reinterpret_cast<const float4*>(a.ws_o + (slot * M + rr) * D)[lane];
-      acc.x += w * x.x;
-      acc.y += w * x.y;
-      acc.z += w * x.z;
-      acc.w += w * x.w;
-      wsum += w;
+    if (np <= kMaxPieces) {
+      float l2[kMaxPieces];
+      float4 x[kMaxPieces];
+#pragma unroll
+      for (int p = 0; p < kMaxPieces; ++p) {
+        if (p < np) {
+          l2[p] = a.ws_lse[slot[p] * M + rr];
+          x[p] = reinterpret_cast<const float4*>(a.ws_o + (slot[p] * M + rr) * D)[lane];
+        }
+      }
+#pragma unroll
+      for (int p = 0; p < kMaxPieces; ++p)
+        if (p < np) mx = fmaxf(mx, l2[p]);
+#pragma unroll
+      for (int p = 0; p < kMaxPieces; ++p) {
+        if (p >= np) continue;
+        const float w = (l2[p] == -INFINITY) ? 0.f : exp2f(l2[p] - mx);
+        acc.x += w * x[p].x;
+        acc.y += w * x[p].y;
+        acc.z += w * x[p].z;
+        acc.w += w * x[p].w;
+        wsum += w;
+      }
+    } else {
+      // More pieces than registers hold (ranges much shorter than a unit): walk them.
+      for (int pass = 0; pass < 2; ++pass) {
+        for (int64_t v = i0, nxt = pf_vbound(i0 + 1, W, G);;) {
+          const int64_t sl = v * 2 + (v == i0 ? 1 : 0);
+          const float lv = a.ws_lse[sl * M + rr];
+          if (pass == 0) {
+            mx = fmaxf(mx, lv);
+          } else {
+            const float w = (lv == -INFINITY) ? 0.f : exp2f(lv - mx);
+            const float4 xv = reinterpret_cast<const float4*>(a.ws_o + (sl * M + rr) * D)[lane];
+            acc.x += w * xv.x;
+            acc.y += w * xv.y;
+            acc.z += w * xv.z;
+            acc.w += w * xv.w;
+            wsum += w;
+          }
+          if (nxt >= seg_end) break;
+          v = pf_vcta_of_tile(nxt, W, G);
+          nxt = pf_vbound(v + 1, W, G);
+        }
+      }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    const int64_t grow = (int64_t)(c.s.q0 + tok) * a.H + (int64_t)c.g * a.n_rep + rr % a.n_rep;
+    const int64_t grow = (int64_t)(s.q0 + tok) * a.H + (int64_t)g * a.n_rep + rr % a.n_rep;
     const float4 v = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     if (a.out_f32) {
       reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + grow * D)[lane] = v;
@@ -756,7 +822,8 @@ size_t prefill_workspace_bytes(int G) {
   const size_t slots = (size_t)kRounds * G * 2;
   const size_t o_bytes = slots * pf::M * pf::D * 4;
   const size_t l_bytes = (slots * pf::M * 4 + 255) / 256 * 256;
-  return o_bytes + l_bytes;
+  const size_t b_bytes = ((size_t)kRounds * G * 8 * 8 + 255) / 256 * 256;
+  return o_bytes + l_bytes + b_bytes;
 }
 
 cudaError_t launch_prefill(const void* q, const int32_t* cu_q, const void* k_cache,
@@ -784,8 +851,10 @@ cudaError_t launch_prefill(const void* q, const int32_t* cu_q, const void* k_cac
   a.T = T;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.ws_o = reinterpret_cast<float*>(ws);
-  a.ws_lse = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) +
-                                      (size_t)kRounds * num_sms * 2 * M * D * 4);
+  const size_t slots = (size_t)kRounds * num_sms * 2;
+  a.ws_lse = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + slots * M * D * 4);
+  a.ws_bnd = reinterpret_cast<long long*>(reinterpret_cast<uint8_t*>(ws) + slots * M * D * 4 +
+                                          (slots * M * 4 + 255) / 256 * 256);
 
   CUtensorMap tq, tk, tv;
   const uint64_t qdims[3] = {D, (uint64_t)H, (uint64_t)T};
@@ -803,7 +872,8 @@ cudaError_t launch_prefill(const void* q, const int32_t* cu_q, const void* k_cac
   prefill_tc_kernel<<<num_sms, NTHREADS, SMEM_BYTES, stream>>>(a, tq, tk, tv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_dependent(prefill_merge_kernel, dim3(kRounds * num_sms), dim3(256), 0, stream, a, num_sms);
+  return launch_dependent(prefill_merge_kernel, dim3(kRounds * num_sms, M / 32), dim3(256), 0, stream, a,
+                          num_sms);
 }
 
 }  // namespace pkv
