@@ -75,7 +75,21 @@ constexpr int KRB = TT * DRH * 2;  // this CTA's rope part of a tile: TT rows x 
 constexpr int STAGE = NLC * KCH + KRB;  // 4 latent chunks + 32 rope columns (36 KB)
 constexpr int NST = 4;           // K stages
 constexpr int XBUF = TT * M * 4; // one partial score tile, fp32 (32 KB)
-constexpr int NTHREADS = 384;  // TMA warp, S-issue warp, 8 softmax warps, idle, O-issue warp
+#ifndef PKV_MLA_SMW
+#define PKV_MLA_SMW 1
+#endif
+// Softmax warps per TMEM lane quarter: each takes TT / SMW score columns of a tile
+// and DH / SMW columns of O for its head rows.
+constexpr int SMW = PKV_MLA_SMW;
+static_assert(SMW == 1 || SMW == 2, "softmax warps per lane quarter");
+constexpr int NSMT = 128 * SMW;                 // softmax threads
+constexpr int CW = TT / SMW;                   // score columns per softmax thread
+constexpr int OW = DH / SMW;                   // O columns per softmax thread
+constexpr int SM_W0 = SMW == 2 ? 2 : 4;        // first softmax warp (its warp % 4 is its lane quarter)
+constexpr int O_WARP = SMW == 2 ? 11 : 3;      // value-product issuer
+// SMW 2: TMA warp, S-issue warp, 8 softmax warps, idle, O-issue warp;
+// SMW 1: TMA warp, S-issue warp, idle, O-issue warp, 4 softmax warps.
+constexpr int NTHREADS = SMW == 2 ? 384 : 256;
 
 constexpr int OFF_K = 0;
 constexpr int OFF_QR = OFF_K + NST * STAGE;        // rope part of Q (64-byte swizzle)
@@ -243,15 +257,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
     }
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QEMPTY), 1);
-    mbar_init(bar(B_QTFULL), 256);
+    mbar_init(bar(B_QTFULL), NSMT);
     mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_SEMPTY), 256);
+    mbar_init(bar(B_SEMPTY), NSMT);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_PFULL + i), 256);
+      mbar_init(bar(B_PFULL + i), NSMT);
       mbar_init(bar(B_PEMPTY + i), 1);
       mbar_init(bar(B_XFULL + i), 1);
     }
-    mbar_init(bar(B_OFREE), 256);
+    mbar_init(bar(B_OFREE), NSMT);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -359,7 +373,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       if (last) mma_commit(bar(B_QEMPTY));
       next(c, a, cap);
     }
-  } else if (ntiles > 0 && warp == 11 && lane == 0) {
+  } else if (ntiles > 0 && warp == O_WARP && lane == 0) {
     // ------------------------------------------------------------ value-product issuer
     // O(j) reads the latent chunks of stage j % NST; its commit also frees the stage
     // (S(j) completed before the softmax published P(j)).
@@ -385,19 +399,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       mma_commit(bar(B_KEMPTY + st));
       next(c, a, cap);
     }
-  } else if (ntiles > 0 && warp >= 2 && warp < 10) {
+  } else if (ntiles > 0 && warp >= SM_W0 && warp < SM_W0 + 4 * SMW) {
     // ------------------------------------------------------------ softmax / epilogue
     // Eight warps, two per TMEM lane quarter: warp w takes head row r of its quarter
     // and score columns [32 hc, 32 hc + 32) of each tile, O columns [128 hc, +128).
     const int quarter = warp & 3;
-    const int hc = (warp - 2) >> 2;
+    const int hc = (warp - SM_W0) >> 2;  // column part of the row (0 when SMW == 1)
     const int r = quarter * 32 + lane;  // head row
-    const int st_id = hc * 128 + r;     // 0..255
+    const int st_id = hc * 128 + r;     // 0 .. NSMT-1
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t peer = (uint32_t)(half ^ 1);
     // Partial-score buffers: [TT/4 token groups][128 heads][4 tokens] fp32, so a warp's
     // 16-byte accesses cover 512 contiguous bytes. This thread's groups are 8 hc + g.
-    const uint32_t x_peer = mapa_shared(sbase + OFF_X + (uint32_t)(8 * hc * M + r) * 16, peer);
+    const uint32_t x_peer = mapa_shared(sbase + OFF_X + (uint32_t)((CW / 4) * hc * M + r) * 16, peer);
     const uint32_t xbar_peer = mapa_shared(bar(B_XFULL), peer);
     float* red = reinterpret_cast<float*>(base + OFF_RED);
     const int qbar = 1 + quarter;                            // named barrier of the two warps
@@ -418,7 +432,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       tc_fence_after();
       const bool have = r < a.H;
       const int64_t qrow = qi * a.H + r;
-      for (int ch = 2 * hc; ch < 2 * hc + 2; ++ch) {
+      for (int ch = (NLC / SMW) * hc; ch < (NLC / SMW) * (hc + 1); ++ch) {
         const uint4* src = reinterpret_cast<const uint4*>(a.q_nope + qrow * DC + half * DH + ch * 64);
         uint32_t lo[16], hi[16];
 #pragma unroll
@@ -443,6 +457,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
 
     // Sum of a per-row value over the two warps of the quarter.
     auto pair_sum = [&](float v) {
+      if (SMW == 1) return v;
       float* slot = red + red_par * 256;
       slot[st_id] = v;
       named_bar_sync(qbar, 64);
@@ -454,6 +469,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
     // that both warps of a quarter leave the loop at the same tile (they meet at a
     // named barrier in every exchange).
     auto pair_max_abort = [&](float v, bool& stop) {
+      if (SMW == 1) {
+        stop = __any_sync(0xffffffffu, *abort_flag != 0);
+        return v;
+      }
       float2* slot = reinterpret_cast<float2*>(red + 512) + red_par * 256;
       slot[st_id] = make_float2(v, *abort_flag ? 1.f : 0.f);
       named_bar_sync(qbar, 64);
@@ -473,7 +492,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       const bool store = r < a.H;
       const int64_t slot = (p_first == p_segbase) ? (int64_t)pb : (int64_t)a.Bq + ci;
       const int64_t orow = row_index(a, pb);
-      for (int c0 = 128 * hc; c0 < 128 * hc + 128; c0 += 32) {
+      for (int c0 = OW * hc; c0 < OW * hc + OW; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_off + O_COL + c0, v);
         tmem_wait_ld();
@@ -526,19 +545,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
     // enough: tile j+1 is sent only after this thread has consumed the peer's tile j
     // (its values feed the max below), and the peer sends tile j+2 into the buffer of
     // tile j only once this CTA's tile j+1 has reached it.
-    uint32_t sv[TT / 2];  // this warp's 32 partial scores of the tile in flight
+    uint32_t sv[CW];  // this warp's CW partial scores of the tile in flight
     // Read S of tile jn from tensor memory and send it into the peer's buffer.
     auto fetch_send = [&](int jn) {
       if (!mbar_wait(bar(B_SFULL), jn & 1)) fail();
       __syncwarp();
       tc_fence_after();
-      tmem_ld32(tmem + lane_off + S_COL + 32 * hc, sv);
+#pragma unroll
+      for (int c0 = 0; c0 < CW; c0 += 32)
+        tmem_ld32(tmem + lane_off + S_COL + CW * hc + c0, *reinterpret_cast<uint32_t(*)[32]>(&sv[c0]));
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bar(B_SEMPTY));
       const uint32_t xo = (uint32_t)(jn & 1) * XBUF, xbar = xbar_peer + 8u * (jn & 1);
 #pragma unroll
-      for (int g = 0; g < 8; ++g)
+      for (int g = 0; g < CW / 4; ++g)
         st_async_v4(x_peer + xo + g * (M * 16), sv[4 * g], sv[4 * g + 1], sv[4 * g + 2], sv[4 * g + 3], xbar);
     };
     auto lookup_block = [&](const TileCursor& cc) {
@@ -571,30 +592,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       // Peer's partial scores of tile j, added to this CTA's.
       if (opener) mbar_expect_tx(bar(B_XFULL + xb), XBUF);
       if (!mbar_wait_cluster(bar(B_XFULL + xb), (j >> 1) & 1)) fail();
-      const float4* xin = reinterpret_cast<const float4*>(base + OFF_X + xb * XBUF + (8 * hc * M + r) * 16);
-      const int tok0 = c.j * TT + 32 * hc;  // first token of this warp's columns
+      const float4* xin =
+          reinterpret_cast<const float4*>(base + OFF_X + xb * XBUF + ((CW / 4) * hc * M + r) * 16);
+      const int tok0 = c.j * TT + CW * hc;  // first token of this warp's columns
       const bool blk_ok = blk >= 0 && (int64_t)blk < a.num_blocks;
-      const int nvalid = blk_ok ? min(32, c.len - tok0) : 0;  // may be <= 0
+      const int nvalid = blk_ok ? min(CW, c.len - tok0) : 0;  // may be <= 0
       const int nvalid_tile = blk_ok ? min(TT, c.len - c.j * TT) : 0;
-      // Raw scores of this warp's 32 columns (the two partial sums added in pairs);
+      // Raw scores of this warp's CW columns (the two partial sums added in pairs);
       // masked columns become -inf. The max is taken on raw scores (scale > 0).
-      uint64_t x2[16];
+      uint64_t x2[CW / 2];
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
+      for (int g = 0; g < CW / 4; ++g) {
         const float4 pv = xin[g * M];
         x2[2 * g] = fadd2(f2pack(__uint_as_float(sv[4 * g]), __uint_as_float(sv[4 * g + 1])), f2pack(pv.x, pv.y));
         x2[2 * g + 1] = fadd2(f2pack(__uint_as_float(sv[4 * g + 2]), __uint_as_float(sv[4 * g + 3])), f2pack(pv.z, pv.w));
       }
-      if (!__all_sync(0xffffffffu, nvalid >= 32)) {
+      if (!__all_sync(0xffffffffu, nvalid >= CW)) {
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < CW / 2; ++q) {
           const float2 t = f2unpack(x2[q]);
           x2[q] = f2pack(2 * q < nvalid ? t.x : -INFINITY, 2 * q + 1 < nvalid ? t.y : -INFINITY);
         }
       }
       float m2[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
+      for (int q = 0; q < CW / 2; ++q) {
         const float2 t = f2unpack(x2[q]);
         m2[q & 1] = max3f(m2[q & 1], t.x, t.y);
       }
@@ -618,7 +640,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
           tc_fence_after();
           // 16 columns at a time: x and the next tile's scores are live here.
 #pragma unroll 1
-          for (int c0 = 128 * hc; c0 < 128 * hc + 128; c0 += 16) {
+          for (int c0 = OW * hc; c0 < OW * hc + OW; c0 += 16) {
             uint32_t v[16];
             tmem_ld16(tmem + lane_off + O_COL + c0, v);
             tmem_wait_ld();
@@ -642,10 +664,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       // 2^-8) would otherwise scale the whole output row.
       const float mneg = (m_ref == -INFINITY) ? 0.f : -m_ref;
       const uint64_t cs2 = f2pack(a.scale_log2, a.scale_log2), mn2 = f2pack(mneg, mneg);
-      uint32_t pk[16];
+      uint32_t pk[CW / 2];
       uint64_t ps2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)}, pe2[2] = {ps2[0], ps2[1]};
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
+      for (int q = 0; q < CW / 2; ++q) {
         const float2 t = f2unpack(ffma2(x2[q], cs2, mn2));
         const float p0 = exp2f(t.x), p1 = exp2f(t.y);
         __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
@@ -665,8 +687,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       if (nvalid_tile < TT) {
         uint8_t* kt = base + OFF_K + (j % NST) * STAGE;
 #pragma unroll
-        for (int k = 0; k < TT / 8; ++k) {
-          const int pidx = st_id + 256 * k;       // TT rows x 4 chunks x 8 pieces of 16 B
+        for (int k = 0; k < TT * 32 / NSMT; ++k) {
+          const int pidx = st_id + NSMT * k;      // TT rows x 4 chunks x 8 pieces of 16 B
           const int row = pidx >> 5, ch = (pidx >> 3) & 3, q = pidx & 7;
           if (row >= nvalid_tile)
             *reinterpret_cast<uint4*>(kt + ch * KCH + row * 128 + q * 16) = make_uint4(0, 0, 0, 0);
@@ -676,7 +698,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       if (!mbar_wait(bar(B_PEMPTY + xb), ((j >> 1) & 1) ^ 1)) fail();
       __syncwarp();
       tc_fence_after();
-      tmem_st16(tmem + lane_off + p_col(xb) + 16 * hc, pk);
+#pragma unroll
+      for (int c0 = 0; c0 < CW / 2; c0 += 16)
+        tmem_st16(tmem + lane_off + p_col(xb) + (CW / 2) * hc + c0, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c0]));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + xb));
