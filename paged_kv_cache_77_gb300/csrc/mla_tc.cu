@@ -25,10 +25,13 @@
 // buffered and software-pipelined: tile j+1's partial is sent while tile j's softmax
 // runs.
 //
-// Warps: 0 TMA producer, 1 score-product issuer, 2..9 softmax (two per TMEM lane
-// quarter, each with 32 of a tile's 64 score columns and 128 of the 256 O columns; the
-// two warps of a quarter agree on the row max through shared memory), 11 value-product
-// issuer (warp 10 is idle; 12 warps keep at most three per SM sub-partition).
+// Warps (the default, SMW = 1): 0 TMA producer, 1 score-product issuer, 3 value-
+// product issuer, 4..7 softmax, one per TMEM lane quarter, each thread with a head
+// row's 64 score columns and 256 O columns (warp 2 is idle). With SMW = 2 (a build
+// option): 2..9 softmax, two per lane quarter with 32 score columns and 128 O columns
+// each, agreeing on the row max through shared memory, and 11 the value-product
+// issuer. One warp per quarter measured faster (228.6 against 232.5 us on the mla
+// workload): it needs no exchange between warps.
 //
 // Tensor memory (512 columns): S 0..63, P 64..127 (two buffers of 64 bf16 packed in
 // pairs, the A operand of the value product), this CTA's 256 Q latent columns
