@@ -461,6 +461,19 @@ int pkv_paged_attention_decode_static(void* out, int32_t out_dtype, float* lse, 
                                       int32_t head_dim, int32_t block_size, int64_t num_blocks,
                                       float scale, int32_t window, int* dev_status, void* stream);
 
+/* ==========================================================================
+ * Self-test (no counterpart in the pages: a check of the kernels' failure path)
+ * ========================================================================== */
+
+/* Launches one small kernel that waits, with the bounded wait routines every
+ * attention kernel uses, on an mbarrier that nothing completes. Each wait gives up
+ * after its cycle limit (about a second at full clock) and the kernel sets
+ * PKV_DEV_TIMEOUT in *dev_status (device memory, caller-owned; other bits are left
+ * as they are), then returns: the CUDA context stays usable. Asynchronous on
+ * `stream`. Errors: PKV_ERR_INVALID_ARG for a null dev_status; PKV_ERR_LAUNCH if
+ * the launch fails. */
+int pkv_selftest_bounded_wait(int* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

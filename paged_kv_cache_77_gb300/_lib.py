@@ -72,6 +72,7 @@ SIGNATURES = {
                                             i32, i32, i32, i64, f32, vp, sz, vp, vp]),
     "pkv_paged_attention_decode_static": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, i32, vp, i32, i32,
                                                     i32, i32, i32, i64, f32, i32, vp, vp]),
+    "pkv_selftest_bounded_wait": (C.c_int, [vp, vp]),
 }
 
 _lib = None

@@ -721,3 +721,18 @@ def paged_attention_decode_static(q, k_cache, v_cache, block_table, seq_lens, sc
         block_table.shape[1], _ptr(seq_lens), B, H, hkv, d, bs, nb, float(scale), int(window),
         _ptr(dev_status), _stream(stream)), "pkv_paged_attention_decode_static")
     return out
+
+
+DEV_TIMEOUT = 8  # PKV_DEV_TIMEOUT: a bounded wait inside a kernel gave up
+
+
+def selftest_bounded_wait(dev_status, stream=None) -> None:
+    """Launch the failure-path self-test: a kernel whose bounded waits on an mbarrier
+    that nothing completes run out (about a second) and set DEV_TIMEOUT in
+    dev_status (an int32 CUDA tensor of at least one element)."""
+    if not (isinstance(dev_status, torch.Tensor) and dev_status.is_cuda):
+        raise ValueError("dev_status must be an int32 CUDA tensor")
+    status_buffer(dev_status, dev_status.device)
+    check_current_device(dev_status.device)
+    check(load().pkv_selftest_bounded_wait(_ptr(dev_status), _stream(stream)),
+          "pkv_selftest_bounded_wait")

@@ -413,4 +413,10 @@ int pkv_mla_paged_decode_spec(void* out, int32_t out_dtype, float* lse, const vo
                     workspace_bytes, dev_status, stream);
 }
 
+int pkv_selftest_bounded_wait(int* dev_status, void* stream) {
+  PKV_REQUIRE(dev_status != nullptr, PKV_ERR_INVALID_ARG, "pkv_selftest_bounded_wait: null dev_status");
+  return launch_status(launch_bounded_wait(dev_status, static_cast<cudaStream_t>(stream)),
+                       "pkv_selftest_bounded_wait");
+}
+
 }  // extern "C"

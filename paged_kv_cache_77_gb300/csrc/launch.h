@@ -78,4 +78,7 @@ cudaError_t launch_prefill(const void* q, const int32_t* cu_q, const void* k_cac
                            int B, int H, int Hkv, int64_t num_blocks, float scale, int causal,
                            void* ws, int* dev_status, int num_sms, cudaStream_t stream);
 
+// Self-test: a bounded wait that runs out (selftest.cu).
+cudaError_t launch_bounded_wait(int* dev_status, cudaStream_t stream);
+
 }  // namespace pkv
