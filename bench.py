@@ -883,29 +883,54 @@ def run_decode(args, dev, world: int = 1, rank: int = 0):
                % (nbytes["kv"] / 1e9))
 
     # ---- end to end through the public API with host buffers
-    pin = {k: v[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")}
-    lens_pin = torch.from_numpy(d.seq_lens).pin_memory()
+    # The step's inputs (queries, new K/V rows, lengths, slots, block table) sit in one
+    # pinned host staging buffer and cross to the device in one copy, into a device
+    # buffer the calls read through views (each part starts on a 256-byte boundary);
+    # the slots are rebuilt into their part every step. The output comes back in one
+    # copy.
+    parts = [("q", v["q"]), ("k_new", v["k_new"]), ("v_new", v["v_new"]),
+             ("lens", torch.from_numpy(d.seq_lens)), ("slots", torch.from_numpy(slots_np)),
+             ("table", torch.from_numpy(table_np))]
+    offs, total = {}, 0
+    for name, t in parts:
+        offs[name] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    stage_h = torch.empty(total, dtype=torch.uint8).pin_memory()
+    stage_d = torch.empty(total, dtype=torch.uint8, device=dev)
+
+    def view(buf, name, like):
+        n = like.numel() * like.element_size()
+        return buf[offs[name]:offs[name] + n].view(like.dtype).view(like.shape)
+
+    for name, t in parts:
+        view(stage_h, name, t).copy_(t.cpu())
+    dq, dk, dv = (view(stage_d, n, v[n]) for n in ("q", "k_new", "v_new"))
+    lens_d = view(stage_d, "lens", parts[3][1])
+    slots_d = view(stage_d, "slots", parts[4][1])
+    slots_h = view(stage_h, "slots", parts[4][1]).numpy()
+    table_d = view(stage_d, "table", parts[5][1])
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    dq, dk, dv = torch.empty_like(v["q"]), torch.empty_like(v["k_new"]), torch.empty_like(v["v_new"])
-    slots_dev = torch.empty_like(slots)
-    h2d = sum(t.numel() * t.element_size() for t in pin.values()) + lens_pin.numel() * 4 + \
-        slots_np.nbytes
+    h2d = sum(t.numel() * t.element_size() for _, t in parts)
     d2h = out_host.numel() * out_host.element_size()
+
+    def attend_e2e(q):
+        if spec:
+            api.paged_attention_decode_spec(q, v["k_cache"], v["v_cache"], table_d, lens_d,
+                                            wl.scale, wl.window, out=out, workspace=ws)
+        else:
+            api.paged_attention_decode(q, v["k_cache"], v["v_cache"], table_d, lens_d, wl.scale,
+                                       wl.window, out=out, workspace=ws)
 
     def e2e_step():
         if flush is not None:
             flush(1)
             torch.cuda.current_stream().synchronize()
         t = time.perf_counter()
-        sm = api.build_slot_mapping(table_np, d.start_pos, d.num_new, wl.block_size)
-        sm_pin = torch.from_numpy(sm)
-        dq.copy_(pin["q"], non_blocking=True)
-        dk.copy_(pin["k_new"], non_blocking=True)
-        dv.copy_(pin["v_new"], non_blocking=True)
-        seq_lens.copy_(lens_pin, non_blocking=True)
-        slots_dev.copy_(sm_pin, non_blocking=False)
-        api.kv_cache_write(v["k_cache"], v["v_cache"], dk, dv, slots_dev)
-        attend(dq)
+        # The previous step's copy ended at its synchronize, so its part can be rewritten.
+        slots_h[:] = api.build_slot_mapping(table_np, d.start_pos, d.num_new, wl.block_size)
+        stage_d.copy_(stage_h, non_blocking=True)
+        api.kv_cache_write(v["k_cache"], v["v_cache"], dk, dv, slots_d)
+        attend_e2e(dq)
         out_host.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
         return time.perf_counter() - t
