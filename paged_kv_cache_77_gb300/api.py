@@ -18,7 +18,8 @@ PKV_BF16, PKV_F32 = 0, 1
 
 
 def _ptr(t):
-    return None if t is None else C.c_void_p(t.data_ptr())
+    # ctypes turns the int into the c_void_p argument the signature declares.
+    return None if t is None else t.data_ptr()
 
 
 def _np_ptr(a: np.ndarray):
@@ -27,7 +28,7 @@ def _np_ptr(a: np.ndarray):
 
 def _stream(stream=None):
     s = torch.cuda.current_stream() if stream is None else stream
-    return C.c_void_p(s.cuda_stream)
+    return s.cuda_stream
 
 
 def _dev_bf16(t, name):
