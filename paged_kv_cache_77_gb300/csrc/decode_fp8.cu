@@ -568,20 +568,22 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       const bool valid = blk_ok && pos < c.len && pos >= lo;
       const float smul = sk * kWidenScale * a.scale_log2;
       float x[HG];
+      bool over = false;  // a score of this thread beats its head's reference by > kLazy
 #pragma unroll
       for (int h = 0; h < HG; ++h) {
         // Column h0 + h, chosen between two compile-time indices (no local memory).
         const uint32_t sx = grp ? svr[(HG + h) & 15] : svr[h];
         x[h] = (valid && has_heads) ? __uint_as_float(sx) * (smul * qmul[h]) : -INFINITY;
-        const float m = warp_max(x[h]);
-        if (lane == 0 && has_heads) red[(sb * 4 + quarter) * 16 + h0 + h] = m;
+        over |= x[h] > m_run[h] + kLazy;
       }
       if (grp == 0) {
         const float fv = warp_max(valid ? sv : 0.f);
         if (lane == 0) fred[sb * 4 + quarter] = fv;
       }
       if (ts == 0) abort_snap[sb] = *abort_flag;
-      named_bar_sync(1, NSOFT);
+      // One barrier publishes the V-scale maxima and tells every thread whether any
+      // score of the tile beats its reference: most tiles need no block max at all.
+      const bool any_over = named_bar_any(1, NSOFT, over);
       if (abort_snap[sb]) {
         aborted = true;
         break;
@@ -589,22 +591,30 @@ __global__ void __launch_bounds__(f8d::NTHREADS, 1)
       float f = fmaxf(fmaxf(fred[sb * 4], fred[sb * 4 + 1]), fmaxf(fred[sb * 4 + 2], fred[sb * 4 + 3]));
       f = f > 0.f ? f : 1.f;
       const float vmul = valid ? __fdividef(sv, f) : 0.f;
-      // Block max per head and the reference test; both groups read the same
-      // maxima for their own heads, so `resc` is uniform within a group.
-      float mb[HG];
       resc = false;
-#pragma unroll
-      for (int h = 0; h < HG; ++h) {
-        const float* rr = red + sb * 64 + h0 + h;
-        mb[h] = has_heads ? fmaxf(fmaxf(rr[0], rr[16]), fmaxf(rr[32], rr[48])) : -INFINITY;
-        resc |= mb[h] > m_run[h] + kLazy;
-      }
-      if (resc) {
+      if (any_over) {
+        // Block max per head and the reference test; both groups read the same
+        // maxima for their own heads, so `resc` is uniform within a group.
 #pragma unroll
         for (int h = 0; h < HG; ++h) {
-          const float mn = fmaxf(m_run[h], mb[h]);
-          alpha[h] = exp2f(m_run[h] - mn);
-          m_run[h] = mn;
+          const float m = warp_max(x[h]);
+          if (lane == 0 && has_heads) red[(sb * 4 + quarter) * 16 + h0 + h] = m;
+        }
+        named_bar_sync(1, NSOFT);
+        float mb[HG];
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+          const float* rr = red + sb * 64 + h0 + h;
+          mb[h] = has_heads ? fmaxf(fmaxf(rr[0], rr[16]), fmaxf(rr[32], rr[48])) : -INFINITY;
+          resc |= mb[h] > m_run[h] + kLazy;
+        }
+        if (resc) {
+#pragma unroll
+          for (int h = 0; h < HG; ++h) {
+            const float mn = fmaxf(m_run[h], mb[h]);
+            alpha[h] = exp2f(m_run[h] - mn);
+            m_run[h] = mn;
+          }
         }
       }
 #pragma unroll
