@@ -428,63 +428,73 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
 #pragma unroll
         for (int i = 0; i < CW; ++i) x[i] = (i >= ilo && i < ihi) ? __uint_as_float(sv[i]) : -INFINITY;
       }
-      {
-        float wm[CW];
+      const float cs = a.scale_log2;
+      // The reference moves only when a column's block max beats it by more than
+      // kLazy. One barrier with an OR reduction asks whether any thread of the block
+      // sees such a score; the block max per column (warp reductions, an exchange
+      // through shared memory and a second barrier) is taken only then.
+      bool over = false;
 #pragma unroll
-        for (int i = 0; i < CW; ++i) wm[i] = warp_max(x[i]);
-        float* dst = cred + (sb * 4 + quarter) * N;
-        if (lane == 0) {
-          if constexpr (CW % 4 == 0) {
-#pragma unroll
-            for (int i = 0; i < CW; i += 4)
-              *reinterpret_cast<float4*>(dst + i) = make_float4(wm[i], wm[i + 1], wm[i + 2], wm[i + 3]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < CW; ++i) dst[i] = wm[i];
-          }
-        }
-      }
+      for (int i = 0; i < CW; ++i) over |= x[i] * cs > m_run[i] + kLazy;
       // One thread snapshots the abort flag before the barrier so that every
       // thread of the block takes the same decision after it.
       if (r == 0) snap[sb] = *abort_flag;
-      named_bar_sync(bar_id, 128);
+      const bool any_over = named_bar_any(bar_id, 128, over);
       if (snap[sb]) {
         aborted = true;
         break;
       }
-      // Block max per column (raw units; scale > 0), then the reference test. Every
-      // thread of the block reads the same maxima, so `resc` is uniform.
-      float mb[CW];
-      {
-        const float* src = cred + sb * 4 * N;
-        if constexpr (CW % 4 == 0) {
-#pragma unroll
-          for (int i = 0; i < CW; i += 4) {
-            const float4 q0 = *reinterpret_cast<const float4*>(src + i);
-            const float4 q1 = *reinterpret_cast<const float4*>(src + N + i);
-            const float4 q2 = *reinterpret_cast<const float4*>(src + 2 * N + i);
-            const float4 q3 = *reinterpret_cast<const float4*>(src + 3 * N + i);
-            mb[i] = fmaxf(fmaxf(q0.x, q1.x), fmaxf(q2.x, q3.x));
-            mb[i + 1] = fmaxf(fmaxf(q0.y, q1.y), fmaxf(q2.y, q3.y));
-            mb[i + 2] = fmaxf(fmaxf(q0.z, q1.z), fmaxf(q2.z, q3.z));
-            mb[i + 3] = fmaxf(fmaxf(q0.w, q1.w), fmaxf(q2.w, q3.w));
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < CW; ++i)
-            mb[i] = fmaxf(fmaxf(src[i], src[N + i]), fmaxf(src[2 * N + i], src[3 * N + i]));
-        }
-      }
-      const float cs = a.scale_log2;
       resc = false;
+      if (any_over) {
+        {
+          float wm[CW];
 #pragma unroll
-      for (int i = 0; i < CW; ++i) resc |= mb[i] * cs > m_run[i] + kLazy;
-      if (resc) {
+          for (int i = 0; i < CW; ++i) wm[i] = warp_max(x[i]);
+          float* dst = cred + (sb * 4 + quarter) * N;
+          if (lane == 0) {
+            if constexpr (CW % 4 == 0) {
 #pragma unroll
-        for (int i = 0; i < CW; ++i) {
-          const float mn = fmaxf(m_run[i], mb[i] * cs);
-          alpha[i] = exp2f(m_run[i] - mn);
-          m_run[i] = mn;
+              for (int i = 0; i < CW; i += 4)
+                *reinterpret_cast<float4*>(dst + i) = make_float4(wm[i], wm[i + 1], wm[i + 2], wm[i + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < CW; ++i) dst[i] = wm[i];
+            }
+          }
+        }
+        named_bar_sync(bar_id, 128);
+        // Block max per column (raw units; scale > 0), then the reference test. Every
+        // thread of the block reads the same maxima, so `resc` is uniform.
+        float mb[CW];
+        {
+          const float* src = cred + sb * 4 * N;
+          if constexpr (CW % 4 == 0) {
+#pragma unroll
+            for (int i = 0; i < CW; i += 4) {
+              const float4 q0 = *reinterpret_cast<const float4*>(src + i);
+              const float4 q1 = *reinterpret_cast<const float4*>(src + N + i);
+              const float4 q2 = *reinterpret_cast<const float4*>(src + 2 * N + i);
+              const float4 q3 = *reinterpret_cast<const float4*>(src + 3 * N + i);
+              mb[i] = fmaxf(fmaxf(q0.x, q1.x), fmaxf(q2.x, q3.x));
+              mb[i + 1] = fmaxf(fmaxf(q0.y, q1.y), fmaxf(q2.y, q3.y));
+              mb[i + 2] = fmaxf(fmaxf(q0.z, q1.z), fmaxf(q2.z, q3.z));
+              mb[i + 3] = fmaxf(fmaxf(q0.w, q1.w), fmaxf(q2.w, q3.w));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < CW; ++i)
+              mb[i] = fmaxf(fmaxf(src[i], src[N + i]), fmaxf(src[2 * N + i], src[3 * N + i]));
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < CW; ++i) resc |= mb[i] * cs > m_run[i] + kLazy;
+        if (resc) {
+#pragma unroll
+          for (int i = 0; i < CW; ++i) {
+            const float mn = fmaxf(m_run[i], mb[i] * cs);
+            alpha[i] = exp2f(m_run[i] - mn);
+            m_run[i] = mn;
+          }
         }
       }
       // P enters the value product as bf16 (pairs of columns packed with one
