@@ -314,17 +314,20 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
     // large finite negative value, so no -inf arithmetic is needed anywhere.
     constexpr float kLazy = 8.f;
     constexpr float kMinit = -1e30f;
-    // o_reg holds the output of the tiles folded so far, scaled to the reference of
-    // the newest tile whose scores are done: acc_o(j - 1) runs after tile j's
-    // rescale factors are known and applies them together with O(j - 1).
-    float m_run[CW], l_part[CW], o_reg[CW];
+    // o_reg holds the output of the tiles folded so far. O(j - 1) is folded after
+    // P(j) is published, or, when tile j raises the reference, before the rescale
+    // of everything accumulated.
+    // l_part sums the weights as the value product uses them (rounded to bf16) and
+    // divides the output; le_part sums the exact fp32 weights and gives the
+    // log-sum-exp (the reported lse and the weight of a split piece in the merge).
+    float m_run[CW], l_part[CW], le_part[CW], o_reg[CW];
     // State of the piece being accumulated.
     int pb = 0, pg = 0;
     int64_t p_first = t0, p_segbase = 0;
     bool p_whole = false;
     bool aborted = false;
 
-    auto acc_o = [&](int jj, bool resc, const float (&alpha)[CW]) {
+    auto acc_o = [&](int jj) {
       const int ob = jj & 1;
       if (!mbar_wait(bar(B_OFULL + ob), (jj >> 1) & 1)) fail();
       __syncwarp();
@@ -334,32 +337,44 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bar(B_OEMPTY + ob));
-      if (resc) {
 #pragma unroll
-        for (int i = 0; i < CW; ++i) o_reg[i] = (o_reg[i] + __uint_as_float(v[i])) * alpha[i];
-      } else {
-#pragma unroll
-        for (int i = 0; i < CW; ++i) o_reg[i] += __uint_as_float(v[i]);
-      }
+      for (int i = 0; i < CW; ++i) o_reg[i] += __uint_as_float(v[i]);
     };
     auto finalize = [&]() {
 #pragma unroll
       for (int i = 0; i < CW; ++i) {
-        float l = l_part[i];
+        float l = l_part[i], le = le_part[i];
 #pragma unroll
-        for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) clred[quarter * N + i] = l;
+        for (int o = 16; o; o >>= 1) {
+          l += __shfl_xor_sync(0xffffffffu, l, o);
+          le += __shfl_xor_sync(0xffffffffu, le, o);
+        }
+        l_part[i] = l;
+        le_part[i] = le;
       }
-      named_bar_sync(bar_id, 128);
+      // The four warps' partial sums of both normalisers, one after the other through
+      // the same [4][N] slots (once per piece); the totals replace the partials.
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        float* part = k ? le_part : l_part;
+        if (lane == 0) {
+#pragma unroll
+          for (int i = 0; i < CW; ++i) clred[quarter * N + i] = part[i];
+        }
+        named_bar_sync(bar_id, 128);
+#pragma unroll
+        for (int i = 0; i < CW; ++i) part[i] = clred[i] + clred[N + i] + clred[2 * N + i] + clred[3 * N + i];
+        named_bar_sync(bar_id, 128);  // the slots are rewritten next (or by the next piece)
+      }
       const int64_t slot = (p_first == p_segbase) ? (int64_t)pb * a.Hkv + pg
                                                   : (int64_t)a.B * a.Hkv + blockIdx.x;
 #pragma unroll
       for (int i = 0; i < CW; ++i) {
         const int h = qbase + i;  // column: query token h / NREP, head h % NREP
         if (NCH > 1 && h >= NR) continue;
-        const float l = clred[i] + clred[N + i] + clred[2 * N + i] + clred[3 * N + i];
+        const float l = l_part[i], le = le_part[i];
         const float ov = l > 0.f ? o_reg[i] / l : 0.f;
-        const float lse2 = l > 0.f ? m_run[i] + log2f(l) : -INFINITY;
+        const float lse2 = le > 0.f ? m_run[i] + log2f(le) : -INFINITY;
         if (p_whole) {
           const int64_t row = ((int64_t)pb * QL + h / NREP) * a.H + (int64_t)pg * NREP + h % NREP;
           if (a.out_f32)
@@ -372,22 +387,21 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
           if (r == 0) a.ws_lse[slot * NR + h] = lse2;
         }
       }
-      named_bar_sync(bar_id, 128);  // lred reused by the next piece
     };
 
-    float alpha[CW];
     bool resc = false;
     for (int j = 0; j < ntiles; ++j) {
       const bool first = (j == 0) || (c.j == 0);
       if (first) {
         if (j > 0) {
-          acc_o(j - 1, false, alpha);
+          acc_o(j - 1);
           finalize();
         }
 #pragma unroll
         for (int i = 0; i < CW; ++i) {
           m_run[i] = kMinit;
           l_part[i] = 0.f;
+          le_part[i] = 0.f;
           o_reg[i] = 0.f;
         }
         pb = c.b;
@@ -489,18 +503,30 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
 #pragma unroll
         for (int i = 0; i < CW; ++i) resc |= mb[i] * cs > m_run[i] + kLazy;
         if (resc) {
+          // Everything accumulated so far moves to the new reference now: O(j - 1),
+          // which the value product may still be computing, is folded in first (rare;
+          // otherwise it is folded after P(j) is published).
+          float alpha[CW];
 #pragma unroll
           for (int i = 0; i < CW; ++i) {
             const float mn = fmaxf(m_run[i], mb[i] * cs);
             alpha[i] = exp2f(m_run[i] - mn);
             m_run[i] = mn;
           }
+          if (!first) acc_o(j - 1);
+#pragma unroll
+          for (int i = 0; i < CW; ++i) {
+            o_reg[i] *= alpha[i];
+            l_part[i] *= alpha[i];
+            le_part[i] *= alpha[i];
+          }
         }
       }
       // P enters the value product as bf16 (pairs of columns packed with one
-      // round-to-nearest-even conversion); the normaliser sums the same rounded
-      // weights, so the output is an exact convex combination of V rows. A masked
-      // score is -inf and gives weight exp2(-inf) = 0.
+      // round-to-nearest-even conversion); the output's normaliser sums the same
+      // rounded weights, so the output is an exact convex combination of V rows, and
+      // the log-sum-exp's sums the exact fp32 weights. A masked score is -inf and
+      // gives weight exp2(-inf) = 0.
 #pragma unroll
       for (int i = 0; i < CW; ++i) x[i] = exp2f(fmaf(x[i], cs, -m_run[i]));
       uint32_t pk[8];
@@ -511,16 +537,10 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
         __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
         pk[jj] = *reinterpret_cast<uint32_t*>(&h2);
       }
-      if (resc) {
 #pragma unroll
-        for (int i = 0; i < CW; ++i)
-          l_part[i] = l_part[i] * alpha[i] + ((i & 1) ? __uint_as_float(pk[i >> 1] & 0xffff0000u)
-                                                      : __uint_as_float(pk[i >> 1] << 16));
-      } else {
-#pragma unroll
-        for (int i = 0; i < CW; ++i)
-          l_part[i] += (i & 1) ? __uint_as_float(pk[i >> 1] & 0xffff0000u)
-                               : __uint_as_float(pk[i >> 1] << 16);
+      for (int i = 0; i < CW; ++i) {
+        l_part[i] += (i & 1) ? __uint_as_float(pk[i >> 1] & 0xffff0000u) : __uint_as_float(pk[i >> 1] << 16);
+        le_part[i] += x[i];
       }
       // A position no query row sees may hold any bytes (an unwritten tail slot):
       // once the tile has landed, zero its V row so that its weight 0 cannot meet a
@@ -546,11 +566,11 @@ __global__ void __launch_bounds__(tcd::Shape<NREP, QL>::NTHREADS, 1)
       fence_proxy_async_smem();
       mbar_arrive(bar(B_PFULL + sb));
       // ---- fold the previous tile's O^T into the registers, with this tile's rescale
-      if (!first) acc_o(j - 1, resc, alpha);
+      if (!first && !resc) acc_o(j - 1);
       cursor_next(c, a.seq_lens, a.B, a.Hkv, BS, a.window, cap);
     }
     if (!aborted) {
-      acc_o(ntiles - 1, false, alpha);
+      acc_o(ntiles - 1);
       finalize();
     }
   }

@@ -513,6 +513,13 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
     const int tok_local = r / a.n_rep, hl = r % a.n_rep;
     PfCursor c;
     pf_begin(c, a, W, G, blockIdx.x);
+    // l sums the weights as the value product uses them (rounded to bf16, added in
+    // fp32): it divides the output, which is then an exact convex combination of V
+    // rows, and gives the log-sum-exp, which then weighs a split piece exactly as its
+    // output was normalised. With the lazy reference max a dominant key's weight is
+    // 2^d (0 < d <= 8) rather than 1; with the fp32 weights summed instead, that
+    // weight's rounding (up to 2^-8) would scale the whole output row. The reported
+    // log-sum-exp is within ln(1 + 2^-8) of the exact one.
     float m_ref = -INFINITY, l = 0.f;
     bool aborted = false;
     int pqt = 0, pg = 0;
@@ -668,11 +675,11 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       tc_fence_after();
       // p = exp2(s * scale_log2 - m_ref): one FMA and one exp2 per key. A row with no
       // visible key so far keeps m_ref = -inf; its p are all 0 (exp2(-inf)).
-      // Scores are taken in pairs: one fma.f32x2 scales and shifts two of them, one
-      // add.f32x2 adds two weights to the normaliser.
+      // Scores are taken in pairs: one fma.f32x2 scales and shifts two of them; the
+      // two rounded weights are added to the normaliser by mixed-precision adds.
       const float mneg = (m_ref == -INFINITY) ? 0.f : -m_ref;
       const uint64_t cs2 = f2pack(a.scale_log2, a.scale_log2), mn2 = f2pack(mneg, mneg);
-      uint64_t ps2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+      float lr4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t pk[16];
@@ -682,19 +689,13 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
                                           cs2, mn2));
           const float p0 = exp2f(t.x), p1 = exp2f(t.y);
           __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-          // The normaliser sums the fp32 weights; the MMA uses them rounded to bf16
-          // (relative difference up to 2^-8 per weight). With the lazy reference max a
-          // dominant key's weight is 2^d (0 < d <= 8), so its rounding scales a row that
-          // it dominates; at these shapes (d = 128, scale 1/sqrt(128)) no key dominates
-          // a row that spans two key tiles, and the effect stays near 1e-3.
-          ps2[(k >> 1) & 1] = fadd2(ps2[(k >> 1) & 1], f2pack(p0, p1));
           pk[k / 2] = *reinterpret_cast<uint32_t*>(&h2);
+          add_bf16x2_to_f32(lr4[(k >> 1) & 1], lr4[2 + ((k >> 1) & 1)], pk[k / 2]);
         }
         tmem_st16(tmem + lane_off + p_col(sb) + half * 32 + c0 / 2, pk);
       }
       {
-        const float2 s0 = f2unpack(ps2[0]), s1 = f2unpack(ps2[1]);
-        l += (s0.x + s0.y) + (s1.x + s1.y);
+        l += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
       }
       tmem_wait_st();
       tc_fence_before();

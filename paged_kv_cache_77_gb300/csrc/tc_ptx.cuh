@@ -135,6 +135,14 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
 }
+// a += low bf16 of x, b += high bf16 of x, in fp32 (mixed-precision adds: the bf16
+// values are widened exactly).
+__device__ __forceinline__ void add_bf16x2_to_f32(float& a, float& b, uint32_t x) {
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n add.rn.f32.bf16 %0, lo, %0;\n"
+      " add.rn.f32.bf16 %1, hi, %1;\n}\n"
+      : "+f"(a), "+f"(b)
+      : "r"(x));
+}
 // Named barrier that also returns whether `pred` held in any of its threads (the same
 // memory ordering as bar.sync).
 __device__ __forceinline__ bool named_bar_any(int id, int threads, bool pred) {

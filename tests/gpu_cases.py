@@ -14,6 +14,12 @@ from paged_kv_cache_77_gb300 import api
 MAX_ABS_TOL = 1e-2  # attention outputs from bf16 inputs vs the fp64 oracle
 MEAN_ABS_TOL = 1e-3
 LSE_TOL = 2e-3
+# The prefill kernel's log-sum-exp is taken from the sum of the bf16-rounded weights
+# that its output uses (the output is then an exact convex combination of V rows).
+# Round-to-nearest-even to bf16's 8 significant bits moves each weight by at most 2^-8
+# of itself, so the sum too, and its log by at most ln(1 + 2^-8) = 3.9e-3 (reached
+# when one key dominates a row); the scores' own fp32 error comes on top.
+PREFILL_LSE_TOL = 4e-3 + 5e-4
 
 
 def tables(wl: synth.Workload, d: synth.Draw):
@@ -95,7 +101,7 @@ def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
 
 
 def compare(out: torch.Tensor, lse: torch.Tensor | None, o_ref: np.ndarray, lse_ref: np.ndarray,
-            rows, what: str):
+            rows, what: str, lse_tol: float = LSE_TOL):
     """Max / mean abs error on the selected leading-index rows.
 
     A bf16 output is the kernel's fp32 result rounded to nearest even, so each element
@@ -117,7 +123,8 @@ def compare(out: torch.Tensor, lse: torch.Tensor | None, o_ref: np.ndarray, lse_
         le = lse_ref[rows]
         fin = np.isfinite(le)
         assert np.array_equal(np.isfinite(lg), fin)
-        assert np.abs(lg[fin] - le[fin]).max(initial=0) <= LSE_TOL, f"{what}: lse"
+        dl = np.abs(lg[fin] - le[fin]).max(initial=0)
+        assert dl <= lse_tol, f"{what}: lse error {dl:.3e} (|lse| up to {np.abs(le[fin]).max(initial=0):.1f})"
     return float(err.max()), float(err.mean())
 
 

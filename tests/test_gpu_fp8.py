@@ -21,11 +21,12 @@ class Fp8Case:
     against the oracle's own quantisation), with the new rows then written by the
     FP8 write and the tails of the last blocks poisoned with NaN codes and scales."""
 
-    def __init__(self, wl, d=None, check_rows=None, whole=False):
+    def __init__(self, wl, d=None, check_rows=None, whole=False, base=None):
         """``whole``: the oracle's side is left to ``oracle_fp8_all`` (per sequence, in
         a process pool), which gets host copies of the codes and scales taken here
-        right after the GPU's writes; only the GPU's tails are poisoned."""
-        self.base = DecodeCase(wl, d, poison=True)
+        right after the GPU's writes; only the GPU's tails are poisoned. ``base``: a
+        DecodeCase of (wl, d) prepared by the caller, used in place of a fresh one."""
+        self.base = base if base is not None else DecodeCase(wl, d, poison=True)
         c, wl = self.base, self.base.wl
         nb, bs, hkv, dh = c.v["k_cache"].shape
         self.nb, self.bs, self.hkv = nb, bs, hkv
