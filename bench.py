@@ -927,7 +927,7 @@ def run_decode(args, dev, world: int = 1, rank: int = 0):
             torch.cuda.current_stream().synchronize()
         t = time.perf_counter()
         # The previous step's copy ended at its synchronize, so its part can be rewritten.
-        slots_h[:] = api.build_slot_mapping(table_np, d.start_pos, d.num_new, wl.block_size)
+        api.build_slot_mapping(table_np, d.start_pos, d.num_new, wl.block_size, out=slots_h)
         stage_d.copy_(stage_h, non_blocking=True)
         api.kv_cache_write(v["k_cache"], v["v_cache"], dk, dv, slots_d)
         attend_e2e(dq)

@@ -23,12 +23,20 @@ def _ptr(t):
 
 
 def _np_ptr(a: np.ndarray):
-    return C.c_void_p(a.ctypes.data)
+    return a.ctypes.data
+
+
+# The current stream's raw handle without building a Stream object (the public
+# torch.cuda.current_stream() costs ~10 us of host time per call on the machine's cores).
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(stream=None):
-    s = torch.cuda.current_stream() if stream is None else stream
-    return s.cuda_stream
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _dev_bf16(t, name):
@@ -73,7 +81,7 @@ def check_current_device(device) -> None:
 
 
 def check_shape(t, shape, name) -> None:
-    if tuple(t.shape) != tuple(int(x) for x in shape):
+    if t.shape != tuple(shape):
         raise ValueError(f"{name} has shape {_shape_str(t.shape)}, expected {_shape_str(shape)}")
 
 
@@ -302,12 +310,19 @@ def build_block_table_arange(batch: int, blocks_per_seq: int) -> np.ndarray:
     return table
 
 
-def build_slot_mapping(block_table: np.ndarray, start_pos, num_new, block_size: int) -> np.ndarray:
+def build_slot_mapping(block_table: np.ndarray, start_pos, num_new, block_size: int,
+                       out: np.ndarray | None = None) -> np.ndarray:
+    """slot_mapping of the new rows; `out` (optional): a contiguous int32 array with room
+    for them, written in place (a view of its first entries is returned)."""
     table = np.ascontiguousarray(block_table, dtype=np.int32)
     sp = np.ascontiguousarray(start_pos, dtype=np.int32)
     nn = np.ascontiguousarray(num_new, dtype=np.int32)
     cap = int(nn.sum())
-    out = np.empty(max(cap, 1), dtype=np.int32)
+    if out is None:
+        out = np.empty(max(cap, 1), dtype=np.int32)
+    elif (not isinstance(out, np.ndarray) or out.dtype != np.int32 or out.ndim != 1
+          or not out.flags["C_CONTIGUOUS"] or len(out) < cap):
+        raise ValueError(f"out must be a contiguous 1-D int32 array of at least {cap} entries")
     n = check(load().pkv_build_slot_mapping(_np_ptr(table), table.shape[1], _np_ptr(sp),
                                             _np_ptr(nn), len(nn), block_size, _np_ptr(out), cap),
               "pkv_build_slot_mapping")
@@ -334,7 +349,7 @@ def block_num_full_online(available_bytes, per_token_bytes, block_size) -> int:
 def _cache_dims(cache, name, ndim=4):
     if cache.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dimensions [num_blocks, block_size, H_kv, d]")
-    return tuple(int(x) for x in cache.shape)
+    return tuple(cache.shape)
 
 
 def _table_and_lens(block_table, seq_lens, B, lens_name="seq_lens"):

@@ -53,6 +53,17 @@ def test_generator_matches_oracle_on_workload_draws(name):
     slots = api.build_slot_mapping(lib_table, d.start_pos, d.num_new, wl.block_size)
     ref_slots = bp.slot_mapping(ref_table, d.start_pos, d.num_new, wl.block_size)
     assert slots.dtype == np.int32 and np.array_equal(slots, ref_slots)
+    # The same slots written into a caller's buffer (a staging buffer, say), with room
+    # to spare; too small or of the wrong type is refused.
+    buf = np.full(len(ref_slots) + 7, -5, dtype=np.int32)
+    got = api.build_slot_mapping(lib_table, d.start_pos, d.num_new, wl.block_size, out=buf)
+    assert np.array_equal(got, ref_slots) and np.shares_memory(got, buf)
+    assert (buf[len(ref_slots):] == -5).all()
+    for bad in (np.zeros(max(len(ref_slots) - 1, 0), np.int32), np.zeros(len(ref_slots), np.int64)):
+        if len(ref_slots) == 0 and bad.dtype == np.int32:
+            continue
+        with pytest.raises(ValueError):
+            api.build_slot_mapping(lib_table, d.start_pos, d.num_new, wl.block_size, out=bad)
     if wl.layout == "arange":
         # The pages' simplified decode formula: slot = kv_len + b * max_seq_len.
         assert np.array_equal(slots, bp.slot_mapping_contiguous_decode(
