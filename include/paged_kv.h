@@ -225,7 +225,8 @@ int64_t pkv_manager_fork(pkv_kv_manager* mgr, int64_t parent_id, const int64_t* 
  * The MLA latent write passes cache_nope as k (H_kv 1, 512) and cache_rope as v
  * (H_kv 1, 64). A bit-exact copy; slot < 0 skips the row; slot >= num_blocks *
  * block_size skips it and sets PKV_DEV_BAD_SLOT. Duplicate slots in one call are
- * undefined (one of the rows wins). Row sizes must be multiples of 16 bytes. */
+ * undefined (one of the rows wins). Row sizes must be multiples of 16 bytes. With
+ * num_tokens = 0 nothing is launched and k, v and slot_mapping may be NULL. */
 int pkv_kv_cache_write(void* k_cache, void* v_cache, const void* k, const void* v,
                        const int32_t* slot_mapping, int64_t num_tokens, int64_t num_blocks,
                        int32_t block_size, int32_t num_kv_heads, int32_t head_dim_k,

@@ -46,7 +46,9 @@ int pkv_kv_cache_write(void* k_cache, void* v_cache, const void* k, const void* 
               PKV_ERR_INVALID_ARG, "pkv_kv_cache_write: non-positive size");
   PKV_REQUIRE(k_cache && (num_tokens == 0 || (k && slot_mapping)), PKV_ERR_INVALID_ARG,
               "pkv_kv_cache_write: null pointer");
-  PKV_REQUIRE((v_cache == nullptr) == (v == nullptr), PKV_ERR_INVALID_ARG,
+  // v goes with v_cache; with no rows to write, v may be NULL (an empty tensor's
+  // storage) either way.
+  PKV_REQUIRE(v_cache ? (num_tokens == 0 || v != nullptr) : (v == nullptr), PKV_ERR_INVALID_ARG,
               "pkv_kv_cache_write: v_cache and v must both be set or both be NULL");
   const int64_t row_k = (int64_t)num_kv_heads * head_dim_k * 2;
   const int64_t row_v = v_cache ? (int64_t)num_kv_heads * head_dim_v * 2 : 0;
