@@ -317,12 +317,15 @@ def build_slot_mapping(block_table: np.ndarray, start_pos, num_new, block_size: 
     table = np.ascontiguousarray(block_table, dtype=np.int32)
     sp = np.ascontiguousarray(start_pos, dtype=np.int32)
     nn = np.ascontiguousarray(num_new, dtype=np.int32)
-    cap = int(nn.sum())
     if out is None:
+        cap = int(nn.sum())
         out = np.empty(max(cap, 1), dtype=np.int32)
-    elif (not isinstance(out, np.ndarray) or out.dtype != np.int32 or out.ndim != 1
-          or not out.flags["C_CONTIGUOUS"] or len(out) < cap):
-        raise ValueError(f"out must be a contiguous 1-D int32 array of at least {cap} entries")
+    else:
+        # Its length is the capacity the library checks the rows against.
+        if (not isinstance(out, np.ndarray) or out.dtype != np.int32 or out.ndim != 1
+                or not out.flags["C_CONTIGUOUS"]):
+            raise ValueError("out must be a contiguous 1-D int32 array")
+        cap = len(out)
     n = check(load().pkv_build_slot_mapping(_np_ptr(table), table.shape[1], _np_ptr(sp),
                                             _np_ptr(nn), len(nn), block_size, _np_ptr(out), cap),
               "pkv_build_slot_mapping")
