@@ -327,7 +327,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::NTHREADS, 1)
       const int blk = __ldg(a.block_table + (int64_t)seq_of(a, c.b) * a.max_blocks + tok0 / BS);
       const bool ok = blk >= 0 && (int64_t)blk < a.num_blocks;
       const int row = ok ? blk * BS + (tok0 % BS) : rows_oob;
-      if (!mbar_wait_sleepy(bar(B_KEMPTY + st), ((j / NST) & 1) ^ 1)) { fail(); break; }
+      if (!mbar_wait(bar(B_KEMPTY + st), ((j / NST) & 1) ^ 1)) { fail(); break; }
       if (!ok) flag_status(a.dev_status, PKV_DEV_BAD_BLOCK);
       const uint32_t ks = sbase + OFF_K + st * STAGE;
       mbar_expect_tx(bar(B_KFULL + st), STAGE);
