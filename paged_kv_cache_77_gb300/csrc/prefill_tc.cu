@@ -58,6 +58,20 @@ constexpr int M = 128;
 constexpr int NQ = PKV_PF_NQ;    // Q buffers
 constexpr int NK = PKV_PF_NK;    // K ring: a K tile is released once its score product is done
 constexpr int NV = 7 - NQ - NK;  // V ring: a V tile is released after its value product
+#ifndef PKV_PF_NPB
+#define PKV_PF_NPB 3
+#endif
+#ifndef PKV_PF_NOB
+#define PKV_PF_NOB 1
+#endif
+// Tensor memory: P buffers (64 columns each) and O buffers (128 columns each) after
+// the 128 columns of S. A third P buffer (the softmax of block j waits for O(j - 3)
+// rather than O(j - 2)) beats a second O buffer (which spares the next unit's value
+// products the read-out of the previous unit's O): 882.5 against 904.4 us on the
+// mixed prefill workload; a fourth P buffer measured 926.6 us.
+constexpr int NPB = PKV_PF_NPB;
+constexpr int NOB = PKV_PF_NOB;
+static_assert(NPB >= 2 && NOB >= 1 && 128 + NPB * 64 + NOB * 128 <= 512, "tensor memory");
 static_assert(NQ >= 1 && NQ <= 2 && NK >= 2 && NV >= 2,
               "prefill ring");
 constexpr int NTHREADS = 384;    // warp 0 Q/K loads, 1 score MMAs, 2 V loads, 3 value MMAs, 4-11 softmax
@@ -78,13 +92,13 @@ enum {
   B_SFULL = B_QEMPTY + 2,
   B_SEMPTY = B_SFULL + 2,
   B_PFULL = B_SEMPTY + 2,
-  B_PEMPTY = B_PFULL + 2,
-  // One commit after each value product O(j) completes phase j/2 of barrier j%2:
-  // "P buffer free" and "O holds block j" are the same event, so one barrier pair
-  // serves both.
+  B_PEMPTY = B_PFULL + NPB,
+  // One commit after each value product O(j) completes phase j / NPB of barrier
+  // j % NPB: "P buffer free" and "O holds block j" are the same event, so one set of
+  // barriers serves both.
   B_ODONE = B_PEMPTY,
-  B_OFREE = B_PEMPTY + 2,  // per O buffer
-  B_COUNT = B_OFREE + 2
+  B_OFREE = B_PEMPTY + NPB,  // per O buffer
+  B_COUNT = B_OFREE + NOB
 };
 constexpr int OFF_XCH = OFF_BAR + B_COUNT * 8;      // float [2 halves][128 rows]
 constexpr int OFF_AFL = OFF_XCH + 2 * 128 * 4;      // int [2 halves][4 quarters] abort votes
@@ -93,13 +107,12 @@ constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 constexpr uint32_t TMEM_COLS = 512;
 // Tensor memory (512 columns): one S buffer (the next score product is issued once the
-// softmax has read S into registers), two P buffers of 64 columns (128 bf16 weights
-// packed in pairs), and two O buffers: a unit accumulates into the O buffer its
-// predecessor did not use, so reading out one unit's O never stalls the next unit's
-// value products.
+// softmax has read S into registers), NPB P buffers of 64 columns (128 bf16 weights
+// packed in pairs), and NOB O buffers: a unit accumulates into the O buffer after its
+// predecessor's, which its first value product waits for until that one is read out.
 __device__ __forceinline__ uint32_t s_col(int) { return 0; }
 __device__ __forceinline__ uint32_t p_col(int b) { return 128 + b * 64; }
-__device__ __forceinline__ uint32_t o_col(int ob) { return 256 + ob * 128; }
+__device__ __forceinline__ uint32_t o_col(int ob) { return 128 + NPB * 64 + ob * 128; }
 }  // namespace pf
 
 struct PrefillArgs {
@@ -323,11 +336,12 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       mbar_init(bar(B_QEMPTY + i), 1);
       mbar_init(bar(B_SFULL + i), 1);
       mbar_init(bar(B_SEMPTY + i), NSM);
+    }
+    for (int i = 0; i < NPB; ++i) {
       mbar_init(bar(B_PFULL + i), NSM);
       mbar_init(bar(B_PEMPTY + i), 1);
     }
-    mbar_init(bar(B_OFREE), NSM);
-    mbar_init(bar(B_OFREE + 1), NSM);
+    for (int i = 0; i < NOB; ++i) mbar_init(bar(B_OFREE + i), NSM);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -464,19 +478,19 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
     bool ok = true;
     for (int j = 0; j < ntiles && !*abort_flag; ++j) {
       const bool first = (j == 0) || (c.j == 0) || c.range_start;
-      const int st = j % NV, sb = j & 1;
+      const int st = j % NV, sb = j % NPB;
       if (!mbar_wait(bar(B_VFULL + st), (j / NV) & 1)) { ok = false; break; }
-      if (!mbar_wait(bar(B_PFULL + sb), (j >> 1) & 1)) { ok = false; break; }
+      if (!mbar_wait(bar(B_PFULL + sb), (j / NPB) & 1)) { ok = false; break; }
       if (first) {
         ++piece_o;
-        if (!mbar_wait(bar(B_OFREE + (piece_o & 1)), ((piece_o >> 1) & 1) ^ 1)) { ok = false; break; }
+        if (!mbar_wait(bar(B_OFREE + piece_o % NOB), ((piece_o / NOB) & 1) ^ 1)) { ok = false; break; }
       }
       tc_fence_after();
       const uint64_t vd = smem_desc(sbase + OFF_V + st * TILE, HALF, 1024, kSwizzle128);
       const uint32_t pt = tmem + p_col(sb);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tmem + o_col(piece_o & 1), pt + kk * 8, desc_add(vd, kk * 2048), ID_O, !(first && kk == 0));
+        mma_ts(tmem + o_col(piece_o % NOB), pt + kk * 8, desc_add(vd, kk * 2048), ID_O, !(first && kk == 0));
       mma_commit(bar(B_PEMPTY + sb));
       mma_commit(bar(B_VEMPTY + st));
       pf_next(c, a);
@@ -531,7 +545,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
     auto finalize = [&](int jl) {
       // Row normaliser: sum of both halves.
       const float lt = l + exchange(l);
-      if (!mbar_wait(bar(B_ODONE + (jl & 1)), (jl >> 1) & 1)) fail();
+      if (!mbar_wait(bar(B_ODONE + jl % NPB), (jl / NPB) & 1)) fail();
       __syncwarp();
       tc_fence_after();
       const int tok = pqt * a.qt_tokens + tok_local;  // query index inside the sequence
@@ -600,9 +614,9 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
         p_vcta = (int64_t)c.round * G + blockIdx.x;
         p_start = (c.t == c.seg_base);
         p_whole = p_start && (c.seg_base + c.n <= c.t_end);
-        pob = (pob < 0) ? 0 : (pob ^ 1);  // O buffer of this piece (alternates)
+        pob = (pob < 0) ? 0 : (pob + 1) % NOB;  // O buffer of this piece (in turn)
       }
-      const int sb = j & 1;  // P buffer
+      const int sb = j % NPB;  // P buffer
       if (!mbar_wait(bar(B_SFULL), j & 1)) fail();
       __syncwarp();
       tc_fence_after();
@@ -639,7 +653,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
         const float m_new = need ? mt : m_ref;
         const float alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - m_new);
         if (!first) {
-          if (!mbar_wait(bar(B_ODONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) fail();
+          if (!mbar_wait(bar(B_ODONE + (j - 1) % NPB), ((j - 1) / NPB) & 1)) fail();
           __syncwarp();
           tc_fence_after();
           // 16 columns at a time: the 64 scores of this block are live here.
@@ -670,7 +684,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
         for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(vrow + q * 16) = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
       }
-      if (!mbar_wait(bar(B_PEMPTY + sb), ((j >> 1) & 1) ^ 1)) fail();
+      if (!mbar_wait(bar(B_PEMPTY + sb), ((j / NPB) & 1) ^ 1)) fail();
       __syncwarp();
       tc_fence_after();
       // p = exp2(s * scale_log2 - m_ref): one FMA and one exp2 per key. A row with no
