@@ -64,14 +64,23 @@ constexpr int NV = 7 - NQ - NK;  // V ring: a V tile is released after its value
 #ifndef PKV_PF_NOB
 #define PKV_PF_NOB 1
 #endif
-// Tensor memory: P buffers (64 columns each) and O buffers (128 columns each) after
-// the 128 columns of S. A third P buffer (the softmax of block j waits for O(j - 3)
-// rather than O(j - 2)) beats a second O buffer (which spares the next unit's value
-// products the read-out of the previous unit's O): 882.5 against 904.4 us on the
-// mixed prefill workload; a fourth P buffer measured 926.6 us.
+#ifndef PKV_PF_ALIAS
+#define PKV_PF_ALIAS 1
+#endif
+// PKV_PF_ALIAS 1: NPB buffers of 128 columns each hold S(j) and then, over the
+// columns the softmax has read, P(j); S(j) waits only for O(j - NPB) to free its
+// buffer, so the score product runs NPB - 1 blocks ahead of the softmax.
+// PKV_PF_ALIAS 0: one S buffer (the next score product waits until the softmax has
+// read S) and NPB P buffers of 64 columns. Either way NOB O buffers of 128 columns.
+// Measured on the mixed prefill workload: unaliased, 3 P buffers and 1 O buffer
+// 882.5 us against 904.4 with 2 and 2 and 926.6 with 4 and 1; aliased with 3 buffers
+// 877.8 against 890.9 unaliased on one box.
+constexpr bool kAlias = PKV_PF_ALIAS != 0;
 constexpr int NPB = PKV_PF_NPB;
 constexpr int NOB = PKV_PF_NOB;
-static_assert(NPB >= 2 && NOB >= 1 && 128 + NPB * 64 + NOB * 128 <= 512, "tensor memory");
+static_assert(NPB >= 2 && NOB >= 1 &&
+                  (kAlias ? NPB * 128 + NOB * 128 : 128 + NPB * 64 + NOB * 128) <= 512,
+              "tensor memory");
 static_assert(NQ >= 1 && NQ <= 2 && NK >= 2 && NV >= 2,
               "prefill ring");
 constexpr int NTHREADS = 384;    // warp 0 Q/K loads, 1 score MMAs, 2 V loads, 3 value MMAs, 4-11 softmax
@@ -89,8 +98,8 @@ enum {
   B_VEMPTY = B_VFULL + NV,
   B_QFULL = B_VEMPTY + NV,
   B_QEMPTY = B_QFULL + 2,
-  B_SFULL = B_QEMPTY + 2,
-  B_SEMPTY = B_SFULL + 2,
+  B_SFULL = B_QEMPTY + 2,  // [NPB] aliased, else [0] only
+  B_SEMPTY = B_SFULL + NPB,
   B_PFULL = B_SEMPTY + 2,
   B_PEMPTY = B_PFULL + NPB,
   // One commit after each value product O(j) completes phase j / NPB of barrier
@@ -106,13 +115,15 @@ constexpr int OFF_MISC = OFF_AFL + 2 * 4 * 4;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 constexpr uint32_t TMEM_COLS = 512;
-// Tensor memory (512 columns): one S buffer (the next score product is issued once the
-// softmax has read S into registers), NPB P buffers of 64 columns (128 bf16 weights
-// packed in pairs), and NOB O buffers: a unit accumulates into the O buffer after its
-// predecessor's, which its first value product waits for until that one is read out.
-__device__ __forceinline__ uint32_t s_col(int) { return 0; }
-__device__ __forceinline__ uint32_t p_col(int b) { return 128 + b * 64; }
-__device__ __forceinline__ uint32_t o_col(int ob) { return 128 + NPB * 64 + ob * 128; }
+// Tensor memory (512 columns): S and P buffers as above (P holds 128 bf16 weights
+// packed in pairs in 64 columns), then NOB O buffers: a unit accumulates into the O
+// buffer after its predecessor's, which its first value product waits for until that
+// one is read out.
+__device__ __forceinline__ uint32_t s_col(int b) { return kAlias ? b * 128 : 0; }
+// P of buffer b; aliased, half h of a row writes its 32 columns at the start of the
+// 64 S columns it read (the value product's K-steps 4h..4h+3 read them there).
+__device__ __forceinline__ uint32_t p_col(int b, int h) { return kAlias ? b * 128 + h * 64 : 128 + b * 64 + h * 32; }
+__device__ __forceinline__ uint32_t o_col(int ob) { return (kAlias ? NPB * 128 : 128 + NPB * 64) + ob * 128; }
 }  // namespace pf
 
 struct PrefillArgs {
@@ -334,10 +345,10 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_QFULL + i), 1);
       mbar_init(bar(B_QEMPTY + i), 1);
-      mbar_init(bar(B_SFULL + i), 1);
       mbar_init(bar(B_SEMPTY + i), NSM);
     }
     for (int i = 0; i < NPB; ++i) {
+      mbar_init(bar(B_SFULL + i), 1);
       mbar_init(bar(B_PFULL + i), NSM);
       mbar_init(bar(B_PEMPTY + i), 1);
     }
@@ -454,16 +465,23 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       const int qb = piece_s % NQ;
       if (first && !mbar_wait(bar(B_QFULL + qb), (piece_s / NQ) & 1)) { ok = false; break; }
       if (!mbar_wait(bar(B_KFULL + st), (j / NK) & 1)) { ok = false; break; }
-      if (!mbar_wait(bar(B_SEMPTY), (j & 1) ^ 1)) { ok = false; break; }  // softmax has read S(j-1)
+      const int sbuf = kAlias ? j % NPB : 0;
+      if (kAlias) {
+        // S/P buffer j % NPB is free once O(j - NPB) has read P(j - NPB) from it.
+        if (!mbar_wait(bar(B_ODONE + sbuf), ((j / NPB) & 1) ^ 1)) { ok = false; break; }
+      } else if (!mbar_wait(bar(B_SEMPTY), (j & 1) ^ 1)) {  // softmax has read S(j-1)
+        ok = false;
+        break;
+      }
       tc_fence_after();
       // Base descriptors once per tile; each K step only adds a constant offset.
       const uint64_t qd = smem_desc(sbase + OFF_Q + qb * TILE, 16, 1024, kSwizzle128);
       const uint64_t kd = smem_desc(sbase + OFF_K + st * TILE, 16, 1024, kSwizzle128);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ss(tmem + s_col(0), desc_add(qd, (kk >> 2) * HALF + (kk & 3) * 32),
+        mma_ss(tmem + s_col(sbuf), desc_add(qd, (kk >> 2) * HALF + (kk & 3) * 32),
                desc_add(kd, (kk >> 2) * HALF + (kk & 3) * 32), ID_S, kk > 0);
-      mma_commit(bar(B_SFULL));
+      mma_commit(bar(B_SFULL + sbuf));
       mma_commit(bar(B_KEMPTY + st));
       if (last) mma_commit(bar(B_QEMPTY + qb));
       pf_next(c, a);
@@ -487,10 +505,10 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       }
       tc_fence_after();
       const uint64_t vd = smem_desc(sbase + OFF_V + st * TILE, HALF, 1024, kSwizzle128);
-      const uint32_t pt = tmem + p_col(sb);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tmem + o_col(piece_o % NOB), pt + kk * 8, desc_add(vd, kk * 2048), ID_O, !(first && kk == 0));
+        mma_ts(tmem + o_col(piece_o % NOB), tmem + p_col(sb, kk >> 2) + (kk & 3) * 8, desc_add(vd, kk * 2048),
+               ID_O, !(first && kk == 0));
       mma_commit(bar(B_PEMPTY + sb));
       mma_commit(bar(B_VEMPTY + st));
       pf_next(c, a);
@@ -617,7 +635,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
         pob = (pob < 0) ? 0 : (pob + 1) % NOB;  // O buffer of this piece (in turn)
       }
       const int sb = j % NPB;  // P buffer
-      if (!mbar_wait(bar(B_SFULL), j & 1)) fail();
+      if (kAlias ? !mbar_wait(bar(B_SFULL + sb), (j / NPB) & 1) : !mbar_wait(bar(B_SFULL), j & 1)) fail();
       __syncwarp();
       tc_fence_after();
       // Visible keys of this row in block c.j: key < kvlen and (causal) key <= c + tok.
@@ -631,7 +649,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       tmem_ld32(tmem + lane_off + s_col(sb) + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bar(B_SEMPTY));
+      if (!kAlias) mbar_arrive(bar(B_SEMPTY));
       if (!__all_sync(0xffffffffu, nvis >= 64)) {
 #pragma unroll
         for (int k = 0; k < 64; ++k)
@@ -684,7 +702,8 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
         for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(vrow + q * 16) = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
       }
-      if (!mbar_wait(bar(B_PEMPTY + sb), ((j / NPB) & 1) ^ 1)) fail();
+      // Aliased, buffer sb is this tile's until P(j) is published.
+      if (!kAlias && !mbar_wait(bar(B_PEMPTY + sb), ((j / NPB) & 1) ^ 1)) fail();
       __syncwarp();
       tc_fence_after();
       // p = exp2(s * scale_log2 - m_ref): one FMA and one exp2 per key. A row with no
@@ -706,7 +725,7 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
           pk[k / 2] = *reinterpret_cast<uint32_t*>(&h2);
           add_bf16x2_to_f32(lr4[(k >> 1) & 1], lr4[2 + ((k >> 1) & 1)], pk[k / 2]);
         }
-        tmem_st16(tmem + lane_off + p_col(sb) + half * 32 + c0 / 2, pk);
+        tmem_st16(tmem + lane_off + p_col(sb, half) + c0 / 2, pk);
       }
       {
         l += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
