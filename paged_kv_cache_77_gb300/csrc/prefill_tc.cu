@@ -15,12 +15,17 @@
 //   S [128 x 128] = Q [128 x 128 d] . K_blk^T          (tcgen05, fp32 in TMEM)
 //   O [128 x 128] += P [128 x 128 keys] . V_blk         (P bf16 in TMEM, V MN-major)
 //
+// S of block j and then its P share one of three tensor-memory buffers (P is written
+// over the S columns already read), so the score product runs up to two blocks ahead
+// of the softmax; one O buffer holds the unit's output.
 // Softmax: eight warps, two per TMEM lane quarter, each owning half of every row's
 // 128 scores; the running max is raised only when a block exceeds it by more than
-// 8 (log2 units), and O in TMEM is rescaled only then (warp-uniform).
-// Loads: warp 0 streams Q and K tiles (K ring 2 deep, a tile freed as soon as its
-// score product completes), warp 2 streams V tiles (3 deep). Warp 1 issues the
-// score products and warp 3 the value products, so neither waits behind the other.
+// 8 (log2 units), and O in TMEM is rescaled only then (warp-uniform). The output is
+// divided by the sum of the weights as the value product uses them (bf16).
+// Loads: warp 0 streams Q and K tiles (one Q buffer, K ring 3 deep, a tile freed as
+// soon as its score product completes), warp 2 streams V tiles (3 deep). Warp 1
+// issues the score products and warp 3 the value products, so neither waits behind
+// the other.
 // Work split: stream-K over all (unit, key block) tiles in kRounds rounds (see
 // pf_vbound), one persistent CTA per SM with an equal share of every round; a unit
 // cut by a range boundary leaves partial (o, lse) pieces that prefill_merge_kernel
