@@ -55,7 +55,7 @@ def cache_write(cache_bits: np.ndarray, rows_bits: np.ndarray, slot_mapping) -> 
     out = np.array(cache_bits, dtype=np.uint16, copy=True)
     nb, bs = out.shape[0], out.shape[1]
     flat = out.reshape(nb * bs, -1)
-    rows = np.asarray(rows_bits, dtype=np.uint16).reshape(len(slot_mapping), -1)
+    rows = np.asarray(rows_bits, dtype=np.uint16).reshape(len(slot_mapping), flat.shape[1])
     for t, s in enumerate(np.asarray(slot_mapping).reshape(-1)):
         s = int(s)
         if s < 0:

@@ -41,6 +41,9 @@ def test_cache_write_touches_only_target_rows():
     assert np.array_equal(cache.reshape(32, -1), flat_in)  # input not modified
     with pytest.raises(IndexError):
         ref.cache_write(cache, rows[:1], np.array([32]))
+    # No rows to write (a step with no new tokens): the cache comes back unchanged.
+    empty = ref.cache_write(cache, rows[:0], np.array([], dtype=np.int64))
+    assert np.array_equal(empty, cache)
 
 
 def test_worked_slot_write_lands_at_block_18_offset_44():
