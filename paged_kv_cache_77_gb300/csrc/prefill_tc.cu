@@ -12,16 +12,21 @@
 // 3-D TMA box {64 d, n_rep heads, 128/n_rep tokens} loads it and the group's K/V
 // tile serves all of them. Per 128-key block of the unit's causal range:
 //
-//   S [128 x 128] = Q [128 x 128 d] . K_blk^T          (tcgen05, fp32 in TMEM)
-//   O [128 x 128] += P [128 x 128 keys] . V_blk         (P bf16 in TMEM, V MN-major)
+//   S [128 x 128] = Q [128 x 128 d] . K_blk^T                  (tcgen05, fp32 in TMEM)
+//   O_h [128 x 128] += P_h [128 x 64 keys] . V_blk[64h, 64h + 64)  (P bf16 in TMEM, V MN-major)
 //
-// S of block j and then its P share one of three tensor-memory buffers (P is written
-// over the S columns already read), so the score product runs up to two blocks ahead
-// of the softmax; one O buffer holds the unit's output.
-// Softmax: eight warps, two per TMEM lane quarter, each owning half of every row's
-// 128 scores; the running max is raised only when a block exceeds it by more than
-// 8 (log2 units), and O in TMEM is rescaled only then (warp-uniform). The output is
-// divided by the sum of the weights as the value product uses them (bf16).
+// S of block j and then its P share one of two tensor-memory buffers (P is written
+// over the S columns already read), so the score product runs a block ahead of the
+// softmax; two O accumulators hold the unit's output, one per key half.
+// Softmax: eight warps, two per TMEM lane quarter. Warp half h owns keys
+// [64h, 64h + 64) of every block of its 32 rows, with its own running max, normaliser
+// and accumulator O_h, so the two warps of a row never wait for each other inside a
+// unit; they combine (m_h, l_h, O_h) by the log-sum-exp rule when the unit ends. Each
+// running max is raised only when a block exceeds it by more than 8 (log2 units), and
+// O_h in TMEM is rescaled only then (warp-uniform). Each half's normaliser sums the
+// weights as the value product uses them (bf16). Built with PKV_PF_SPLIT=0 the two
+// warps share one max, normaliser and O (three S/P buffers), exchanging the row max
+// through shared memory every block.
 // Loads: warp 0 streams Q and K tiles (one Q buffer, K ring 3 deep, a tile freed as
 // soon as its score product completes), warp 2 streams V tiles (3 deep). Warp 1
 // issues the score products and warp 3 the value products, so neither waits behind
@@ -63,8 +68,15 @@ constexpr int M = 128;
 constexpr int NQ = PKV_PF_NQ;    // Q buffers
 constexpr int NK = PKV_PF_NK;    // K ring: a K tile is released once its score product is done
 constexpr int NV = 7 - NQ - NK;  // V ring: a V tile is released after its value product
+#ifndef PKV_PF_SPLIT
+#define PKV_PF_SPLIT 1
+#endif
 #ifndef PKV_PF_NPB
+#if PKV_PF_SPLIT
+#define PKV_PF_NPB 2
+#else
 #define PKV_PF_NPB 3
+#endif
 #endif
 #ifndef PKV_PF_NOB
 #define PKV_PF_NOB 1
@@ -81,11 +93,19 @@ constexpr int NV = 7 - NQ - NK;  // V ring: a V tile is released after its value
 // 882.5 us against 904.4 with 2 and 2 and 926.6 with 4 and 1; aliased with 3 buffers
 // 877.8 against 890.9 unaliased on one box.
 constexpr bool kAlias = PKV_PF_ALIAS != 0;
+// PKV_PF_SPLIT 1: the two softmax warps of a row keep separate running maxima,
+// normalisers and O accumulators, one for keys [0, 64) and one for keys [64, 128) of
+// every block, and combine them once per unit; no per-block exchange couples them.
+// Tensor memory then holds two S/P buffers and the two O halves. Measured on the mixed
+// prefill workload (per call, two boxes, each A/B on one box): 848 against 877 us and
+// 874.7 against 877.4 us for the unsplit kernel with three S/P buffers.
+constexpr bool kSplit = PKV_PF_SPLIT != 0;
 constexpr int NPB = PKV_PF_NPB;
 constexpr int NOB = PKV_PF_NOB;
 static_assert(NPB >= 2 && NOB >= 1 &&
-                  (kAlias ? NPB * 128 + NOB * 128 : 128 + NPB * 64 + NOB * 128) <= 512,
+                  (kAlias ? NPB * 128 + (kSplit ? 2 : NOB) * 128 : 128 + NPB * 64 + NOB * 128) <= 512,
               "tensor memory");
+static_assert(!kSplit || (kAlias && NOB == 1), "split halves need aliased S/P buffers and one O pair");
 static_assert(NQ >= 1 && NQ <= 2 && NK >= 2 && NV >= 2,
               "prefill ring");
 constexpr int NTHREADS = 384;    // warp 0 Q/K loads, 1 score MMAs, 2 V loads, 3 value MMAs, 4-11 softmax
@@ -105,14 +125,15 @@ enum {
   B_QEMPTY = B_QFULL + 2,
   B_SFULL = B_QEMPTY + 2,  // [NPB] aliased, else [0] only
   B_SEMPTY = B_SFULL + NPB,
-  B_PFULL = B_SEMPTY + 2,
-  B_PEMPTY = B_PFULL + NPB,
+  B_PFULL = B_SEMPTY + 2,  // [NPB] or, split, [NPB][2 halves]
+  B_PEMPTY = B_PFULL + NPB * (kSplit ? 2 : 1),
   // One commit after each value product O(j) completes phase j / NPB of barrier
   // j % NPB: "P buffer free" and "O holds block j" are the same event, so one set of
   // barriers serves both.
   B_ODONE = B_PEMPTY,
   B_OFREE = B_PEMPTY + NPB,  // per O buffer
-  B_COUNT = B_OFREE + NOB
+  B_XCH = B_OFREE + NOB,     // split: per lane quarter, the halves' end-of-unit exchange
+  B_COUNT = B_XCH + (kSplit ? 4 : 0)
 };
 constexpr int OFF_XCH = OFF_BAR + B_COUNT * 8;      // float [2 halves][128 rows]
 constexpr int OFF_AFL = OFF_XCH + 2 * 128 * 4;      // int [2 halves][4 quarters] abort votes
@@ -129,6 +150,8 @@ __device__ __forceinline__ uint32_t s_col(int b) { return kAlias ? b * 128 : 0; 
 // 64 S columns it read (the value product's K-steps 4h..4h+3 read them there).
 __device__ __forceinline__ uint32_t p_col(int b, int h) { return kAlias ? b * 128 + h * 64 : 128 + b * 64 + h * 32; }
 __device__ __forceinline__ uint32_t o_col(int ob) { return (kAlias ? NPB * 128 : 128 + NPB * 64) + ob * 128; }
+// Split: O_h accumulates the value products of keys [64h, 64h + 64) of every block.
+__device__ __forceinline__ uint32_t o_half(int h) { return NPB * 128 + h * 128; }
 }  // namespace pf
 
 struct PrefillArgs {
@@ -354,10 +377,12 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
     }
     for (int i = 0; i < NPB; ++i) {
       mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_PFULL + i), NSM);
       mbar_init(bar(B_PEMPTY + i), 1);
     }
+    for (int i = 0; i < NPB * (kSplit ? 2 : 1); ++i) mbar_init(bar(B_PFULL + i), kSplit ? NSM / 2 : NSM);
     for (int i = 0; i < NOB; ++i) mbar_init(bar(B_OFREE + i), NSM);
+    if (kSplit)
+      for (int i = 0; i < 4; ++i) mbar_init(bar(B_XCH + i), 64);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -503,22 +528,259 @@ __global__ void __launch_bounds__(pf::NTHREADS, 1)
       const bool first = (j == 0) || (c.j == 0) || c.range_start;
       const int st = j % NV, sb = j % NPB;
       if (!mbar_wait(bar(B_VFULL + st), (j / NV) & 1)) { ok = false; break; }
-      if (!mbar_wait(bar(B_PFULL + sb), (j / NPB) & 1)) { ok = false; break; }
-      if (first) {
-        ++piece_o;
-        if (!mbar_wait(bar(B_OFREE + piece_o % NOB), ((piece_o / NOB) & 1) ^ 1)) { ok = false; break; }
-      }
-      tc_fence_after();
       const uint64_t vd = smem_desc(sbase + OFF_V + st * TILE, HALF, 1024, kSwizzle128);
+      if (kSplit) {
+        // O_h += P_h . V rows [64h, 64h + 64): each half's product issues as soon as
+        // that half's weights are published.
+        if (first) {
+          ++piece_o;
+          if (!mbar_wait(bar(B_OFREE), (piece_o & 1) ^ 1)) { ok = false; break; }
+        }
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (!mbar_wait(bar(B_PFULL + sb * 2 + h), (j / NPB) & 1)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tmem + o_col(piece_o % NOB), tmem + p_col(sb, kk >> 2) + (kk & 3) * 8, desc_add(vd, kk * 2048),
-               ID_O, !(first && kk == 0));
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + o_half(h), tmem + p_col(sb, h) + kk * 8, desc_add(vd, (4 * h + kk) * 2048), ID_O,
+                   !(first && kk == 0));
+        }
+        if (!ok) break;
+      } else {
+        if (!mbar_wait(bar(B_PFULL + sb), (j / NPB) & 1)) { ok = false; break; }
+        if (first) {
+          ++piece_o;
+          if (!mbar_wait(bar(B_OFREE + piece_o % NOB), ((piece_o / NOB) & 1) ^ 1)) { ok = false; break; }
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + o_col(piece_o % NOB), tmem + p_col(sb, kk >> 2) + (kk & 3) * 8, desc_add(vd, kk * 2048),
+                 ID_O, !(first && kk == 0));
+      }
       mma_commit(bar(B_PEMPTY + sb));
       mma_commit(bar(B_VEMPTY + st));
       pf_next(c, a);
     }
     if (!ok) fail();
+  } else if (kSplit && ntiles > 0 && warp >= 4) {
+    // ------------------------------------------------------------ softmax / epilogue (split)
+    // Warp w handles rows quarter*32 + lane and keys [half*64, half*64 + 64) of every
+    // block, with its own running max m_h, normaliser l_h and accumulator O_h, as if
+    // the unit's keys were two sequences merged at the end. The two warps of a row
+    // never wait for each other inside a unit, so their exp2 phases need not line up.
+    // At the end of a unit they exchange (m_h, l_h) and each writes half of the
+    // output columns: o = (2^(m_0 - M) O_0 + 2^(m_1 - M) O_1) / (2^(m_0 - M) l_0 +
+    // 2^(m_1 - M) l_1), M = max(m_0, m_1).
+    const int quarter = warp & 3;
+    const int half = (warp - 4) >> 2;
+    const int r = quarter * 32 + lane;  // row = token_local * n_rep + head
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    float* xch = reinterpret_cast<float*>(base + OFF_XCH);  // [2 halves][128 rows]
+    // Keys past the sequence's end: this thread clears key zkey's d-half zdh of the V
+    // tile (the half's 128 threads cover its 64 keys).
+    const int zkey = half * 64 + (r & 63), zdh = r >> 6;
+    int xph = 0;  // phases completed on this quarter's exchange barrier
+    // One value to the other half of the row and one back: write, meet, read, meet
+    // again so that the next exchange cannot overwrite an unread value. Bounded waits,
+    // their outcome made warp-uniform (tensor-memory loads follow).
+    auto pair_xch = [&](float v, float& other) -> bool {
+      xch[half * 128 + r] = v;
+      mbar_arrive(bar(B_XCH + quarter));
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_XCH + quarter), xph & 1))) return false;
+      ++xph;
+      other = xch[(half ^ 1) * 128 + r];
+      mbar_arrive(bar(B_XCH + quarter));
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_XCH + quarter), xph & 1))) return false;
+      ++xph;
+      return true;
+    };
+    const int tok_local = r / a.n_rep, hl = r % a.n_rep;
+    PfCursor c;
+    pf_begin(c, a, W, G, blockIdx.x);
+    // l sums the weights as the value product uses them (rounded to bf16, added in
+    // fp32), as in the unsplit path.
+    float m_ref = -INFINITY, l = 0.f;
+    bool aborted = false;
+    int pqt = 0, pg = 0;
+    int64_t p_vcta = 0;
+    PfSeq ps{};
+    bool p_start = false, p_whole = false;
+
+    auto finalize = [&](int jl) -> bool {
+      float m_o = -INFINITY, l_o = 0.f;
+      if (!pair_xch(m_ref, m_o) || !pair_xch(l, l_o)) return false;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_ODONE + jl % NPB), (jl / NPB) & 1))) return false;
+      __syncwarp();
+      tc_fence_after();
+      const float mx = fmaxf(m_ref, m_o);
+      const float a_own = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - mx);
+      const float a_oth = (m_o == -INFINITY) ? 0.f : exp2f(m_o - mx);
+      const float lt = l * a_own + l_o * a_oth;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float lse2 = lt > 0.f ? mx + log2f(lt) : -INFINITY;
+      const float w0 = (half == 0 ? a_own : a_oth) * inv, w1 = (half == 0 ? a_oth : a_own) * inv;
+      const int tok = pqt * a.qt_tokens + tok_local;  // query index inside the sequence
+      const bool row_ok = tok < ps.qlen;
+      const int64_t grow = (int64_t)(ps.q0 + tok) * a.H + (int64_t)pg * a.n_rep + hl;  // [T, H] row
+      const int64_t slot = p_vcta * 2 + (p_start ? 1 : 0);
+      for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tmem + lane_off + o_half(0) + c0, v0);
+        tmem_ld32(tmem + lane_off + o_half(1) + c0, v1);
+        tmem_wait_ld();
+        float f[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) f[k] = fmaf(__uint_as_float(v0[k]), w0, __uint_as_float(v1[k]) * w1);
+        if (p_whole) {
+          if (!row_ok) continue;
+          if (a.out_f32) {
+            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + grow * D + c0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[k] = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+          } else {
+            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + grow * D + c0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(f[8 * k + 2 * e], f[8 * k + 2 * e + 1]);
+                w[e] = *reinterpret_cast<uint32_t*>(&h2);
+              }
+              o[k] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        } else {
+          float4* o = reinterpret_cast<float4*>(a.ws_o + (slot * M + r) * D + c0);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) o[k] = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+        }
+      }
+      if (half == 0) {
+        if (p_whole) {
+          if (row_ok && a.lse) a.lse[grow] = lse2 * kLn2;
+        } else {
+          a.ws_lse[slot * M + r] = lse2;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(B_OFREE));
+      return true;
+    };
+
+    // The block id of a tile is loaded one tile ahead, off the path from S to P.
+    int blk_next = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.j);
+    for (int j = 0; j < ntiles; ++j) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+        aborted = true;
+        break;
+      }
+      const bool first = (j == 0) || (c.j == 0) || c.range_start;
+      const int blk = blk_next;
+      if (first) {
+        if (j > 0 && !finalize(j - 1)) {
+          fail();
+          aborted = true;
+          break;
+        }
+        m_ref = -INFINITY;
+        l = 0.f;
+        pqt = c.qt;
+        pg = c.g;
+        ps = c.s;
+        p_vcta = (int64_t)c.round * G + blockIdx.x;
+        p_start = (c.t == c.seg_base);
+        p_whole = p_start && (c.seg_base + c.n <= c.t_end);
+      }
+      const int sb = j % NPB;
+      if (!mbar_wait(bar(B_SFULL + sb), (j / NPB) & 1)) fail();
+      __syncwarp();
+      tc_fence_after();
+      // Visible keys of this row in block c.j: key < kvlen and (causal) key <= c + tok.
+      const int tok = c.qt * a.qt_tokens + tok_local;
+      const int key_end = a.causal ? min(c.s.c + tok + 1, c.s.kvlen) : c.s.kvlen;
+      const bool blk_ok = blk >= 0 && (int64_t)blk < a.num_blocks;
+      const int nvis = blk_ok ? max(0, min(64, key_end - c.j * BS - half * 64)) : 0;
+      uint32_t sv[64];
+      tmem_ld32(tmem + lane_off + s_col(sb) + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld32(tmem + lane_off + s_col(sb) + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      if (!__all_sync(0xffffffffu, nvis >= 64)) {
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+          if (k >= nvis) sv[k] = __float_as_uint(-INFINITY);
+      }
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int k = 0; k < 64; k += 2)
+        m4[(k >> 1) & 3] = max3f(m4[(k >> 1) & 3], __uint_as_float(sv[k]), __uint_as_float(sv[k + 1]));
+      // This half's max (raw scores; scale_log2 > 0 keeps the order).
+      const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2;
+      const bool need = mt > m_ref + 8.f;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? mt : m_ref;
+        const float alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - m_new);
+        if (!first) {
+          if (!mbar_wait(bar(B_ODONE + (j - 1) % NPB), ((j - 1) / NPB) & 1)) fail();
+          __syncwarp();
+          tc_fence_after();
+          // O_h, all 128 columns of this thread's row, 16 at a time.
+#pragma unroll 1
+          for (int c0 = 0; c0 < 128; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(tmem + lane_off + o_half(half) + c0, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * (need ? alpha : 1.f));
+            tmem_st16(tmem + lane_off + o_half(half) + c0, v);
+          }
+          tmem_wait_st();
+        }
+        if (need) {
+          l *= alpha;
+          m_ref = m_new;
+        }
+      }
+      // Keys past the sequence's end in this block hold any bytes (unwritten tail
+      // slots): zero this half's V rows once the tile has landed, so that a weight 0
+      // cannot meet a NaN in the value product.
+      if (c.j * BS + zkey >= c.s.kvlen) {
+        const int vst = j % NV;
+        if (!mbar_wait(bar(B_VFULL + vst), (j / NV) & 1)) fail();
+        uint8_t* vrow = base + OFF_V + vst * TILE + zdh * HALF + zkey * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(vrow + q * 16) = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      tc_fence_after();
+      // p = exp2(s * scale_log2 - m_h), pairs of scores per fma.f32x2, as above.
+      const float mneg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      const uint64_t cs2 = f2pack(a.scale_log2, a.scale_log2), mn2 = f2pack(mneg, mneg);
+      float lr4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float2 t = f2unpack(ffma2(f2pack(__uint_as_float(sv[c0 + k]), __uint_as_float(sv[c0 + k + 1])),
+                                          cs2, mn2));
+          const float p0 = exp2f(t.x), p1 = exp2f(t.y);
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          pk[k / 2] = *reinterpret_cast<uint32_t*>(&h2);
+          add_bf16x2_to_f32(lr4[(k >> 1) & 1], lr4[2 + ((k >> 1) & 1)], pk[k / 2]);
+        }
+        tmem_st16(tmem + lane_off + p_col(sb, half) + c0 / 2, pk);
+      }
+      l += (lr4[0] + lr4[1]) + (lr4[2] + lr4[3]);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(B_PFULL + sb * 2 + half));
+      pf_next(c, a);
+      if (j + 1 < ntiles) blk_next = __ldg(a.block_table + (int64_t)c.b * a.max_blocks + c.j);
+    }
+    if (!aborted && !finalize(ntiles - 1)) fail();
   } else if (ntiles > 0 && warp >= 4) {
     // ------------------------------------------------------------ softmax / epilogue
     // Two warps per TMEM lane quarter: warp w handles rows quarter*32 + lane and
