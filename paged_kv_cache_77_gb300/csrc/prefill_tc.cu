@@ -135,16 +135,17 @@ enum {
   B_XCH = B_OFREE + NOB,     // split: per lane quarter, the halves' end-of-unit exchange
   B_COUNT = B_XCH + (kSplit ? 4 : 0)
 };
-constexpr int OFF_XCH = OFF_BAR + B_COUNT * 8;      // float [2 halves][128 rows]
-constexpr int OFF_AFL = OFF_XCH + 2 * 128 * 4;      // int [2 halves][4 quarters] abort votes
+constexpr int OFF_XCH = OFF_BAR + B_COUNT * 8;      // float [2 halves][128 rows], the halves' exchange
+constexpr int OFF_AFL = OFF_XCH + 2 * 128 * 4;      // int [2 halves][4 quarters] abort votes (unsplit)
 constexpr int OFF_MISC = OFF_AFL + 2 * 4 * 4;
 constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 constexpr uint32_t TMEM_COLS = 512;
 // Tensor memory (512 columns): S and P buffers as above (P holds 128 bf16 weights
-// packed in pairs in 64 columns), then NOB O buffers: a unit accumulates into the O
-// buffer after its predecessor's, which its first value product waits for until that
-// one is read out.
+// packed in pairs in 64 columns), then the O accumulators: with split halves the two
+// O_h of 128 columns each, else NOB O buffers. A unit accumulates into the O
+// buffer(s) after its predecessor's, which its first value product waits for until
+// they are read out.
 __device__ __forceinline__ uint32_t s_col(int b) { return kAlias ? b * 128 : 0; }
 // P of buffer b; aliased, half h of a row writes its 32 columns at the start of the
 // 64 S columns it read (the value product's K-steps 4h..4h+3 read them there).
