@@ -1,4 +1,4 @@
-"""The prefill kernel's split-halves softmax rule, restated in float64 and checked
+"""The attention kernels' softmax rules, restated in float64 and checked
 against the oracle's attention (CPU).
 
 The prefill kernel hands the two softmax warps of a query row the two key halves of
@@ -10,10 +10,15 @@ the end of the row's unit:
     M = max(m_0, m_1),  a_h = 2^(m_h - M)
     o = (a_0 O_0 + a_1 O_1) / (a_0 l_0 + a_1 l_1),  lse = ln 2 * (M + log2(a_0 l_0 + a_1 l_1))
 
-The emulation below takes those steps in float64 (no bf16 rounding of the weights), so
-it must equal softmax attention to rounding for any scores, masks and lengths. It is a
-check of the rule the kernel uses, independent of the GPU; the GPU tests compare the
-kernel itself with the oracle.
+The decode kernels cut a row's keys into split-K pieces at tile boundaries (a CTA's
+range of tiles). Each piece runs the same lazy running max over its 128-key tiles and
+leaves a normalised partial output and its log2-sum-exp. The merge weighs the pieces by
+2^(lse_i - max) (the split merge of the hot path).
+
+The emulations below take those steps in float64 (no bf16 rounding of the weights), so
+they must equal softmax attention to rounding for any scores, masks, lengths and cuts.
+They check the rules the kernels use, independent of the GPU; the GPU tests compare
+the kernels themselves with the oracle.
 """
 import math
 
@@ -114,3 +119,51 @@ def test_dropping_the_rescale_is_caught():
     o_bad, _ = split_rule(z / LN2, V, rescale=False)
     o_ref, _, _ = ref.softmax_combine(z, V, visible)
     assert np.abs(o_bad - o_ref).max() > 1e-3
+
+
+def piece_rule(z2, V, lo, hi, tile=BLOCK):
+    """One split-K piece [lo, hi) of a row as the decode kernels run it: a running max
+    over tiles raised only past +8 (log2), rescaling what was accumulated; returns the
+    piece's normalised output and log2-sum-exp (the partial the merge reads)."""
+    m, l, O = -np.inf, 0.0, np.zeros(V.shape[1])
+    for t0 in range(lo, hi, tile):
+        zz = z2[t0:min(t0 + tile, hi)]
+        mt = zz.max()
+        if mt > m + 8.0:
+            alpha = 0.0 if m == -np.inf else 2.0 ** (m - mt)
+            O *= alpha
+            l *= alpha
+            m = mt
+        p = np.zeros(len(zz)) if m == -np.inf else 2.0 ** (zz - m)
+        O += p @ V[t0:t0 + len(zz)]
+        l += p.sum()
+    if l <= 0.0:
+        return np.zeros(V.shape[1]), -np.inf
+    return O / l, m + math.log2(l)
+
+
+def merge_pieces(parts):
+    """The log-sum-exp merge of (o_i, lse2_i) pieces: weights 2^(lse2_i - max)."""
+    lses = np.array([p[1] for p in parts])
+    if np.all(lses == -np.inf):
+        return np.zeros_like(parts[0][0]), -np.inf
+    mx = lses.max()
+    w = np.where(lses == -np.inf, 0.0, 2.0 ** (lses - mx))
+    o = sum(wi * p[0] for wi, p in zip(w, parts)) / w.sum()
+    return o, LN2 * (mx + math.log2(w.sum()))
+
+
+@pytest.mark.parametrize("n,cuts", [(1, []), (300, [128]), (1000, [256, 640]), (1000, [128, 256, 384, 896]),
+                                    (4097, [1024, 2048, 3072, 4096]), (700, [0, 700])])
+def test_split_k_pieces_merged_equal_softmax_attention(n, cuts):
+    # Pieces start on tile boundaries (a CTA's range is whole tiles); an empty piece
+    # contributes nothing.
+    rng = np.random.default_rng(2000 + n + len(cuts))
+    z, V, visible = _row(rng, n, True, n)
+    z2 = z / LN2
+    bounds = [0] + cuts + [n]
+    parts = [piece_rule(z2, V, a, b) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+    o, lse = merge_pieces(parts)
+    o_ref, lse_ref, _ = ref.softmax_combine(z, V, visible)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12 * max(1.0, np.abs(V).max()))
+    assert abs(lse - lse_ref) <= 1e-12 * max(1.0, abs(lse_ref))
